@@ -1,0 +1,511 @@
+"""Benchmark of the DDP Reducer gradient path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one reducer iteration of the BERT-large-shaped workload (391
+fp32 tensors, 335,141,888 elements, W = 4 replicas resident in HBM, 25 MiB
+buckets -> 37 buckets): ``begin_iteration`` then ``mark_ready`` for every
+parameter in the stored straggler ready order; each released bucket range
+is one fused launch (gather of the W replicas' per-parameter gradients,
+fp32 rank-order sum, x 1/W, bucket write, copy-back).  The bucket build is
+construction time and is not in the step.
+
+Metric: algorithmic HBM bytes per step / time, in GB/s, where the bytes are
+W*N*4 (replica reads) + N*4 (bucket write) + N*4 (copy-back write); gradient
+elements per second are W*N / time.  Inputs (5.4 GB read per step) exceed
+the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
+own independent replica of the workload (the path needs no collective on one
+GPU: "replicas only"); value = total bytes over ranks / max time over ranks.
+
+``--impl reference`` times the CPU oracle (the plain NumPy restatement of the
+same path) on a bounded sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import gen, shapes  # noqa: E402
+
+MIB = 1 << 20
+METRIC = "fused bucket-reduce HBM GB/s and % of GB300 peak; gradient elems/s at W replicas"
+KERNEL_SRC = os.path.join(ROOT, "reduction_reducer_gb300", "csrc", "ddp_kernels.cu")
+ORDER_FILE = os.path.join(ROOT, "tests", "golden", "bert_large_ready_order.txt")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def read_order(path=ORDER_FILE):
+    with open(path) as f:
+        return [int(l) for l in f if l.strip() and not l.startswith("#")]
+
+
+def view_bytes(W, N, s_in, n_out=1):
+    return W * N * s_in + N * 4 + n_out * N * 4
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms with host
+    arrival times, so samples can be matched to the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.samples = []
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.1]
+        window = "timed region"
+        if not inside:
+            inside = [s for s in self.samples if t0 - 1.0 <= s[0] <= t1 + 1.0]
+            window = "timed region +-1 s (region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "no samples"}
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------- workloads on the device
+
+class Workload:
+    """Device buffers, reducer and step function of one configuration."""
+
+    def __init__(self, name, torch, device, cap_mib=25, n_out=1, driver="hooks", layout="params"):
+        from reduction_reducer_gb300 import Reducer
+        self.torch = torch
+        spec = shapes.WORKLOADS[name]
+        self.name = name
+        self.W = spec["W"]
+        self.dtype = spec["dtype"]
+        self.s_in = 4 if self.dtype == "f32" else 2
+        self.numel = shapes.numels(spec["shapes"]())
+        self.P = len(self.numel)
+        self.N = sum(self.numel)
+        self.cap = cap_mib * MIB
+        self.n_out = n_out
+        self.driver = driver
+        self.red = Reducer(self.numel, self.dtype, self.cap)
+        self.B = self.red.B
+        if layout == "params":          # per-parameter tensors, registration order
+            offs, total = gen.packed_offsets(self.numel, 64)
+        else:                           # replicas laid out as their buckets (as-view)
+            _, boff = self.red.get_bucket_info()
+            locs = self.red.get_locators()
+            offs = [boff[b] + off for (b, _, off, _) in locs]
+            total = boff[-1]
+        self.offs, self.total = offs, total
+        self.flat = [gen.draw_flat_torch(total, r, 0, self.dtype, device) for r in range(self.W)]
+        self.grads = [[f[o:o + n] for o, n in zip(offs, self.numel)] for f in self.flat]
+        self.arena = torch.empty(self.red.arena_numel(), dtype=torch.float32, device=device)
+        if n_out:
+            out_offs, out_total = gen.packed_offsets(self.numel, 64)
+            self.out_flat = torch.empty(out_total, dtype=torch.float32, device=device)
+            outs = [self.out_flat[o:o + n] for o, n in zip(out_offs, self.numel)]
+        else:
+            self.out_flat, outs = None, None
+        self.red.bind(self.grads, self.arena, outs)
+        if spec["order"] == "straggler" and name == "bert_large" and cap_mib == 25:
+            self.order = read_order()
+        else:
+            self.order = gen.reverse_order(self.P)
+        self.bytes = view_bytes(self.W, self.N, self.s_in, n_out)
+
+    def step(self, stream):
+        red = self.red
+        if self.driver == "hooks":
+            red.begin_iteration()
+            for v in self.order:
+                red.mark_ready(v, stream)
+        else:
+            red.reduce_all(stream)
+
+    def free(self):
+        self.red.destroy()
+        self.flat = self.grads = self.arena = self.out_flat = None
+
+
+def time_steps(torch, stream, fn, steps, warmup, dist=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    return ms, t0, t1
+
+
+def traffic_for(kernel_key, alg_bytes_per_launch):
+    """DRAM bytes per launch from the committed ncu summary: the measured
+    ratio of DRAM bytes to algorithmic bytes on the captured case, scaled to
+    this launch's algorithmic bytes; None when the kernel source changed
+    since the capture."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(kernel_key)
+    if not e or e.get("kernel_sha") != kernel_hash():
+        return None
+    return e["dram_bytes_per_algorithmic_byte"] * alg_bytes_per_launch
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_gbs(target_s: float, max_buckets: int = 3):
+    """Time the CPU oracle on the first buckets of the BERT-large layout
+    (fresh NumPy draws), repeating until ``target_s`` of oracle work."""
+    from oracle.buckets import assign_buckets
+    from oracle.reduce import reduce_buckets
+    numel = shapes.numels(shapes.bert_large())
+    W = shapes.WORKLOADS["bert_large"]["W"]
+    members, locs = assign_buckets(numel, 4, 25 * MIB)
+    sub = list(range(min(max_buckets, len(members))))
+    vars_ = sorted(v for b in sub for v in members[b])
+    grads = [[None] * len(numel) for _ in range(W)]
+    for r in range(W):
+        for v in vars_:
+            grads[r][v] = np.random.default_rng(1000 + 7 * r + v).standard_normal(numel[v], dtype=np.float32) * np.float32(1e-3)
+    n_el = sum(numel[v] for v in vars_)
+    bytes_per = view_bytes(W, n_el, 4)
+    reps, t = 0, 0.0
+    while t < target_s:
+        t0 = time.perf_counter()
+        reduce_buckets(grads, members, locs, numel, buckets=sub)
+        t += time.perf_counter() - t0
+        reps += 1
+    gbs = bytes_per * reps / t / 1e9
+    sample = (f"buckets 0..{sub[-1]} of the BERT-large 25 MiB layout ({len(vars_)} tensors, "
+              f"{n_el} elements, W={W}) x {reps} repetitions, {t:.1f} s of oracle work")
+    return gbs, sample, t
+
+
+def cpu_threads_used():
+    return 1   # NumPy elementwise ufuncs run on the calling thread
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        gbs, sample, t = oracle_sample_gbs(args.ref_step_s, max_buckets=2)
+        if i >= args.warmup:
+            per_step.append((gbs, t))
+    total_t = sum(t for _, t in per_step)
+    value = statistics.median(g for g, _ in per_step)
+    numel = shapes.numels(shapes.bert_large())
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * total_t / max(1, len(per_step)), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "bert_large", "W": 4, "P": len(numel), "N": sum(numel), "cap_mib": 25,
+                   "mode": "copy-back (n_out=1)", "sample": "bounded sample, see cpu_baseline"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cpu_threads_used(),
+                         "kind": "oracle", "sample": sample,
+                         "host_cpus": os.cpu_count(), "affinity": len(os.sched_getaffinity(0))},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    peak, peak_kind = peaks()
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(device).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus) if rank == 0 else None
+    stream = torch.cuda.Stream(device=device)
+
+    wl = Workload("bert_large", torch, device, 25, n_out=1, driver="hooks")
+    with torch.cuda.stream(stream):
+        l0 = wl.red.launch_count()
+        ms, t0, t1 = time_steps(torch, stream, lambda: wl.step(stream), args.steps, args.warmup, dist)
+        launches = wl.red.launch_count() - l0
+    # the launch count per step is fixed by the ready order; l0 was taken
+    # before the warm-up steps
+    per_step_launches = launches / (args.steps + args.warmup)
+    timed_launches = int(round(per_step_launches * args.steps))
+    ms_step = ms / args.steps
+    gbs = wl.bytes / (ms_step * 1e-3) / 1e9
+    value = gbs * world
+    elems = wl.W * wl.N / (ms_step * 1e-3)
+
+    # roofline of the dominant kernel (bucket_reduce): the timed stream holds
+    # only its launches, back to back, so bytes / region time bounds the
+    # per-launch achieved bandwidth from below.
+    roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4),
+            "traffic": traffic_for("bucket_reduce", wl.bytes / max(per_step_launches, 1)),
+            "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "kernel": "bucket_reduce_kernel<float,4>", "launches_per_step": round(per_step_launches, 2),
+            "bytes_per_launch_avg": int(wl.bytes / max(per_step_launches, 1)),
+            "duration_source": "CUDA events over the timed region / launches (PDL back-to-back)",
+            "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4)}
+    if roof["traffic"] is not None:
+        roof["traffic"] = int(roof["traffic"])
+
+    extra = {}
+    if not args.no_extra:
+        extra = extra_configs(torch, device, stream, args, dist, keep=wl)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(torch, wl, stream, max(1, min(args.steps, args.e2e_steps)), dist)
+    wl.free()
+    torch.cuda.empty_cache()
+
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs_cpu, sample, _ = oracle_sample_gbs(args.cpu_s)
+        cpu = {"value": round(gbs_cpu, 3), "unit": "GB/s", "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": sample, "host_cpus": os.cpu_count(), "affinity": len(os.sched_getaffinity(0))}
+
+    if dist:
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1e-3) gradients generated on the device)",
+            "config": {"workload": "bert_large", "W": wl.W, "P": wl.P, "N": wl.N, "cap_mib": 25,
+                       "buckets": wl.B, "mode": "copy-back (n_out=1)",
+                       "driver": "begin_iteration + mark_ready over the stored straggler ready order",
+                       "bytes_per_step": wl.bytes,
+                       "l2": "no flush: each step streams 8.0 GB, inputs 5.4 GB > 129 MB L2",
+                       "parallelism": f"replicas only x{world}"},
+            "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+            "grad_elems_per_s": round(elems * world, 1),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": timed_launches * world,
+            "clocks": clocks, "per_config": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(torch, wl, stream, steps, dist):
+    """Same metric through the public API with host buffers: every step copies
+    the W replicas' gradients from pinned host memory, runs the iteration and
+    reads the averaged gradients back to pinned host memory."""
+    host_in = [torch.empty(f.numel(), dtype=f.dtype, pin_memory=True) for f in wl.flat]
+    for h, f in zip(host_in, wl.flat):
+        h.copy_(f)
+    host_out = torch.empty(wl.out_flat.numel(), dtype=torch.float32, pin_memory=True)
+    h2d = sum(f.numel() * f.element_size() for f in wl.flat)
+    d2h = host_out.numel() * 4
+
+    def one():
+        for h, f in zip(host_in, wl.flat):
+            f.copy_(h, non_blocking=True)
+        wl.step(stream)
+        host_out.copy_(wl.out_flat, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        ms, _, _ = time_steps(torch, stream, one, steps, 1, dist)
+    ms_step = ms / steps
+    return {"value": round(wl.bytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
+            "ms_per_step": round(ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "algorithmic bytes of the step / (H2D of replica gradients + iteration + D2H of averaged gradients)"}
+
+
+def extra_configs(torch, device, stream, args, dist, keep):
+    """The other configurations, each timed the same way (GB/s of its own
+    algorithmic bytes)."""
+    out = {}
+    steps, warm = max(5, min(args.steps, 50)), max(3, args.warmup)
+
+    def timed(wl, key, note):
+        with torch.cuda.stream(stream):
+            ms, _, _ = time_steps(torch, stream, lambda: wl.step(stream), steps, warm, dist)
+        t = ms / steps
+        out[key] = {"gbs": round(wl.bytes / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4),
+                    "bytes_per_step": wl.bytes, "buckets": wl.B, "W": wl.W,
+                    "grad_elems_per_s": round(wl.W * wl.N / (t * 1e-3), 1), "note": note}
+
+    # BERT-large, one persistent launch over all buckets (kernel alone)
+    keep.driver = "all"
+    timed(keep, "bert_large_reduce_all", "one reduce_all launch per step")
+    keep.driver = "hooks"
+    # BERT-large as-view: replicas laid out as buckets, no copy-back
+    wl = Workload("bert_large", torch, device, 25, n_out=0, driver="hooks", layout="buckets")
+    timed(wl, "bert_large_as_view", "gradient_as_bucket_view: W*N*4 + N*4 bytes")
+    wl.free()
+    torch.cuda.empty_cache()
+    wl = Workload("resnet50", torch, device, 25, n_out=1, driver="hooks")
+    timed(wl, "resnet50_w8", "ResNet-50 W=8 fp32, reverse order")
+    wl.free()
+    torch.cuda.empty_cache()
+    for cap in (0, 1, 5, 25, 100):
+        wl = Workload("gpt2_medium", torch, device, cap, n_out=1, driver="hooks")
+        timed(wl, f"gpt2_medium_w8_bf16_cap{cap}", f"GPT-2-medium bf16 W=8, cap {cap} MiB")
+        wl.free()
+        torch.cuda.empty_cache()
+    out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
+    return out
+
+
+def nosync_config(torch, device, stream, steps, warm, dist):
+    from reduction_reducer_gb300 import Reducer
+    numel = shapes.numels(shapes.resnet50())
+    W, K = 16, 8
+    N = sum(numel)
+    offs, total = gen.packed_offsets(numel, 64)
+    fresh = [[gen.draw_flat_torch(total, r, k, "f32", device) for r in range(W)] for k in range(K)]
+    fresh_v = [[[f[o:o + n] for o, n in zip(offs, numel)] for f in fk] for fk in fresh]
+    acc_flat = [torch.empty(total, device=device) for _ in range(W)]
+    acc = [[f[o:o + n] for o, n in zip(offs, numel)] for f in acc_flat]
+    red = Reducer(numel, "f32", 25 * MIB)
+    arena = torch.empty(red.arena_numel(), device=device)
+    out_flat = torch.empty(total, device=device)
+    red.bind(acc, arena, [out_flat[o:o + n] for o, n in zip(offs, numel)])
+    order = gen.reverse_order(len(numel))
+
+    def cycle():
+        for k in range(K):
+            red.accumulate_nosync(acc, fresh_v[k], first_step=(k == 0), stream=stream)
+        red.begin_iteration()
+        for v in order:
+            red.mark_ready(v, stream)
+
+    def acc_only():
+        red.accumulate_nosync(acc, fresh_v[1], first_step=False, stream=stream)
+
+    with torch.cuda.stream(stream):
+        ms, _, _ = time_steps(torch, stream, cycle, steps, warm, dist)
+        ms_acc, _, _ = time_steps(torch, stream, acc_only, steps, warm, dist)
+    t = ms / steps
+    cycle_bytes = 2 * W * N * 4 + (K - 1) * 3 * W * N * 4 + view_bytes(W, N, 4)
+    res = {"gbs": round(cycle_bytes / (t * 1e-3) / 1e9, 1), "ms_per_cycle": round(t, 4),
+           "bytes_per_cycle": cycle_bytes, "W": W, "K": K,
+           "accumulate_gbs": round(3 * W * N * 4 / (ms_acc / steps * 1e-3) / 1e9, 1),
+           "accumulate_ms": round(ms_acc / steps, 4),
+           "note": "K accumulate micro-steps (first one a copy) + one hook-driven reduce"}
+    red.destroy()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,186 @@
+/*
+ * ddp_reducer.h -- C ABI of the GB300 DDP Reducer gradient path.
+ *
+ * The library reproduces the gradient path of PyTorch DistributedDataParallel's
+ * Reducer as described in "PyTorch Distributed: Experiences on Accelerating Data
+ * Parallel Training" (Li et al., VLDB 2020), the "Distributed Data Parallel"
+ * notes (section "Internal Design") and "NCCL 专家课程 30: DDP Reducer、Bucket 与
+ * 计算通信重叠":
+ *   - parameters are packed into flat gradient buckets at construction time;
+ *   - during an iteration each ready gradient is copied into its bucket view
+ *     and buckets are launched strictly in index order (early ones park);
+ *   - every bucket is averaged over the W data-parallel replicas and the mean
+ *     is copied back into the parameters' gradients;
+ *   - under no_sync, gradients accumulate locally for several micro-steps.
+ *
+ * On one GPU the W replicas are W gradient sets resident in device memory, so
+ * the cross-replica reduction is arithmetic in a kernel, not communication.
+ *
+ * Conventions for every entry point
+ *   - Every call returns a status (enum ddp_status); nothing aborts or throws
+ *     across the ABI.  ddp_last_error() gives a one-line detail.
+ *   - Device pointers are plain CUDA device addresses owned by the caller;
+ *     "host array" arguments are host memory read during the call only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Kernels run asynchronously on it; results are ordered in that stream only.
+ *   - A context is not thread-safe: one thread drives it at a time.
+ *   - Element offsets and lengths are in elements, not bytes.
+ */
+#ifndef DDP_REDUCER_H
+#define DDP_REDUCER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ddp_ctx ddp_ctx;
+
+/* Gradient element type.  Buckets and copied-back gradients are always fp32;
+ * bf16 gradients are widened exactly and summed in fp32. */
+typedef enum ddp_dtype { DDP_F32 = 0, DDP_BF16 = 1 } ddp_dtype;
+
+/* Where variable v lives: bucket index, position in the bucket's push order,
+ * and the [offset, offset + length) element range inside the flat bucket
+ * ("NCCL 专家课程 30", section "Variable 到 Bucket"). */
+typedef struct ddp_locator {
+    int32_t bucket;
+    int32_t intra;
+    int64_t offset;
+    int64_t length;
+} ddp_locator;
+
+enum ddp_status {
+    DDP_OK = 0,
+    DDP_ERR_INVALID_ARG = -1,                 /* bad index, size, pointer, alignment */
+    DDP_ERR_ALREADY_READY = -2,               /* variable reported twice in one iteration */
+    DDP_ERR_OUT_OF_ORDER = -3,                /* explicit launch of a bucket that is not next */
+    DDP_ERR_PRIOR_REDUCTION_UNFINISHED = -4,  /* previous iteration left buckets unlaunched */
+    DDP_ERR_NOT_BOUND = -5,                   /* launch requested before ddp_bind */
+    DDP_ERR_CUDA = -6,                        /* a CUDA runtime call failed */
+    DDP_ERR_NO_MEMORY = -7                    /* host or library-owned device allocation failed */
+};
+
+/* ---------------------------------------------------------------- construction */
+
+/* Assign P parameters to buckets ("PyTorch Distributed", Section 3.2.2 bucketing;
+ * "NCCL 专家课程 30", section "`bucket_cap_mb` 不是张量切分器").
+ * Walk v = P-1 .. 0 (reverse registration order), append v to the open bucket,
+ * add numel[v] * sizeof(grad_dtype) bytes; close the bucket once its size is
+ * >= cap_bytes; a non-empty remainder closes last.  Tensors are never split, so
+ * a bucket may exceed the cap; cap_bytes = 0 gives one bucket per tensor.
+ *   numel      host array [P] of element counts (>= 0; 0 joins the open bucket)
+ *   P          >= 0 (P = 0 gives zero buckets)
+ *   cap_bytes  >= 0 (bucket_cap_mb * 2^20)
+ *   out        receives a new context (host memory only; no CUDA call is made)
+ * Errors: INVALID_ARG (negative sizes, NULL out, bad dtype), NO_MEMORY. */
+int ddp_build_buckets(const int64_t* numel, int32_t P, ddp_dtype grad_dtype,
+                      int64_t cap_bytes, ddp_ctx** out);
+
+/* Copy the locator table into out[P] (host array). */
+int ddp_get_locators(const ddp_ctx* ctx, ddp_locator* out);
+
+/* Number of buckets, and optionally the bucket arena layout: bucket b occupies
+ * elements [bucket_offsets[b], bucket_offsets[b+1]) of the flat fp32 arena
+ * (buckets back to back in index order, no padding).  bucket_offsets is a host
+ * array of B+1 entries or NULL. */
+int ddp_get_bucket_info(const ddp_ctx* ctx, int32_t* B, int64_t* bucket_offsets);
+
+/* Bind the W replicas' gradients and the outputs.
+ *   grads        host array [W*P]: grads[r*P + v] = device address of replica r's
+ *                gradient of v (numel[v] elements of grad_dtype, contiguous);
+ *                may be NULL for numel[v] == 0
+ *   bucket_arena device fp32 array of bucket_offsets[B] elements, 16-byte aligned;
+ *                receives every reduced bucket (the GradBucket buffer)
+ *   grad_out     host array [n_out*P] of device fp32 addresses, or NULL when
+ *                n_out == 0: grad_out[o*P + v] receives the mean gradient of v
+ *                (the copy-back).  n_out = 0 is gradient_as_bucket_view: the
+ *                caller uses arena views as the gradients and nothing is
+ *                copied back; n_out = 1 writes one shared copy; n_out = W
+ *                writes every replica's copy.
+ * Builds the device segment table (library-owned, freed by ddp_destroy or the
+ * next bind).  Synchronous.  Pointers must stay valid while bound.
+ * Errors: INVALID_ARG (W < 1, NULL pointers, misaligned arena, n_out not in
+ * {0, 1, W}), CUDA, NO_MEMORY. */
+int ddp_bind(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_arena,
+             float* const* grad_out, int32_t n_out);
+
+/* ---------------------------------------------------------------- iteration */
+
+/* Start an iteration: every bucket pending = member count, cursor = 0.
+ * Fails with PRIOR_REDUCTION_UNFINISHED if the previous iteration did not launch
+ * every bucket ("Distributed Data Parallel" notes, "When a parameter never
+ * receives a gradient"); the context is left unchanged -- call
+ * ddp_abort_iteration to discard it.  The launch calls below start an iteration
+ * implicitly when the previous one finished. */
+int ddp_begin_iteration(ddp_ctx* ctx);
+
+/* Discard an unfinished iteration (nothing is launched). */
+int ddp_abort_iteration(ddp_ctx* ctx);
+
+/* Variable `var`'s gradient is final ("NCCL 专家课程 30", section "Autograd Hook
+ * 状态机" / "Bucket 必须按序发起"): --pending of its bucket; at zero the bucket
+ * is ready; if it is the next to launch, it and every following bucket already
+ * ready go out in index order, as ONE kernel launch over that bucket range on
+ * `stream` (gather of the W replicas' gradients, fp32 mean, bucket write and
+ * copy-back); otherwise it parks.
+ *   launched    host array [B] or NULL: receives the launched bucket indices
+ *   n_launched  receives their count (may be NULL)
+ * Errors: INVALID_ARG (var out of range), ALREADY_READY, NOT_BOUND, CUDA.  On
+ * ALREADY_READY the state is unchanged. */
+int ddp_mark_ready(ddp_ctx* ctx, int32_t var, int32_t* launched, int32_t* n_launched,
+                   void* stream);
+
+/* Explicit launch of bucket `bucket`, which must be the next one (else
+ * OUT_OF_ORDER): its members count as ready, it is launched, and any parked
+ * buckets right after it follow in the same launch. */
+int ddp_reduce_bucket(ddp_ctx* ctx, int32_t bucket, void* stream);
+
+/* Launch every bucket not yet launched in this iteration, in index order, as one
+ * persistent kernel launch; the iteration is then finished. */
+int ddp_reduce_all(ddp_ctx* ctx, void* stream);
+
+/* Cursor and parked set: *next_bucket = index of the next bucket to launch
+ * (B when all are out); parked (host array [B] or NULL) receives the ready but
+ * unlaunched buckets, *n_parked their count. */
+int ddp_get_progress(const ddp_ctx* ctx, int32_t* next_bucket, int32_t* parked,
+                     int32_t* n_parked);
+
+/* ---------------------------------------------------------------- no_sync */
+
+/* One local accumulation micro-step for all W replicas ("PyTorch Distributed",
+ * Section 3.2.4; "Distributed Data Parallel" notes, "Gradient sync you can turn
+ * off"): acc[r*P+v] = g[r*P+v] when first_step != 0, else
+ * acc[r*P+v] = fl32(acc[r*P+v] + g[r*P+v]).  fp32 only; W is the bound W.
+ *   acc, g  host arrays [W*P] of device fp32 addresses (numel[v] elements each)
+ * No bucket copy and no reduction happens; the accumulated gradients are reduced
+ * by a later iteration whose bound grads are the accumulators.
+ * Errors: INVALID_ARG (bf16 context, NULL pointers), NOT_BOUND, CUDA. */
+int ddp_accumulate_nosync(ddp_ctx* ctx, void* const* acc, const void* const* g,
+                          int32_t first_step, void* stream);
+
+/* ---------------------------------------------------------------- options, info */
+
+enum ddp_option {
+    DDP_OPT_DRY_RUN = 0,          /* 1: run the state machine, launch nothing (host tests) */
+    DDP_OPT_CTAS_PER_SM = 1,      /* persistent-grid CTAs per SM; 0 = occupancy maximum */
+    DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
+    DDP_OPT_BLOCK_THREADS = 3     /* 128 or 256 (default) */
+};
+int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
+
+/* Kernel launches issued by this context since creation. */
+int ddp_get_launch_count(const ddp_ctx* ctx, int64_t* launches);
+
+const char* ddp_status_string(int status);
+/* Detail of the last failure on ctx (or of the last failed ddp_build_buckets in
+ * this thread when ctx is NULL). */
+const char* ddp_last_error(const ddp_ctx* ctx);
+
+void ddp_destroy(ddp_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DDP_REDUCER_H */

@@ -1,0 +1,74 @@
+"""ctypes declarations of the C ABI in include/ddp_reducer.h.
+
+Argument marshalling only.  Loading fails loudly when the library has not
+been built: there is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libddpreducer.so")
+
+DDP_F32, DDP_BF16 = 0, 1
+
+STATUS = {
+    0: "DDP_OK",
+    -1: "DDP_ERR_INVALID_ARG",
+    -2: "DDP_ERR_ALREADY_READY",
+    -3: "DDP_ERR_OUT_OF_ORDER",
+    -4: "DDP_ERR_PRIOR_REDUCTION_UNFINISHED",
+    -5: "DDP_ERR_NOT_BOUND",
+    -6: "DDP_ERR_CUDA",
+    -7: "DDP_ERR_NO_MEMORY",
+}
+
+OPT_DRY_RUN, OPT_CTAS_PER_SM, OPT_PDL, OPT_BLOCK_THREADS = 0, 1, 2, 3
+
+
+class Locator(C.Structure):
+    _fields_ = [("bucket", C.c_int32), ("intra", C.c_int32), ("offset", C.c_int64), ("length", C.c_int64)]
+
+
+# name -> (restype, argtypes); every symbol of include/ddp_reducer.h
+SIGNATURES = {
+    "ddp_build_buckets": (C.c_int, [C.POINTER(C.c_int64), C.c_int32, C.c_int, C.c_int64, C.POINTER(C.c_void_p)]),
+    "ddp_get_locators": (C.c_int, [C.c_void_p, C.POINTER(Locator)]),
+    "ddp_get_bucket_info": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int64)]),
+    "ddp_bind": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.c_void_p, C.POINTER(C.c_void_p), C.c_int32]),
+    "ddp_begin_iteration": (C.c_int, [C.c_void_p]),
+    "ddp_abort_iteration": (C.c_int, [C.c_void_p]),
+    "ddp_mark_ready": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.c_void_p]),
+    "ddp_reduce_bucket": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p]),
+    "ddp_reduce_all": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "ddp_get_progress": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+    "ddp_accumulate_nosync": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
+    "ddp_set_option": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
+    "ddp_get_launch_count": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64)]),
+    "ddp_status_string": (C.c_char_p, [C.c_int]),
+    "ddp_last_error": (C.c_char_p, [C.c_void_p]),
+    "ddp_destroy": (None, [C.c_void_p]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load (once) and declare the library; raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or `python -m reduction_reducer_gb300.build`). There is no fallback implementation.")
+    lib = C.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

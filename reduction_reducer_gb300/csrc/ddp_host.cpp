@@ -1,0 +1,510 @@
+// Host core of the DDP Reducer gradient path: bucket builder, readiness state
+// machine, bind-time segment tables and the C ABI declared in ddp_reducer.h.
+//
+// Bucket assignment follows "NCCL 专家课程 30: DDP Reducer、Bucket 与计算通信重叠"
+// (section "`bucket_cap_mb` 不是张量切分器": whole tensors, close once the size
+// reaches the cap) and "PyTorch Distributed: Experiences on Accelerating Data
+// Parallel Training" (Section 3.2.2: reverse registration order).  The state
+// machine follows the same course page, sections "Variable 到 Bucket" and
+// "Bucket 必须按序发起" (pending counts, next-bucket cursor, parking), and the
+// prior-reduction check of "Distributed Data Parallel" notes, "When a
+// parameter never receives a gradient".
+
+#include "ddp_reducer.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "ddp_kernels.h"
+
+namespace {
+
+thread_local std::string g_build_error;
+
+}  // namespace
+
+struct ddp_ctx {
+    // ---- construction (host only)
+    int32_t P = 0;
+    ddp_dtype dtype = DDP_F32;
+    int elem = 4;
+    int64_t cap = 0;
+    std::vector<int64_t> numel;
+    std::vector<std::vector<int32_t>> members;   // per bucket, push order
+    std::vector<ddp_locator> loc;                 // per variable
+    std::vector<int64_t> bucket_off;              // B+1 arena offsets
+    int32_t B = 0;
+
+    // ---- iteration state
+    bool active = false;
+    std::vector<int32_t> pending;
+    std::vector<uint8_t> ready;
+    int32_t next = 0;
+
+    // ---- binding
+    bool bound = false;
+    int W = 0;
+    int n_out = 0;
+    int device = -1;
+    float* arena = nullptr;
+    float inv_w = 1.0f;
+    void* dev_table = nullptr;
+    ddpk::SegTable tab{};
+    std::vector<int32_t> bucket_seg;              // B+1 segment ranges
+
+    // ---- options and counters
+    bool dry = false;
+    bool pdl = true;
+    int opt_ctas = 0;
+    int opt_block = 256;
+    ddpk::LaunchCfg cfg{};
+    int acc_ctas = 1;
+    int64_t launches = 0;
+    std::string err;
+};
+
+namespace {
+
+int fail(ddp_ctx* c, int status, const std::string& msg) {
+    if (c) c->err = msg;
+    return status;
+}
+
+int cuda_fail(ddp_ctx* c, cudaError_t e, const char* where) {
+    std::string m = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return fail(c, DDP_ERR_CUDA, m);
+}
+
+void reset_iteration(ddp_ctx* c) {
+    c->pending.assign(c->B, 0);
+    for (int32_t b = 0; b < c->B; ++b) c->pending[b] = static_cast<int32_t>(c->members[b].size());
+    c->ready.assign(c->P, 0);
+    c->next = 0;
+}
+
+void start_iteration(ddp_ctx* c) {
+    reset_iteration(c);
+    c->active = c->B > 0;
+}
+
+// Starts an iteration implicitly when the previous one has finished.
+void ensure_started(ddp_ctx* c) {
+    if (!c->active) start_iteration(c);
+}
+
+void free_binding(ddp_ctx* c) {
+    if (c->dev_table) cudaFree(c->dev_table);
+    c->dev_table = nullptr;
+    c->tab = ddpk::SegTable{};
+    c->bound = false;
+}
+
+int refresh_launch_cfg(ddp_ctx* c) {
+    if (!c->bound) return DDP_OK;
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaDeviceGetAttribute");
+    const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
+    c->cfg.sms = sms;
+    c->cfg.block = c->opt_block;
+    c->cfg.pdl = c->pdl;
+    c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas : ddpk::reduce_max_ctas_per_sm(in, c->W, c->opt_block);
+    c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->opt_block);
+    return DDP_OK;
+}
+
+int check_device(ddp_ctx* c) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+    if (dev != c->device)
+        return fail(c, DDP_ERR_INVALID_ARG, "current CUDA device differs from the device the context was bound on");
+    return DDP_OK;
+}
+
+// One kernel launch over buckets [b0, b1).
+int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
+    if (c->dry || b1 <= b0) return DDP_OK;
+    const long long lo = c->bucket_off[b0], hi = c->bucket_off[b1];
+    const int s0 = c->bucket_seg[b0], s1 = c->bucket_seg[b1];
+    if (hi <= lo || s1 <= s0) return DDP_OK;     // only zero-length tensors
+    int st = check_device(c);
+    if (st != DDP_OK) return st;
+    const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
+    long long n = 0;
+    cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, lo, hi, s0, s1, c->inv_w,
+                                        c->cfg, static_cast<cudaStream_t>(stream), &n);
+    c->launches += n;
+    if (e != cudaSuccess) return cuda_fail(c, e, "bucket reduce launch");
+    return DDP_OK;
+}
+
+// In-order release starting at the cursor: one launch for the whole run of
+// consecutive complete buckets.
+int release(ddp_ctx* c, int32_t* launched, int32_t* n_launched, void* stream) {
+    const int32_t first = c->next;
+    while (c->next < c->B && c->pending[c->next] == 0) ++c->next;
+    if (launched)
+        for (int32_t b = first; b < c->next; ++b) launched[b - first] = b;
+    if (n_launched) *n_launched = c->next - first;
+    if (c->next == c->B) c->active = false;
+    return launch_range(c, first, c->next, stream);
+}
+
+bool is_aligned16(uintptr_t p) { return (p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* ddp_status_string(int status) {
+    switch (status) {
+        case DDP_OK: return "DDP_OK";
+        case DDP_ERR_INVALID_ARG: return "DDP_ERR_INVALID_ARG";
+        case DDP_ERR_ALREADY_READY: return "DDP_ERR_ALREADY_READY";
+        case DDP_ERR_OUT_OF_ORDER: return "DDP_ERR_OUT_OF_ORDER";
+        case DDP_ERR_PRIOR_REDUCTION_UNFINISHED:
+            return "DDP_ERR_PRIOR_REDUCTION_UNFINISHED: Expected to have finished reduction in the prior "
+                   "iteration before starting a new one";
+        case DDP_ERR_NOT_BOUND: return "DDP_ERR_NOT_BOUND";
+        case DDP_ERR_CUDA: return "DDP_ERR_CUDA";
+        case DDP_ERR_NO_MEMORY: return "DDP_ERR_NO_MEMORY";
+        default: return "unknown ddp status";
+    }
+}
+
+const char* ddp_last_error(const ddp_ctx* ctx) {
+    return ctx ? ctx->err.c_str() : g_build_error.c_str();
+}
+
+int ddp_build_buckets(const int64_t* numel, int32_t P, ddp_dtype grad_dtype, int64_t cap_bytes,
+                      ddp_ctx** out) {
+    g_build_error.clear();
+    if (!out) { g_build_error = "out is NULL"; return DDP_ERR_INVALID_ARG; }
+    *out = nullptr;
+    if (P < 0 || (P > 0 && !numel)) { g_build_error = "bad P or numel"; return DDP_ERR_INVALID_ARG; }
+    if (grad_dtype != DDP_F32 && grad_dtype != DDP_BF16) { g_build_error = "bad dtype"; return DDP_ERR_INVALID_ARG; }
+    if (cap_bytes < 0) { g_build_error = "negative cap"; return DDP_ERR_INVALID_ARG; }
+    for (int32_t v = 0; v < P; ++v)
+        if (numel[v] < 0) { g_build_error = "negative numel at " + std::to_string(v); return DDP_ERR_INVALID_ARG; }
+
+    ddp_ctx* c = new (std::nothrow) ddp_ctx();
+    if (!c) { g_build_error = "out of host memory"; return DDP_ERR_NO_MEMORY; }
+    try {
+        c->P = P;
+        c->dtype = grad_dtype;
+        c->elem = grad_dtype == DDP_F32 ? 4 : 2;
+        c->cap = cap_bytes;
+        c->numel.assign(numel, numel + P);
+        c->loc.assign(P, ddp_locator{-1, -1, 0, 0});
+
+        // Walk the parameters in reverse registration order; close a bucket
+        // as soon as its byte size reaches the cap (tensors never split).
+        std::vector<int32_t> cur;
+        int64_t size = 0;
+        for (int32_t v = P - 1; v >= 0; --v) {
+            cur.push_back(v);
+            size += c->numel[v] * c->elem;
+            if (size >= cap_bytes) {
+                c->members.push_back(std::move(cur));
+                cur.clear();
+                size = 0;
+            }
+        }
+        if (!cur.empty()) c->members.push_back(std::move(cur));
+        c->B = static_cast<int32_t>(c->members.size());
+
+        c->bucket_off.assign(c->B + 1, 0);
+        for (int32_t b = 0; b < c->B; ++b) {
+            int64_t off = 0;
+            for (size_t i = 0; i < c->members[b].size(); ++i) {
+                const int32_t v = c->members[b][i];
+                c->loc[v] = ddp_locator{b, static_cast<int32_t>(i), off, c->numel[v]};
+                off += c->numel[v];
+            }
+            c->bucket_off[b + 1] = c->bucket_off[b] + off;
+        }
+        reset_iteration(c);
+    } catch (const std::bad_alloc&) {
+        delete c;
+        g_build_error = "out of host memory";
+        return DDP_ERR_NO_MEMORY;
+    }
+    *out = c;
+    return DDP_OK;
+}
+
+int ddp_get_locators(const ddp_ctx* ctx, ddp_locator* out) {
+    if (!ctx || (!out && ctx->P > 0)) return DDP_ERR_INVALID_ARG;
+    std::copy(ctx->loc.begin(), ctx->loc.end(), out);
+    return DDP_OK;
+}
+
+int ddp_get_bucket_info(const ddp_ctx* ctx, int32_t* B, int64_t* bucket_offsets) {
+    if (!ctx || !B) return DDP_ERR_INVALID_ARG;
+    *B = ctx->B;
+    if (bucket_offsets) std::copy(ctx->bucket_off.begin(), ctx->bucket_off.end(), bucket_offsets);
+    return DDP_OK;
+}
+
+int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_arena, float* const* grad_out,
+             int32_t n_out) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (W < 1) return fail(c, DDP_ERR_INVALID_ARG, "W must be >= 1");
+    if (n_out != 0 && n_out != 1 && n_out != W) return fail(c, DDP_ERR_INVALID_ARG, "n_out must be 0, 1 or W");
+    if (c->P > 0 && !grads) return fail(c, DDP_ERR_INVALID_ARG, "grads is NULL");
+    if (n_out > 0 && c->P > 0 && !grad_out) return fail(c, DDP_ERR_INVALID_ARG, "grad_out is NULL with n_out > 0");
+    const int64_t total = c->bucket_off[c->B];
+    if (total > 0 && !bucket_arena) return fail(c, DDP_ERR_INVALID_ARG, "bucket_arena is NULL");
+    if (!is_aligned16(reinterpret_cast<uintptr_t>(bucket_arena)))
+        return fail(c, DDP_ERR_INVALID_ARG, "bucket_arena must be 16-byte aligned");
+
+    // Host segment table: merge consecutive members of a bucket whose
+    // gradients (every replica) and outputs (every copy) are contiguous.
+    std::vector<int64_t> seg_off;
+    std::vector<const void*> seg_src;
+    std::vector<float*> seg_dst;
+    std::vector<int32_t> seg_vec;
+    std::vector<int32_t> bucket_seg(c->B + 1, 0);
+    std::vector<int64_t> seg_len;
+    try {
+        for (int32_t b = 0; b < c->B; ++b) {
+            bucket_seg[b] = static_cast<int32_t>(seg_off.size());
+            for (int32_t v : c->members[b]) {
+                const int64_t n = c->numel[v];
+                if (n == 0) continue;
+                const int64_t a0 = c->bucket_off[b] + c->loc[v].offset;
+                for (int r = 0; r < W; ++r)
+                    if (!grads[static_cast<int64_t>(r) * c->P + v])
+                        return fail(c, DDP_ERR_INVALID_ARG, "NULL gradient for replica " + std::to_string(r) +
+                                                                " variable " + std::to_string(v));
+                for (int o = 0; o < n_out; ++o)
+                    if (!grad_out[static_cast<int64_t>(o) * c->P + v])
+                        return fail(c, DDP_ERR_INVALID_ARG, "NULL output for copy " + std::to_string(o) +
+                                                                " variable " + std::to_string(v));
+                const size_t S = seg_off.size();
+                bool merge = static_cast<int32_t>(S) > bucket_seg[b];
+                if (merge) {
+                    const int64_t plen = seg_len[S - 1];
+                    for (int r = 0; r < W && merge; ++r) {
+                        const char* prev = static_cast<const char*>(seg_src[(S - 1) * W + r]);
+                        merge = static_cast<const char*>(grads[static_cast<int64_t>(r) * c->P + v]) == prev + plen * c->elem;
+                    }
+                    for (int o = 0; o < n_out && merge; ++o)
+                        merge = grad_out[static_cast<int64_t>(o) * c->P + v] == seg_dst[(S - 1) * n_out + o] + plen;
+                }
+                if (merge) {
+                    seg_len[S - 1] += n;
+                    continue;
+                }
+                // 128-bit path: element a of the arena is 16-byte aligned when a is
+                // a multiple of the vector width; require the same of every stream.
+                bool vec = true;
+                for (int r = 0; r < W; ++r) {
+                    const uintptr_t p = reinterpret_cast<uintptr_t>(grads[static_cast<int64_t>(r) * c->P + v]);
+                    vec = vec && is_aligned16(p - static_cast<uintptr_t>(a0 * c->elem));
+                }
+                for (int o = 0; o < n_out; ++o) {
+                    const uintptr_t p = reinterpret_cast<uintptr_t>(grad_out[static_cast<int64_t>(o) * c->P + v]);
+                    vec = vec && is_aligned16(p - static_cast<uintptr_t>(a0 * 4));
+                }
+                seg_off.push_back(a0);
+                seg_len.push_back(n);
+                for (int r = 0; r < W; ++r) seg_src.push_back(grads[static_cast<int64_t>(r) * c->P + v]);
+                for (int o = 0; o < n_out; ++o) seg_dst.push_back(grad_out[static_cast<int64_t>(o) * c->P + v]);
+                seg_vec.push_back(vec ? 1 : 0);
+            }
+        }
+        bucket_seg[c->B] = static_cast<int32_t>(seg_off.size());
+        seg_off.push_back(total);
+    } catch (const std::bad_alloc&) {
+        return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+
+    // One device block: offsets | source pointers | output pointers | flags.
+    const size_t S = seg_vec.size();
+    auto up16 = [](size_t x) { return (x + 15) / 16 * 16; };
+    const size_t b_off = up16(seg_off.size() * sizeof(int64_t));
+    const size_t b_src = up16(seg_src.size() * sizeof(void*));
+    const size_t b_dst = up16(seg_dst.size() * sizeof(float*));
+    const size_t b_vec = up16(std::max<size_t>(S, 1) * sizeof(int32_t));
+    const size_t bytes = b_off + b_src + b_dst + b_vec;
+    std::vector<unsigned char> host(bytes, 0);
+    std::memcpy(host.data(), seg_off.data(), seg_off.size() * sizeof(int64_t));
+    if (!seg_src.empty()) std::memcpy(host.data() + b_off, seg_src.data(), seg_src.size() * sizeof(void*));
+    if (!seg_dst.empty()) std::memcpy(host.data() + b_off + b_src, seg_dst.data(), seg_dst.size() * sizeof(float*));
+    if (S) std::memcpy(host.data() + b_off + b_src + b_dst, seg_vec.data(), S * sizeof(int32_t));
+
+    free_binding(c);
+    void* d = nullptr;
+    e = cudaMalloc(&d, bytes);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaMalloc(segment table)");
+    e = cudaMemcpy(d, host.data(), bytes, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(d);
+        return cuda_fail(c, e, "cudaMemcpy(segment table)");
+    }
+    auto* base = static_cast<unsigned char*>(d);
+    c->dev_table = d;
+    c->tab.seg_off = reinterpret_cast<const long long*>(base);
+    c->tab.seg_src = reinterpret_cast<const void* const*>(base + b_off);
+    c->tab.seg_dst = reinterpret_cast<float* const*>(base + b_off + b_src);
+    c->tab.seg_vec = reinterpret_cast<const int*>(base + b_off + b_src + b_dst);
+    c->bucket_seg = std::move(bucket_seg);
+    c->W = W;
+    c->n_out = n_out;
+    c->arena = bucket_arena;
+    c->device = dev;
+    c->inv_w = 1.0f / static_cast<float>(W);   // correctly rounded fp32 quotient
+    c->bound = true;
+    return refresh_launch_cfg(c);
+}
+
+int ddp_begin_iteration(ddp_ctx* c) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (c->active)
+        return fail(c, DDP_ERR_PRIOR_REDUCTION_UNFINISHED,
+                    "Expected to have finished reduction in the prior iteration before starting a new one: "
+                    "bucket " + std::to_string(c->next) + " of " + std::to_string(c->B) + " never launched");
+    start_iteration(c);
+    return DDP_OK;
+}
+
+int ddp_abort_iteration(ddp_ctx* c) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    reset_iteration(c);
+    c->active = false;
+    return DDP_OK;
+}
+
+int ddp_mark_ready(ddp_ctx* c, int32_t var, int32_t* launched, int32_t* n_launched, void* stream) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (n_launched) *n_launched = 0;
+    if (var < 0 || var >= c->P) return fail(c, DDP_ERR_INVALID_ARG, "variable index out of range");
+    if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "mark_ready before bind");
+    ensure_started(c);
+    if (c->ready[var]) return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready");
+    c->ready[var] = 1;
+    const int32_t b = c->loc[var].bucket;
+    if (--c->pending[b] == 0 && b == c->next) return release(c, launched, n_launched, stream);
+    return DDP_OK;
+}
+
+int ddp_reduce_bucket(ddp_ctx* c, int32_t bucket, void* stream) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (bucket < 0 || bucket >= c->B) return fail(c, DDP_ERR_INVALID_ARG, "bucket index out of range");
+    if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "reduce_bucket before bind");
+    ensure_started(c);
+    if (bucket != c->next)
+        return fail(c, DDP_ERR_OUT_OF_ORDER, "bucket " + std::to_string(bucket) + " is not next (next is " +
+                                                 std::to_string(c->next) + ")");
+    for (int32_t v : c->members[bucket]) c->ready[v] = 1;
+    c->pending[bucket] = 0;
+    return release(c, nullptr, nullptr, stream);
+}
+
+int ddp_reduce_all(ddp_ctx* c, void* stream) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "reduce_all before bind");
+    ensure_started(c);
+    const int32_t first = c->next;
+    for (int32_t b = first; b < c->B; ++b) {
+        for (int32_t v : c->members[b]) c->ready[v] = 1;
+        c->pending[b] = 0;
+    }
+    c->next = c->B;
+    c->active = false;
+    return launch_range(c, first, c->B, stream);
+}
+
+int ddp_get_progress(const ddp_ctx* c, int32_t* next_bucket, int32_t* parked, int32_t* n_parked) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (next_bucket) *next_bucket = c->next;
+    int32_t n = 0;
+    for (int32_t b = c->next; b < c->B; ++b)
+        if (c->pending[b] == 0) {
+            if (parked) parked[n] = b;
+            ++n;
+        }
+    if (n_parked) *n_parked = n;
+    return DDP_OK;
+}
+
+int ddp_accumulate_nosync(ddp_ctx* c, void* const* acc, const void* const* g, int32_t first_step, void* stream) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (c->dtype != DDP_F32) return fail(c, DDP_ERR_INVALID_ARG, "no_sync accumulation supports fp32 gradients only");
+    if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "accumulate_nosync before bind (W unknown)");
+    if (c->P > 0 && (!acc || !g)) return fail(c, DDP_ERR_INVALID_ARG, "acc or g is NULL");
+    std::vector<ddpk::AccPair> pairs;
+    try {
+        pairs.reserve(static_cast<size_t>(c->W) * c->P);
+        for (int r = 0; r < c->W; ++r)
+            for (int32_t v = 0; v < c->P; ++v) {
+                const int64_t i = static_cast<int64_t>(r) * c->P + v;
+                if (c->numel[v] == 0) continue;
+                if (!acc[i] || !g[i])
+                    return fail(c, DDP_ERR_INVALID_ARG, "NULL accumulator or gradient at replica " +
+                                                            std::to_string(r) + " variable " + std::to_string(v));
+                pairs.push_back(ddpk::AccPair{static_cast<const float*>(g[i]), static_cast<float*>(acc[i]), c->numel[v]});
+            }
+    } catch (const std::bad_alloc&) {
+        return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+    if (c->dry || pairs.empty()) return DDP_OK;
+    int st = check_device(c);
+    if (st != DDP_OK) return st;
+    ddpk::LaunchCfg cfg = c->cfg;
+    cfg.ctas_per_sm = c->acc_ctas;
+    long long n = 0;
+    cudaError_t e = ddpk::launch_accumulate(pairs.data(), static_cast<int>(pairs.size()), first_step ? 1 : 0, cfg,
+                                            static_cast<cudaStream_t>(stream), &n);
+    c->launches += n;
+    if (e != cudaSuccess) return cuda_fail(c, e, "accumulate launch");
+    return DDP_OK;
+}
+
+int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    switch (option) {
+        case DDP_OPT_DRY_RUN: c->dry = value != 0; return DDP_OK;
+        case DDP_OPT_CTAS_PER_SM:
+            if (value < 0 || value > 64) return fail(c, DDP_ERR_INVALID_ARG, "ctas_per_sm out of range");
+            c->opt_ctas = static_cast<int>(value);
+            return refresh_launch_cfg(c);
+        case DDP_OPT_PDL:
+            c->pdl = value != 0;
+            c->cfg.pdl = c->pdl;
+            return DDP_OK;
+        case DDP_OPT_BLOCK_THREADS:
+            if (value != 128 && value != 256)
+                return fail(c, DDP_ERR_INVALID_ARG, "block threads must be 128 or 256");
+            c->opt_block = static_cast<int>(value);
+            return refresh_launch_cfg(c);
+        default: return fail(c, DDP_ERR_INVALID_ARG, "unknown option");
+    }
+}
+
+int ddp_get_launch_count(const ddp_ctx* c, int64_t* launches) {
+    if (!c || !launches) return DDP_ERR_INVALID_ARG;
+    *launches = c->launches;
+    return DDP_OK;
+}
+
+void ddp_destroy(ddp_ctx* c) {
+    if (!c) return;
+    free_binding(c);
+    delete c;
+}
+
+}  // extern "C"

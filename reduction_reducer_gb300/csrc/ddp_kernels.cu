@@ -1,0 +1,505 @@
+// Device kernels of the DDP Reducer gradient path for sm_103a (GB300).
+//
+// bucket_reduce_kernel -- the fused bucket pass: for every element of the
+//   launched bucket range, read the W replicas' gradients straight from their
+//   per-parameter tensors (the gather into the bucket view needs no staging
+//   copy), sum them in fp32 in rank order, scale by fl32(1/W), and write the
+//   result into the bucket arena and into each copy-back output.  The
+//   operation follows the gradient path of "PyTorch Distributed: Experiences
+//   on Accelerating Data Parallel Training" (bucket copy, all-reduce to the
+//   mean, copy-back) and "Distributed Data Parallel" notes, "Backward pass";
+//   the one-GPU emulation turns the all-reduce over W ranks into arithmetic.
+//
+// accumulate_kernel -- no_sync micro-step: acc = g or acc = fl32(acc + g)
+//   ("PyTorch Distributed", Section 3.2.4, gradient accumulation).
+//
+// Both are HBM-streaming kernels (about 0.2 flop per byte): no tensor cores.
+// Design for GB300:
+//   * persistent grid: (SMs x resident CTAs) CTAs, each owning one contiguous,
+//     equal slice of the launch's flat element range, so a bucket range of any
+//     shape (one 125 MiB embedding or hundreds of 1024-element LayerNorm
+//     vectors) costs one launch and balances across all 152 SMs;
+//   * the CTA finds the segment holding its first element with a 32-way
+//     warp-ballot search over the segment offsets, then walks the segments;
+//   * 128-bit loads through the non-coherent path without L1 allocation,
+//     all W replicas x U vectors issued before the first add, and
+//     evict-first 128-bit stores: each byte crosses HBM once;
+//   * programmatic dependent launch: a launch triggers its successor at
+//     entry, so the next bucket range's CTAs are resident when this one
+//     drains; every launch still waits (griddepcontrol.wait) for its
+//     predecessor before touching memory, so stream order is preserved
+//     whatever precedes it.
+// Bit exactness: accumulate starts at x_0 (keeps -0.0), adds with __fadd_rn
+// in rank order and scales with __fmul_rn, so no FMA contraction and no
+// flush-to-zero (the build never uses fast-math).
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ddp_kernels.h"
+
+namespace ddpk {
+
+namespace {
+
+constexpr int kMaxBlock = 256;
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ float4 ld_stream(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(float* p, float4 v) {
+    __stcs(reinterpret_cast<float4*>(p), v);
+}
+
+// ------------------------------------------------------------------ element types
+
+// bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
+__device__ __forceinline__ float widen1(float x) { return x; }
+__device__ __forceinline__ float widen1(uint16_t x) {
+    return __uint_as_float(static_cast<uint32_t>(x) << 16);
+}
+
+template <typename Tin> struct Vec;
+
+template <> struct Vec<float> {
+    static constexpr int N = 4;          // elements per 16-byte load
+    using Raw = float4;
+    __device__ __forceinline__ static void unpack(const Raw& r, float (&f)[N]) {
+        f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
+    }
+};
+
+template <> struct Vec<uint16_t> {
+    static constexpr int N = 8;
+    using Raw = uint4;
+    __device__ __forceinline__ static void unpack(const Raw& r, float (&f)[N]) {
+        f[0] = __uint_as_float(r.x << 16); f[1] = __uint_as_float(r.x & 0xffff0000u);
+        f[2] = __uint_as_float(r.y << 16); f[3] = __uint_as_float(r.y & 0xffff0000u);
+        f[4] = __uint_as_float(r.z << 16); f[5] = __uint_as_float(r.z & 0xffff0000u);
+        f[6] = __uint_as_float(r.w << 16); f[7] = __uint_as_float(r.w & 0xffff0000u);
+    }
+};
+
+// ------------------------------------------------------------------ segment search
+
+// Largest s in [s0, s1) with off[s] <= x, given off[s0] <= x < off[s1].
+// 32-ary search: each round every lane tests one of 32 evenly spaced
+// candidates and a ballot picks the last one not above x.  Call with the
+// whole warp converged.
+__device__ __forceinline__ int find_segment(const long long* __restrict__ off, int s0, int s1,
+                                            long long x) {
+    const int lane = threadIdx.x & 31;
+    int lo = s0;
+    int n = s1 - s0;
+    while (n > 32) {
+        const int stride = (n + 31) >> 5;
+        const int idx = lo + lane * stride;
+        const bool le = idx < s1 && __ldg(off + idx) <= x;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        lo += (31 - __clz(m)) * stride;
+        n = min(stride, s1 - lo);
+    }
+    const int idx = lo + lane;
+    const bool le = lane < n && __ldg(off + idx) <= x;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    return lo + 31 - __clz(m);
+}
+
+// ------------------------------------------------------------------ reduce kernel
+
+struct ReduceParams {
+    const long long* seg_off;
+    const void* const* seg_src;
+    float* const* seg_dst;
+    const int* seg_vec;
+    float* arena;
+    long long base;     // start of slice 0 (lo rounded down to the vector width)
+    long long lo, hi;   // arena range of this launch
+    long long piece;    // elements per CTA, multiple of the vector width
+    int s0, s1;         // segment range of this launch
+    int W;
+    int n_out;
+    float inv_w;
+};
+
+// Scalar path for ragged heads/tails and segments whose pointers do not share
+// the arena's 16-byte phase.
+template <typename Tin>
+__device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* const* src,
+                                              float* const* dst, long long a0, long long x,
+                                              long long e, int W) {
+    for (long long a = x + threadIdx.x; a < e; a += blockDim.x) {
+        const long long j = a - a0;
+        float acc = widen1(src[0][j]);
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, widen1(src[r][j]));
+        const float m = __fmul_rn(acc, p.inv_w);
+        p.arena[a] = m;
+        for (int o = 0; o < p.n_out; ++o) dst[o][j] = m;
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void store_vec(const ReduceParams& p, float* const* dst, long long a,
+                                          long long j, const float (&m)[N]) {
+#pragma unroll
+    for (int q = 0; q < N; q += 4)
+        st_stream(p.arena + a + q, make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]));
+    for (int o = 0; o < p.n_out; ++o) {
+        float* d = dst[o] + j;
+#pragma unroll
+        for (int q = 0; q < N; q += 4)
+            st_stream(d + q, make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]));
+    }
+}
+
+// Vector body, W known at compile time: all WC x U loads in flight at once.
+template <typename Tin, int WC, int U>
+__device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Tin* const* src,
+                                                 float* const* dst, long long a0, long long kb,
+                                                 long long ke) {
+    using V = Vec<Tin>;
+    constexpr int N = V::N;
+    const Tin* s[WC];
+#pragma unroll
+    for (int r = 0; r < WC; ++r) s[r] = src[r];
+    const long long step = static_cast<long long>(blockDim.x);
+    for (long long k = kb + threadIdx.x; k < ke; k += U * step) {
+        typename V::Raw raw[U][WC];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long kk = k + u * step;
+            if (kk < ke) {
+                const long long j = kk * N - a0;
+#pragma unroll
+                for (int r = 0; r < WC; ++r)
+                    raw[u][r] = ld_stream(reinterpret_cast<const typename V::Raw*>(s[r] + j));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long kk = k + u * step;
+            if (kk < ke) {
+                float acc[N], f[N];
+                V::unpack(raw[u][0], acc);
+#pragma unroll
+                for (int r = 1; r < WC; ++r) {
+                    V::unpack(raw[u][r], f);
+#pragma unroll
+                    for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < N; ++q) acc[q] = __fmul_rn(acc[q], p.inv_w);
+                store_vec<N>(p, dst, kk * N, kk * N - a0, acc);
+            }
+        }
+    }
+}
+
+// Vector body for any W: replicas in groups of 4, still summed in rank order.
+template <typename Tin>
+__device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin* const* src,
+                                               float* const* dst, long long a0, long long kb,
+                                               long long ke, int W) {
+    using V = Vec<Tin>;
+    constexpr int N = V::N;
+    for (long long k = kb + threadIdx.x; k < ke; k += blockDim.x) {
+        const long long j = k * N - a0;
+        float acc[N], f[N];
+        V::unpack(ld_stream(reinterpret_cast<const typename V::Raw*>(src[0] + j)), acc);
+        for (int r = 1; r < W; r += 4) {
+            typename V::Raw raw[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                if (r + g < W) raw[g] = ld_stream(reinterpret_cast<const typename V::Raw*>(src[r + g] + j));
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (r + g < W) {
+                    V::unpack(raw[g], f);
+#pragma unroll
+                    for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < N; ++q) acc[q] = __fmul_rn(acc[q], p.inv_w);
+        store_vec<N>(p, dst, k * N, j, acc);
+    }
+}
+
+template <typename Tin, int WC>
+__global__ void __launch_bounds__(kMaxBlock)
+bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    pdl_trigger();
+    pdl_wait();
+    using V = Vec<Tin>;
+    constexpr int N = V::N;
+    constexpr int U = WC == 0 ? 1 : (WC >= 16 ? 1 : (16 / WC > 4 ? 4 : 16 / WC));
+    const int W = WC > 0 ? WC : p.W;
+
+    long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
+    long long y = x + p.piece;
+    x = x < p.lo ? p.lo : x;
+    y = y > p.hi ? p.hi : y;
+    if (x >= y) return;   // whole CTA leaves together
+
+    int s = find_segment(p.seg_off, p.s0, p.s1, x);
+    while (x < y) {
+        const long long a0 = __ldg(p.seg_off + s);
+        const long long a1 = __ldg(p.seg_off + s + 1);
+        const long long e = a1 < y ? a1 : y;
+        const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(s) * W;
+        float* const* dst = p.seg_dst + static_cast<long long>(s) * p.n_out;
+        const long long kb = (x + N - 1) / N;   // first whole vector
+        const long long ke = e / N;             // one past the last whole vector
+        if (__ldg(p.seg_vec + s) && kb < ke) {
+            reduce_scalar<Tin>(p, src, dst, a0, x, kb * N, W);
+            if constexpr (WC > 0)
+                reduce_vec_fixed<Tin, WC, U>(p, src, dst, a0, kb, ke);
+            else
+                reduce_vec_any<Tin>(p, src, dst, a0, kb, ke, W);
+            reduce_scalar<Tin>(p, src, dst, a0, ke * N, e, W);
+        } else {
+            reduce_scalar<Tin>(p, src, dst, a0, x, e, W);
+        }
+        x = e;
+        ++s;
+    }
+}
+
+// ------------------------------------------------------------------ accumulate kernel
+
+constexpr int kMaxAccPairs = 1000;   // 32 B each: the parameter block stays < 32 KiB
+
+struct AccPairDev {
+    const float* g;
+    float* acc;
+    long long off;   // start in the launch's flat space (multiple of 4)
+    long long len;
+};
+
+struct AccParams {
+    long long total;   // flat extent (last pair's padded end)
+    long long piece;   // elements per CTA, multiple of 4
+    int npairs;
+    int first;
+    AccPairDev pair[kMaxAccPairs];
+};
+
+__device__ __forceinline__ int find_pair(const AccParams& p, long long x) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0;
+    int n = p.npairs;
+    while (n > 32) {
+        const int stride = (n + 31) >> 5;
+        const int idx = lo + lane * stride;
+        const bool le = idx < p.npairs && p.pair[idx].off <= x;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        lo += (31 - __clz(m)) * stride;
+        n = min(stride, p.npairs - lo);
+    }
+    const int idx = lo + lane;
+    const bool le = lane < n && p.pair[idx].off <= x;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    return lo + 31 - __clz(m);
+}
+
+__global__ void __launch_bounds__(kMaxBlock)
+accumulate_kernel(const __grid_constant__ AccParams p) {
+    pdl_trigger();
+    pdl_wait();
+    long long x = static_cast<long long>(blockIdx.x) * p.piece;
+    long long y = x + p.piece;
+    y = y > p.total ? p.total : y;
+    if (x >= y) return;
+    int i = find_pair(p, x);
+    const long long step = blockDim.x;
+    while (x < y && i < p.npairs) {
+        const AccPairDev& q = p.pair[i];
+        const long long end = q.off + q.len;
+        const long long e = end < y ? end : y;
+        if (x < e) {
+            const float* g = q.g - q.off;      // indexed by flat position
+            float* acc = q.acc - q.off;
+            const bool vec = ((reinterpret_cast<uintptr_t>(q.g) | reinterpret_cast<uintptr_t>(q.acc)) & 15u) == 0;
+            long long kb = (x + 3) >> 2, ke = e >> 2;
+            if (!vec || kb >= ke) { kb = ke = 0; }
+            const long long sc_end = vec && kb < ke ? kb * 4 : e;
+            for (long long a = x + threadIdx.x; a < sc_end; a += step)
+                acc[a] = p.first ? g[a] : __fadd_rn(acc[a], g[a]);
+            for (long long k = kb + threadIdx.x; k < ke; k += 2 * step) {
+                const long long k2 = k + step;
+                const float4 g0 = ld_stream(reinterpret_cast<const float4*>(g + 4 * k));
+                float4 g1 = g0;
+                if (k2 < ke) g1 = ld_stream(reinterpret_cast<const float4*>(g + 4 * k2));
+                if (p.first) {
+                    st_stream(acc + 4 * k, g0);
+                    if (k2 < ke) st_stream(acc + 4 * k2, g1);
+                } else {
+                    const float4 c0 = __ldcs(reinterpret_cast<const float4*>(acc + 4 * k));
+                    float4 c1 = c0;
+                    if (k2 < ke) c1 = __ldcs(reinterpret_cast<const float4*>(acc + 4 * k2));
+                    st_stream(acc + 4 * k, make_float4(__fadd_rn(c0.x, g0.x), __fadd_rn(c0.y, g0.y),
+                                                       __fadd_rn(c0.z, g0.z), __fadd_rn(c0.w, g0.w)));
+                    if (k2 < ke)
+                        st_stream(acc + 4 * k2, make_float4(__fadd_rn(c1.x, g1.x), __fadd_rn(c1.y, g1.y),
+                                                            __fadd_rn(c1.z, g1.z), __fadd_rn(c1.w, g1.w)));
+                }
+            }
+            if (vec && kb < ke)
+                for (long long a = ke * 4 + threadIdx.x; a < e; a += step)
+                    acc[a] = p.first ? g[a] : __fadd_rn(acc[a], g[a]);
+        }
+        x = end > x ? end : x;
+        // skip the padding up to the next pair's start
+        ++i;
+        if (i < p.npairs && p.pair[i].off > x) x = p.pair[i].off;
+    }
+}
+
+// ------------------------------------------------------------------ launch helpers
+
+template <typename Kernel, typename Params>
+cudaError_t launch(Kernel k, int grid, int block, const Params& params, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, params);
+}
+
+using ReduceKernel = void (*)(ReduceParams);
+
+ReduceKernel pick_reduce(InType in, int W) {
+    if (in == IN_F32) {
+        switch (W) {
+            case 2: return bucket_reduce_kernel<float, 2>;
+            case 4: return bucket_reduce_kernel<float, 4>;
+            case 8: return bucket_reduce_kernel<float, 8>;
+            case 16: return bucket_reduce_kernel<float, 16>;
+            default: return bucket_reduce_kernel<float, 0>;
+        }
+    }
+    switch (W) {
+        case 2: return bucket_reduce_kernel<uint16_t, 2>;
+        case 4: return bucket_reduce_kernel<uint16_t, 4>;
+        case 8: return bucket_reduce_kernel<uint16_t, 8>;
+        case 16: return bucket_reduce_kernel<uint16_t, 16>;
+        default: return bucket_reduce_kernel<uint16_t, 0>;
+    }
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+int reduce_max_ctas_per_sm(InType in, int W, int block) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick_reduce(in, W), block, 0) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+int accumulate_max_ctas_per_sm(int block) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, accumulate_kernel, block, 0) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float* arena,
+                          long long lo, long long hi, int s0, int s1, float inv_w,
+                          const LaunchCfg& cfg, cudaStream_t stream, long long* launches) {
+    if (hi <= lo || s1 <= s0) return cudaSuccess;
+    const int N = in == IN_F32 ? 4 : 8;
+    ReduceParams p;
+    p.seg_off = t.seg_off;
+    p.seg_src = t.seg_src;
+    p.seg_dst = t.seg_dst;
+    p.seg_vec = t.seg_vec;
+    p.arena = arena;
+    p.lo = lo;
+    p.hi = hi;
+    p.base = lo - lo % N;
+    p.s0 = s0;
+    p.s1 = s1;
+    p.W = W;
+    p.n_out = n_out;
+    p.inv_w = inv_w;
+    // One slice per CTA, at least two vectors per thread so tiny ranges use
+    // few CTAs; slices are multiples of the vector width so no vector is split.
+    const long long span = hi - p.base;
+    const long long min_piece = static_cast<long long>(cfg.block) * N * 2;
+    long long grid = static_cast<long long>(cfg.sms) * cfg.ctas_per_sm;
+    grid = grid < ceil_div(span, min_piece) ? grid : ceil_div(span, min_piece);
+    if (grid < 1) grid = 1;
+    p.piece = ceil_div(ceil_div(span, grid), N) * N;
+    grid = ceil_div(span, p.piece);
+    cudaError_t err = launch(pick_reduce(in, W), static_cast<int>(grid), cfg.block, p, cfg.pdl, stream);
+    if (err == cudaSuccess && launches) ++*launches;
+    return err;
+}
+
+cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+                              cudaStream_t stream, long long* launches) {
+    thread_local AccParams p;   // ~32 KiB: kept off the stack, one per host thread
+    int i = 0;
+    while (i < n) {
+        p.npairs = 0;
+        p.first = first;
+        long long off = 0;
+        while (i < n && p.npairs < kMaxAccPairs) {
+            if (pairs[i].len > 0) {
+                AccPairDev& d = p.pair[p.npairs++];
+                d.g = pairs[i].g;
+                d.acc = pairs[i].acc;
+                d.off = off;
+                d.len = pairs[i].len;
+                off += (pairs[i].len + 3) / 4 * 4;
+            }
+            ++i;
+        }
+        if (p.npairs == 0) continue;
+        p.total = off;
+        const long long min_piece = static_cast<long long>(cfg.block) * 8;
+        long long grid = static_cast<long long>(cfg.sms) * cfg.ctas_per_sm;
+        grid = grid < ceil_div(off, min_piece) ? grid : ceil_div(off, min_piece);
+        if (grid < 1) grid = 1;
+        p.piece = ceil_div(ceil_div(off, grid), 4) * 4;
+        grid = ceil_div(off, p.piece);
+        cudaError_t err = launch(accumulate_kernel, static_cast<int>(grid), cfg.block, p, cfg.pdl, stream);
+        if (err != cudaSuccess) return err;
+        if (launches) ++*launches;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace ddpk

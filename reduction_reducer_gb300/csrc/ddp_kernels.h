@@ -1,0 +1,56 @@
+// Internal interface between the host core (ddp_host.cpp) and the device
+// kernels (ddp_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ddpk {
+
+// Device copy of the bind-time segment table.  A segment is a run of
+// variables of one bucket that is contiguous in the arena, in every replica's
+// gradients and in every copy-back output, so one pointer per stream covers
+// it.  seg_off[s] is the arena element index where segment s starts
+// (strictly increasing; seg_off[S] = arena length); seg_src[s*W + r] points
+// at replica r's first element of the segment; seg_dst[s*n_out + o] at output
+// copy o's first element; seg_vec[s] != 0 when every pointer has the same
+// 16-byte phase as the arena, so 128-bit accesses line up.
+struct SegTable {
+    const long long* seg_off;
+    const void* const* seg_src;
+    float* const* seg_dst;
+    const int* seg_vec;
+};
+
+struct LaunchCfg {
+    int sms;           // multiprocessors on the device
+    int block;         // threads per CTA
+    int ctas_per_sm;   // persistent CTAs per SM
+    bool pdl;          // programmatic dependent launch
+};
+
+enum InType { IN_F32 = 0, IN_BF16 = 1 };
+
+// Fused bucket pass over arena range [lo, hi) = segments [s0, s1):
+// gather W replicas, fp32 sum in rank order, x inv_w, write arena and copies.
+cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float* arena,
+                          long long lo, long long hi, int s0, int s1, float inv_w,
+                          const LaunchCfg& cfg, cudaStream_t stream, long long* launches);
+
+// Largest number of resident CTAs per SM of the reduce kernel for (in, W, block).
+int reduce_max_ctas_per_sm(InType in, int W, int block);
+
+// One accumulation pair: acc[0..len) (+)= g[0..len).
+struct AccPair {
+    const float* g;
+    float* acc;
+    long long len;
+};
+
+// acc = g (first != 0) or acc = fl32(acc + g) for every pair.
+cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+                              cudaStream_t stream, long long* launches);
+
+int accumulate_max_ctas_per_sm(int block);
+
+}  // namespace ddpk

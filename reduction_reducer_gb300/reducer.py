@@ -1,0 +1,203 @@
+"""Thin Python binding of the C ABI (same names as include/ddp_reducer.h).
+
+Only argument marshalling happens here: tensors become device addresses,
+streams become ``cudaStream_t`` handles, status codes become exceptions.
+Every step of the gradient path runs in the library's C++ host core and
+CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _lib
+from ._lib import DDP_BF16, DDP_F32, Locator
+
+DTYPES = {"f32": DDP_F32, "bf16": DDP_BF16}
+
+
+class DDPError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.name = _lib.STATUS.get(status, str(status))
+        super().__init__(f"{self.name}: {detail}")
+
+
+class InvalidArg(DDPError): pass
+class AlreadyReady(DDPError): pass
+class OutOfOrder(DDPError): pass
+class PriorReductionUnfinished(DDPError): pass
+class NotBound(DDPError): pass
+class CudaError(DDPError): pass
+class NoMemory(DDPError): pass
+
+
+_ERRORS = {-1: InvalidArg, -2: AlreadyReady, -3: OutOfOrder, -4: PriorReductionUnfinished,
+           -5: NotBound, -6: CudaError, -7: NoMemory}
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) if torch.cuda.is_available() else 0
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _ptr_array(ptrs):
+    arr = (C.c_void_p * max(len(ptrs), 1))()
+    for i, p in enumerate(ptrs):
+        arr[i] = p or None
+    return arr
+
+
+class Reducer:
+    """One bucketed reducer context (``ddp_ctx``)."""
+
+    def __init__(self, numel, dtype: str = "f32", cap_bytes: int = 25 << 20):
+        self.lib = _lib.load()
+        self.numel = [int(n) for n in numel]
+        self.dtype = dtype
+        arr = (C.c_int64 * max(len(self.numel), 1))(*self.numel)
+        h = C.c_void_p()
+        st = self.lib.ddp_build_buckets(arr, len(self.numel), DTYPES[dtype], int(cap_bytes), C.byref(h))
+        if st != 0:
+            raise _ERRORS.get(st, DDPError)(st, self.lib.ddp_last_error(None).decode())
+        self._h = h
+        B = C.c_int32()
+        self.lib.ddp_get_bucket_info(self._h, C.byref(B), None)
+        self.B = B.value
+        self.P = len(self.numel)
+        self._launched = (C.c_int32 * max(self.B, 1))()
+        self._keep = ()
+
+    build_buckets = classmethod(lambda cls, numel, dtype="f32", cap_bytes=25 << 20: cls(numel, dtype, cap_bytes))
+
+    # ---------------------------------------------------------------- helpers
+    def _check(self, st: int):
+        if st != 0:
+            detail = self.lib.ddp_last_error(self._h) or b""
+            raise _ERRORS.get(st, DDPError)(st, detail.decode())
+
+    # ---------------------------------------------------------------- info
+    def get_locators(self):
+        out = (Locator * max(self.P, 1))()
+        self._check(self.lib.ddp_get_locators(self._h, out))
+        return [(out[v].bucket, out[v].intra, out[v].offset, out[v].length) for v in range(self.P)]
+
+    def get_bucket_info(self):
+        B = C.c_int32()
+        offs = (C.c_int64 * (self.B + 1))()
+        self._check(self.lib.ddp_get_bucket_info(self._h, C.byref(B), offs))
+        return B.value, list(offs)
+
+    def get_members(self):
+        members = [[] for _ in range(self.B)]
+        for v, (b, intra, _, _) in enumerate(self.get_locators()):
+            members[b].append((intra, v))
+        return [[v for _, v in sorted(m)] for m in members]
+
+    def arena_numel(self) -> int:
+        return self.get_bucket_info()[1][-1]
+
+    # ---------------------------------------------------------------- bind
+    def bind(self, grads, bucket_arena, grad_out=None):
+        """grads: W lists of P tensors (or device addresses); bucket_arena: fp32
+        tensor of ``arena_numel()`` elements; grad_out: None (gradient as bucket
+        view), a list of P fp32 tensors (one shared copy) or W such lists."""
+        W = len(grads)
+        flat = []
+        want = "torch.float32" if self.dtype == "f32" else "torch.bfloat16"
+        for r in range(W):
+            if len(grads[r]) != self.P:
+                raise ValueError("each replica needs one gradient per parameter")
+            for v, t in enumerate(grads[r]):
+                if not isinstance(t, int) and t is not None:
+                    if t.numel() != self.numel[v] or not t.is_contiguous() or str(t.dtype) != want:
+                        raise ValueError(f"replica {r} gradient {v}: expected {self.numel[v]} contiguous {want}")
+                flat.append(_ptr(t))
+        if grad_out is None:
+            outs = []
+        elif len(grad_out) == self.P and (self.P == 0 or not isinstance(grad_out[0], (list, tuple))):
+            outs = [grad_out]
+        else:
+            outs = list(grad_out)
+        out_flat = []
+        for o in outs:
+            for v, t in enumerate(o):
+                if not isinstance(t, int) and t is not None:
+                    if t.numel() != self.numel[v] or not t.is_contiguous() or str(t.dtype) != "torch.float32":
+                        raise ValueError(f"output {v}: expected {self.numel[v]} contiguous fp32")
+                out_flat.append(_ptr(t))
+        if not isinstance(bucket_arena, int) and bucket_arena is not None:
+            if bucket_arena.numel() < self.arena_numel() or str(bucket_arena.dtype) != "torch.float32":
+                raise ValueError("bucket_arena too small or not fp32")
+        self._gp = _ptr_array(flat)
+        self._op = _ptr_array(out_flat) if outs else None
+        self._check(self.lib.ddp_bind(self._h, W, self._gp, _ptr(bucket_arena),
+                                      self._op, len(outs)))
+        self.W = W
+        self._keep = (grads, bucket_arena, grad_out)
+
+    # ---------------------------------------------------------------- iteration
+    def begin_iteration(self):
+        self._check(self.lib.ddp_begin_iteration(self._h))
+
+    def abort_iteration(self):
+        self._check(self.lib.ddp_abort_iteration(self._h))
+
+    def mark_ready(self, var: int, stream=None):
+        n = C.c_int32()
+        self._check(self.lib.ddp_mark_ready(self._h, int(var), self._launched, C.byref(n), _stream(stream)))
+        return [self._launched[i] for i in range(n.value)]
+
+    def reduce_bucket(self, bucket: int, stream=None):
+        self._check(self.lib.ddp_reduce_bucket(self._h, int(bucket), _stream(stream)))
+
+    def reduce_all(self, stream=None):
+        self._check(self.lib.ddp_reduce_all(self._h, _stream(stream)))
+
+    def get_progress(self):
+        nxt, n = C.c_int32(), C.c_int32()
+        parked = (C.c_int32 * max(self.B, 1))()
+        self._check(self.lib.ddp_get_progress(self._h, C.byref(nxt), parked, C.byref(n)))
+        return nxt.value, [parked[i] for i in range(n.value)]
+
+    # ---------------------------------------------------------------- no_sync
+    def accumulate_nosync(self, acc, g, first_step: bool, stream=None):
+        """acc, g: W lists of P fp32 tensors."""
+        a = _ptr_array([_ptr(t) for rep in acc for t in rep])
+        b = _ptr_array([_ptr(t) for rep in g for t in rep])
+        self._check(self.lib.ddp_accumulate_nosync(self._h, a, b, 1 if first_step else 0, _stream(stream)))
+
+    # ---------------------------------------------------------------- options
+    def set_option(self, option: int, value: int):
+        self._check(self.lib.ddp_set_option(self._h, int(option), int(value)))
+
+    def set_dry_run(self, on: bool = True):
+        self.set_option(_lib.OPT_DRY_RUN, 1 if on else 0)
+
+    def launch_count(self) -> int:
+        n = C.c_int64()
+        self._check(self.lib.ddp_get_launch_count(self._h, C.byref(n)))
+        return n.value
+
+    def destroy(self):
+        if getattr(self, "_h", None):
+            self.lib.ddp_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

@@ -1,0 +1,401 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Every comparison is bitwise (0 ULP; NaN compared as a class): the kernels
+use the oracle's summation order, so the tolerance the gradient path allows
+for a tree order (2e-7 relative per element) is not needed.
+
+* small and reduced workloads: every element of the bucket arena and of every
+  copied-back gradient against the oracle, plus guard words around them;
+* full-size workloads in the launch configuration the bench times: sampled
+  elements (random positions plus the first and last 40 elements of every
+  parameter) against the oracle computed on exactly those inputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.buckets import assign_buckets
+from oracle.nosync import accumulate_steps
+from oracle.reduce import reduce_buckets, replica_mean
+from reduction_reducer_gb300 import InvalidArg, Reducer
+from workloads import gen, shapes
+
+from gpu_util import (bits_equal, first_mismatch, host_grads, host_to_device_views, layout,
+                      run_path, sampled_check)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+GUARD = np.uint32(0x7FC0DEAD)      # a NaN payload no kernel writes
+MIB = 1 << 20
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import os
+    from reduction_reducer_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    _lib.load()
+    torch.cuda.set_device(0)
+
+
+def guarded(n, pad=64):
+    """fp32 device buffer of n elements with `pad` guard words on each side
+    (16-byte alignment preserved); returns (whole, view)."""
+    whole = torch.from_numpy(np.full(n + 2 * pad, GUARD, np.uint32).view(np.float32)).to(DEV)
+    return whole, whole[pad:pad + n]
+
+
+def guards_intact(whole, pad, n):
+    h = whole.cpu().numpy().view(np.uint32)
+    return np.all(h[:pad] == GUARD) and np.all(h[pad + n:] == GUARD)
+
+
+def make_order(kind, numel, members, seed=0):
+    if kind == "reverse":
+        return gen.reverse_order(len(numel))
+    if kind == "straggler":
+        return gen.straggler_order(members, p=0.5, seed=seed)
+    if kind == "random":
+        rng = np.random.default_rng(seed)
+        return [int(v) for v in rng.permutation(len(numel))]
+    raise ValueError(kind)
+
+
+def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_ready", odd=False,
+                 special=False, stream=None, iterations=1, out_odd=False):
+    elem = 4 if dtype == "f32" else 2
+    flats, views, offs = host_grads(numel, W, dtype, odd=odd, special=special)
+    members, locs = assign_buckets(numel, elem, cap)
+    want_arena, want_outs = reduce_buckets(views, members, locs, numel, n_out=max(n_out, 1))
+    flat_dev, grads_dev = host_to_device_views(flats, numel, offs, dtype, DEV)
+
+    red = Reducer(numel, dtype, cap)
+    N = red.arena_numel()
+    arena_whole, arena = guarded(N)
+    out_offs, out_total = layout(numel, 64, out_odd)
+    out_bufs, outs = [], []
+    for o in range(n_out):
+        whole, flat = guarded(out_total)
+        out_bufs.append((whole, flat))
+        outs.append([flat[off:off + n] for off, n in zip(out_offs, numel)])
+    grad_out = None if n_out == 0 else (outs[0] if n_out == 1 else outs)
+    ordr = make_order(order, numel, members)
+    for _ in range(iterations):
+        run_path(red, grads_dev, arena, grad_out, order=ordr, mode=mode, stream=stream)
+
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    assert guards_intact(arena_whole, 64, N)
+    covered = np.zeros(out_total, bool)
+    for off, n in zip(out_offs, numel):
+        covered[off:off + n] = True
+    for o in range(n_out):
+        whole, flat = out_bufs[o]
+        host = flat.cpu().numpy()
+        for v, (off, n) in enumerate(zip(out_offs, numel)):
+            assert bits_equal(host[off:off + n], want_outs[0][v]), (o, v, first_mismatch(host[off:off + n], want_outs[0][v]))
+        assert np.all(host.view(np.uint32)[~covered] == GUARD), "copy-back wrote outside the views"
+        assert guards_intact(whole, 64, out_total)
+    # the inputs are read only
+    for r in range(W):
+        back = flat_dev[r].view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else flat_dev[r].cpu().numpy()
+        assert np.array_equal(back.view(np.uint8), flats[r].view(np.uint8))
+    launches = red.launch_count()
+    red.destroy()
+    return launches
+
+
+# ---------------------------------------------------------------- the worked example
+
+def test_linear_example_bitexact_and_full_batch():
+    numel = shapes.numels(shapes.linear_10x10())
+    ex = gen.linear_example(W=2, n=20, seed=0)
+    members, locs = assign_buckets(numel, 4, 25 * MIB)
+    want_arena, want_outs = reduce_buckets(ex["grads"], members, locs, numel)
+    red = Reducer(numel, "f32", 25 * MIB)
+    grads = [[torch.from_numpy(g).to(DEV) for g in ex["grads"][r]] for r in range(2)]
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+    run_path(red, grads, arena, outs, order=[1, 0])
+    assert bits_equal(arena.cpu().numpy(), want_arena)
+    for v in range(2):
+        assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])
+    # and the mean is the full-batch gradient of the 40 x 10 batch (fp64)
+    x = np.concatenate([xi.astype(np.float64) for xi in ex["x"]])
+    out = x @ ex["weight"].astype(np.float64).T + ex["bias"].astype(np.float64)
+    dw = (2.0 / out.size) * out.T @ x
+    assert np.allclose(outs[0].cpu().numpy(), dw.reshape(-1), rtol=1e-4, atol=1e-7)
+
+
+def test_replicas_identical_after_step():
+    """Broadcast form (n_out = W): every replica receives the same bits and
+    the SGD step keeps the replicas identical."""
+    W = 4
+    numel = shapes.numels(shapes.linear_10x10())
+    ex = gen.linear_example(W=W, n=20, seed=0)
+    red = Reducer(numel, "f32", 25 * MIB)
+    grads = [[torch.from_numpy(g).to(DEV) for g in ex["grads"][r]] for r in range(W)]
+    arena = torch.empty(red.arena_numel(), device=DEV)
+    outs = [[torch.full((n,), float("nan"), device=DEV) for n in numel] for _ in range(W)]
+    run_path(red, grads, arena, outs, order=[1, 0])
+    params = [[torch.from_numpy(ex["weight"].reshape(-1).copy()).to(DEV), torch.from_numpy(ex["bias"].copy()).to(DEV)]
+              for _ in range(W)]
+    for r in range(W):
+        for p, g in zip(params[r], outs[r]):
+            p.sub_(0.001 * g)
+    for r in range(1, W):
+        for v in range(2):
+            assert torch.equal(outs[r][v].view(torch.int32), outs[0][v].view(torch.int32))
+            assert torch.equal(params[r][v].view(torch.int32), params[0][v].view(torch.int32))
+
+
+# ---------------------------------------------------------------- ragged lists, every W
+
+RAGGED = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 70001, 0, 9, 300007, 16, 31]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 16])
+def test_ragged_every_W(W, dtype):
+    full_compare(RAGGED, W, dtype, cap=64 * 1024, order="straggler", n_out=1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n_out", [0, 1, "W"])
+def test_output_modes(dtype, n_out):
+    W = 4
+    full_compare(RAGGED, W, dtype, cap=32 * 1024, order="random", n_out=W if n_out == "W" else n_out)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [2, 3, 8])
+def test_misaligned_views(W, dtype):
+    """Parameters at odd offsets of their buffers (no common 16-byte phase)
+    take the scalar path; outputs at odd offsets too."""
+    full_compare(RAGGED, W, dtype, cap=16 * 1024, order="straggler", odd=True, out_odd=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_special_values(dtype):
+    full_compare(RAGGED, 4, dtype, cap=64 * 1024, special=True)
+    full_compare(RAGGED, 3, dtype, cap=64 * 1024, special=True)
+
+
+@pytest.mark.parametrize("mode", ["reduce_all", "reduce_bucket"])
+def test_explicit_launch_modes(mode):
+    full_compare(RAGGED, 8, "f32", cap=16 * 1024, mode=mode)
+
+
+def test_repeated_iterations_and_side_stream():
+    s = torch.cuda.Stream()
+    full_compare(RAGGED, 4, "f32", cap=16 * 1024, iterations=3, stream=s)
+
+
+def test_cap_zero_per_gradient():
+    n = full_compare(RAGGED, 4, "bf16", cap=0, order="reverse")
+    # one launch per non-empty bucket: reverse order releases each at once
+    assert n == sum(1 for x in RAGGED if x > 0)
+
+
+def test_mixed_hooks_then_reduce_all():
+    numel = RAGGED
+    W = 4
+    flats, views, offs = host_grads(numel, W, "f32")
+    members, locs = assign_buckets(numel, 4, 16 * 1024)
+    want_arena, want_outs = reduce_buckets(views, members, locs, numel)
+    flat_dev, grads_dev = host_to_device_views(flats, numel, offs, "f32", DEV)
+    red = Reducer(numel, "f32", 16 * 1024)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+    red.bind(grads_dev, arena, outs)
+    red.begin_iteration()
+    for v in gen.reverse_order(len(numel))[:7]:
+        red.mark_ready(v)
+    red.reduce_all()
+    torch.cuda.synchronize()
+    assert bits_equal(arena.cpu().numpy(), want_arena)
+    for v in range(len(numel)):
+        assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])
+
+
+def test_bucket_order_contiguous_replicas_merge():
+    """Replicas laid out in bucket order (gradient-as-bucket-view style):
+    consecutive members merge into one segment per bucket."""
+    numel = RAGGED
+    W = 4
+    members, locs = assign_buckets(numel, 4, 64 * 1024)
+    lens = [sum(numel[v] for v in m) for m in members]
+    starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    offs = [int(starts[locs[v].bucket] + locs[v].offset) for v in range(len(numel))]
+    total = int(starts[-1])
+    flats = [gen.draw_flat_np(total, r) for r in range(W)]
+    views = [[f[o:o + n] for o, n in zip(offs, numel)] for f in flats]
+    want_arena, _ = reduce_buckets(views, members, locs, numel)
+    flat_dev, grads_dev = host_to_device_views(flats, numel, offs, "f32", DEV)
+    red = Reducer(numel, "f32", 64 * 1024)
+    arena = torch.full((total,), float("nan"), device=DEV)
+    run_path(red, grads_dev, arena, None, mode="reduce_all")
+    assert bits_equal(arena.cpu().numpy(), want_arena)
+
+
+def test_bind_rejects_misaligned_arena():
+    red = Reducer([8, 8], "f32", 1 << 20)
+    g = [[torch.zeros(8, device=DEV), torch.zeros(8, device=DEV)]]
+    buf = torch.zeros(20, device=DEV)
+    with pytest.raises(InvalidArg):
+        red.bind(g, buf[1:], None)
+
+
+def test_empty_and_zero_length_models():
+    red = Reducer([], "f32", 25 * MIB)
+    red.bind([[]], torch.zeros(4, device=DEV), None)
+    red.reduce_all()
+    assert red.launch_count() == 0
+    red = Reducer([0, 0, 0], "f32", 0)
+    z = torch.zeros(0, device=DEV)
+    red.bind([[z, z, z], [z, z, z]], torch.zeros(4, device=DEV), [z, z, z])
+    red.begin_iteration()
+    for v in (2, 1, 0):
+        red.mark_ready(v)
+    torch.cuda.synchronize()
+    assert red.launch_count() == 0
+
+
+# ---------------------------------------------------------------- reduced workloads, every element
+
+def test_resnet50_full_size_every_element():
+    numel = shapes.numels(shapes.resnet50())
+    full_compare(numel, 8, "f32", 25 * MIB, order="reverse", n_out=1)
+
+
+def test_bert_reduced_straggler_every_element():
+    numel = shapes.numels(shapes.bert_large(layers=3, vocab=4096))
+    full_compare(numel, 4, "f32", 2 * MIB, order="straggler", n_out=1)
+
+
+@pytest.mark.parametrize("cap_mib", [0, 1, 5, 25, 100])
+def test_gpt2_reduced_caps_every_element(cap_mib):
+    numel = shapes.numels(shapes.gpt2_medium(layers=2, vocab=3000, n_ctx=256))
+    full_compare(numel, 8, "bf16", cap_mib * MIB, order="reverse", n_out=1)
+
+
+def test_nosync_small_every_element():
+    numel = RAGGED
+    W, K = 3, 4
+    steps_np = [host_grads(numel, W, "f32", step=k)[1] for k in range(K)]
+    offs = host_grads(numel, W, "f32", step=0)[2]
+    acc_np = [accumulate_steps([steps_np[k][r] for k in range(K)]) for r in range(W)]
+    members, locs = assign_buckets(numel, 4, 64 * 1024)
+    want_arena, want_outs = reduce_buckets(acc_np, members, locs, numel)
+    dev_steps = []
+    for k in range(K):
+        fl, _, _ = host_grads(numel, W, "f32", step=k)
+        dev_steps.append(host_to_device_views(fl, numel, offs, "f32", DEV)[1])
+    acc_dev = [[torch.full((n,), float("nan"), device=DEV) for n in numel] for _ in range(W)]
+    red = Reducer(numel, "f32", 64 * 1024)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+    red.bind(acc_dev, arena, outs)
+    for k in range(K):
+        red.accumulate_nosync(acc_dev, dev_steps[k], first_step=(k == 0))
+    red.begin_iteration()
+    for v in gen.reverse_order(len(numel)):
+        red.mark_ready(v)
+    torch.cuda.synchronize()
+    for r in range(W):
+        for v in range(len(numel)):
+            assert bits_equal(acc_dev[r][v].cpu().numpy(), acc_np[r][v])
+    assert bits_equal(arena.cpu().numpy(), want_arena)
+    for v in range(len(numel)):
+        assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled
+
+def device_replicas(numel, W, dtype, step=0):
+    offs, total = gen.packed_offsets(numel, 64)
+    flat = [gen.draw_flat_torch(total, r, step, dtype, DEV) for r in range(W)]
+    views = [[f[o:o + n] for o, n in zip(offs, numel)] for f in flat]
+    return flat, views, offs
+
+
+def full_size_run(numel, W, dtype, cap, order, mode="mark_ready"):
+    flat, views, offs = device_replicas(numel, W, dtype)
+    red = Reducer(numel, dtype, cap)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    out_offs, out_total = gen.packed_offsets(numel, 64)
+    out_flat = torch.full((out_total,), float("nan"), device=DEV)
+    outs = [out_flat[o:o + n] for o, n in zip(out_offs, numel)]
+    run_path(red, views, arena, outs, order=order, mode=mode)
+    n = sampled_check(numel, dtype, W, cap, flat, offs, arena, [(out_flat, out_offs)], 1)
+    assert not torch.isnan(arena).any(), "arena not fully written"
+    red.destroy()
+    return n
+
+
+def test_bert_large_full_size_sampled():
+    import os
+    numel = shapes.numels(shapes.bert_large())
+    path = os.path.join(os.path.dirname(__file__), "golden", "bert_large_ready_order.txt")
+    order = [int(l) for l in open(path) if l.strip() and not l.startswith("#")]
+    assert full_size_run(numel, 4, "f32", 25 * MIB, order) > 100_000
+
+
+@pytest.mark.parametrize("cap_mib", [0, 1, 5, 25, 100])
+def test_gpt2_medium_full_size_sampled(cap_mib):
+    numel = shapes.numels(shapes.gpt2_medium())
+    assert full_size_run(numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel))) > 100_000
+
+
+def test_bert_large_full_size_reduce_all_sampled():
+    numel = shapes.numels(shapes.bert_large())
+    full_size_run(numel, 4, "f32", 25 * MIB, None, mode="reduce_all")
+
+
+def test_nosync_resnet50_full_size_sampled():
+    numel = shapes.numels(shapes.resnet50())
+    W, K = 16, 8
+    steps = [device_replicas(numel, W, "f32", step=k) for k in range(K)]
+    offs = steps[0][2]
+    acc_flat = [torch.full_like(steps[0][0][r], float("nan")) for r in range(W)]
+    acc = [[f[o:o + n] for o, n in zip(offs, numel)] for f in acc_flat]
+    red = Reducer(numel, "f32", 25 * MIB)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    out_flat = torch.full_like(steps[0][0][0], float("nan"))
+    outs = [out_flat[o:o + n] for o, n in zip(offs, numel)]
+    red.bind(acc, arena, outs)
+    for k in range(K):
+        red.accumulate_nosync(acc, steps[k][1], first_step=(k == 0))
+    red.begin_iteration()
+    for v in gen.reverse_order(len(numel)):
+        red.mark_ready(v)
+    torch.cuda.synchronize()
+    # oracle on sampled positions: accumulate the K draws, then the mean
+    members, locs = assign_buckets(numel, 4, 25 * MIB)
+    lens = [sum(numel[v] for v in m) for m in members]
+    starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    from gpu_util import arena_to_var, sample_positions
+    pos = sample_positions(numel, locs, starts, n_random=100_000)
+    var, j = arena_to_var(numel, locs, starts, pos)
+    idx = torch.from_numpy(np.array(offs, np.int64)[var] + j).to(DEV)
+    accs = []
+    for r in range(W):
+        per_step = [[steps[k][0][r].index_select(0, idx).cpu().numpy()] for k in range(K)]
+        accs.append(accumulate_steps(per_step)[0])
+        got_acc = acc_flat[r].index_select(0, idx).cpu().numpy()
+        assert bits_equal(got_acc, accs[r]), first_mismatch(got_acc, accs[r])
+    want = replica_mean(accs)
+    got = arena.index_select(0, torch.from_numpy(pos).to(DEV)).cpu().numpy()
+    assert bits_equal(got, want), first_mismatch(got, want)
+    got = out_flat.index_select(0, idx).cpu().numpy()
+    assert bits_equal(got, want), first_mismatch(got, want)
+
+
+def test_largest_tensor_64bit_offsets():
+    """One tensor of 2^31 + 37 bf16 elements (past 32-bit indexing) behind a
+    small one, W = 2: sampled check including both ends."""
+    numel = [1000, (1 << 31) + 37]
+    full_size_run(numel, 2, "bf16", 25 * MIB, [1, 0])

@@ -1,0 +1,187 @@
+"""Host-side checks of the C-ABI library (no GPU, no compute call).
+
+* the library loads and exports every function include/ddp_reducer.h declares;
+* the C++ bucket builder reproduces the oracle's locators bit for bit on
+  every workload and on brute-force tiny lists;
+* the C++ readiness state machine (dry-run: state only, nothing launched)
+  reproduces the oracle's launches and parked sets on every permutation of
+  tiny lists and on the stored BERT-large straggler order;
+* error codes of the failure cases the pages name.
+"""
+
+import itertools
+import os
+import re
+
+import pytest
+
+from oracle.buckets import assign_buckets
+from oracle.readiness import ReadinessOracle
+from workloads import gen, shapes
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from reduction_reducer_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from reduction_reducer_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(ddp_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    from reduction_reducer_gb300 import _lib
+    declared = header_functions()
+    assert {"ddp_build_buckets", "ddp_mark_ready", "ddp_reduce_bucket", "ddp_reduce_all",
+            "ddp_accumulate_nosync"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared <= set(_lib.SIGNATURES), declared - set(_lib.SIGNATURES)
+
+
+def _make(numel, dtype="f32", cap=25 << 20):
+    from reduction_reducer_gb300 import Reducer
+    return Reducer(numel, dtype, cap)
+
+
+WORKLOAD_CASES = [
+    ("linear", shapes.linear_10x10, "f32", 25),
+    ("resnet50", shapes.resnet50, "f32", 25),
+    ("bert_large", shapes.bert_large, "f32", 25),
+] + [(f"gpt2_medium_cap{c}", shapes.gpt2_medium, "bf16", c) for c in (0, 1, 5, 25, 100)]
+
+
+@pytest.mark.parametrize("name,fn,dtype,cap_mib", WORKLOAD_CASES, ids=[c[0] for c in WORKLOAD_CASES])
+def test_locators_match_oracle_on_workloads(lib, name, fn, dtype, cap_mib):
+    numel = shapes.numels(fn())
+    red = _make(numel, dtype, cap_mib << 20)
+    members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap_mib << 20)
+    assert red.B == len(members)
+    got = red.get_locators()
+    assert got == [(l.bucket, l.intra, l.offset, l.length) for l in locs]
+    B, offs = red.get_bucket_info()
+    lens = [sum(numel[v] for v in m) for m in members]
+    assert offs == [sum(lens[:b]) for b in range(B + 1)]
+
+
+def test_locators_match_oracle_bruteforce(lib):
+    for n in range(0, 5):
+        for numel in itertools.product([0, 1, 3, 4], repeat=n):
+            for cap in (0, 1, 4, 12, 16, 40):
+                red = _make(list(numel), "f32", cap)
+                _, locs = assign_buckets(numel, 4, cap)
+                assert red.get_locators() == [(l.bucket, l.intra, l.offset, l.length) for l in locs], (numel, cap)
+                red.destroy()
+
+
+def _run_dry(red, order):
+    red.set_dry_run(True)
+    red.begin_iteration()
+    trace = []
+    for v in order:
+        launched = red.mark_ready(v)
+        trace.append((launched, red.get_progress()[1]))
+    return trace
+
+
+def _oracle_trace(members, order):
+    sm = ReadinessOracle(members)
+    sm.begin_iteration()
+    out = []
+    for v in order:
+        launched = sm.mark_ready(v)
+        out.append((launched, sm.parked()))
+    return out
+
+
+@pytest.mark.parametrize("numel,cap", [([1] * 6, 2), ([3, 0, 2, 5, 1, 4], 3), ([1] * 6, 0), ([2, 2, 2], 100)])
+def test_state_machine_matches_oracle_all_permutations(lib, numel, cap):
+    members, _ = assign_buckets(numel, 1, cap)
+    red = _make(numel, "f32", cap * 4)      # f32: 4 bytes per element, same layout
+    assert red.get_members() == members
+    for order in itertools.permutations(range(len(numel))):
+        assert _run_dry(red, order) == _oracle_trace(members, order), order
+
+
+def test_state_machine_bert_straggler_order(lib):
+    numel = shapes.numels(shapes.bert_large())
+    with open(os.path.join(GOLDEN, "bert_large_ready_order.txt")) as f:
+        order = [int(l) for l in f if l.strip() and not l.startswith("#")]
+    red = _make(numel, "f32", 25 << 20)
+    members, _ = assign_buckets(numel, 4, 25 << 20)
+    got = _run_dry(red, order)
+    want = _oracle_trace(members, order)
+    assert got == want
+    assert any(parked for _, parked in got)           # the fixture really parks
+
+
+def test_error_codes(lib):
+    from reduction_reducer_gb300 import (AlreadyReady, InvalidArg, NotBound, OutOfOrder,
+                                         PriorReductionUnfinished, Reducer)
+    with pytest.raises(InvalidArg):
+        Reducer([3, -1], "f32", 16)
+    with pytest.raises(InvalidArg):
+        Reducer([3], "f32", -1)
+    red = _make([1, 1, 1], "f32", 4)                  # one bucket per tensor: v -> bucket 2 - v
+    with pytest.raises(NotBound):
+        red.mark_ready(0)                             # no bind and not dry
+    red.set_dry_run(True)
+    with pytest.raises(InvalidArg):
+        red.mark_ready(3)
+    red.begin_iteration()
+    assert red.mark_ready(0) == []                    # bucket 2 parks
+    with pytest.raises(AlreadyReady):
+        red.mark_ready(0)
+    with pytest.raises(OutOfOrder):
+        red.reduce_bucket(2)
+    red.mark_ready(2)                                 # bucket 0 goes
+    # variable 1 never reports: the next iteration must refuse to start
+    with pytest.raises(PriorReductionUnfinished) as ei:
+        red.begin_iteration()
+    assert "prior iteration" in str(ei.value)
+    red.abort_iteration()
+    red.begin_iteration()
+    red.reduce_bucket(0)
+    assert red.get_progress() == (1, [])
+    red.reduce_all()
+    assert red.get_progress() == (3, [])
+    red.begin_iteration()                             # previous one finished
+    with pytest.raises(InvalidArg):
+        red.set_option(3, 300)
+
+
+def test_empty_model(lib):
+    red = _make([], "f32", 25 << 20)
+    assert red.B == 0 and red.get_locators() == [] and red.get_bucket_info() == (0, [0])
+    red.set_dry_run(True)
+    red.begin_iteration()
+    red.reduce_all()
+    red.begin_iteration()
+
+
+def test_explicit_launch_matches_oracle(lib):
+    numel = [1, 1, 1, 1]
+    members, _ = assign_buckets(numel, 4, 4)
+    red = _make(numel, "f32", 4)
+    red.set_dry_run(True)
+    sm = ReadinessOracle(members)
+    red.begin_iteration(); sm.begin_iteration()
+    assert red.mark_ready(1) == sm.mark_ready(1)      # bucket 2 parks
+    red.reduce_bucket(0); sm.launch_next(0)
+    red.reduce_bucket(1); sm.launch_next(1)           # releases parked 2 too
+    assert red.get_progress() == (sm.next, sm.parked())
+    red.reduce_all(); sm.launch_rest()
+    assert red.get_progress() == (sm.next, sm.parked())
