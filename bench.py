@@ -135,7 +135,7 @@ class ClockSampler:
 class Workload:
     """Device buffers, reducer and step function of one configuration."""
 
-    def __init__(self, name, torch, device, cap_mib=25, n_out=1, driver="hooks", layout="params"):
+    def __init__(self, name, torch, device, cap_mib=25, n_out=1, driver="hooks", layout="params", layers=None):
         from reduction_reducer_gb300 import Reducer
         self.torch = torch
         spec = shapes.WORKLOADS[name]
@@ -143,7 +143,8 @@ class Workload:
         self.W = spec["W"]
         self.dtype = spec["dtype"]
         self.s_in = 4 if self.dtype == "f32" else 2
-        self.numel = shapes.numels(spec["shapes"]())
+        self.layers = layers
+        self.numel = shapes.numels(spec["shapes"]() if layers is None else spec["shapes"](layers=layers))
         self.P = len(self.numel)
         self.N = sum(self.numel)
         self.cap = cap_mib * MIB
@@ -169,7 +170,7 @@ class Workload:
         else:
             self.out_flat, outs = None, None
         self.red.bind(self.grads, self.arena, outs)
-        if spec["order"] == "straggler" and name == "bert_large" and cap_mib == 25:
+        if spec["order"] == "straggler" and name == "bert_large" and cap_mib == 25 and layers is None:
             self.order = read_order()
         else:
             self.order = gen.reverse_order(self.P)
@@ -231,20 +232,30 @@ def traffic_for(kernel_key, alg_bytes_per_launch):
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample_gbs(target_s: float, max_buckets: int = 3):
-    """Time the CPU oracle on the first buckets of the BERT-large layout
-    (fresh NumPy draws), repeating until ``target_s`` of oracle work."""
+def oracle_sample_inputs(max_buckets: int = 3):
+    """Host inputs of the CPU-oracle sample: the first buckets of the
+    BERT-large 25 MiB layout, seeded N(0, 1e-3) draws per replica."""
     from oracle.buckets import assign_buckets
-    from oracle.reduce import reduce_buckets
     numel = shapes.numels(shapes.bert_large())
     W = shapes.WORKLOADS["bert_large"]["W"]
     members, locs = assign_buckets(numel, 4, 25 * MIB)
     sub = list(range(min(max_buckets, len(members))))
     vars_ = sorted(v for b in sub for v in members[b])
+    offs, total = gen.packed_offsets([numel[v] for v in vars_])
     grads = [[None] * len(numel) for _ in range(W)]
     for r in range(W):
-        for v in vars_:
-            grads[r][v] = np.random.default_rng(1000 + 7 * r + v).standard_normal(numel[v], dtype=np.float32) * np.float32(1e-3)
+        flat = gen.draw_flat_np(total, r)
+        for v, o in zip(vars_, offs):
+            grads[r][v] = flat[o:o + numel[v]]
+    return dict(numel=numel, W=W, members=members, locs=locs, sub=sub, vars=vars_, grads=grads)
+
+
+def oracle_sample_gbs(target_s: float, max_buckets: int = 3, inputs=None):
+    """Time the CPU oracle on the sample, repeating until ``target_s`` of
+    oracle work; input generation is outside the timing."""
+    from oracle.reduce import reduce_buckets
+    d = inputs or oracle_sample_inputs(max_buckets)
+    numel, W, members, locs, sub, vars_, grads = (d[k] for k in ("numel", "W", "members", "locs", "sub", "vars", "grads"))
     n_el = sum(numel[v] for v in vars_)
     bytes_per = view_bytes(W, n_el, 4)
     reps, t = 0, 0.0
@@ -270,8 +281,9 @@ def run_reference(args):
     if rank != 0:
         return 0
     per_step = []
+    inputs = oracle_sample_inputs(max_buckets=2)
     for i in range(args.warmup + args.steps):
-        gbs, sample, t = oracle_sample_gbs(args.ref_step_s, max_buckets=2)
+        gbs, sample, t = oracle_sample_gbs(args.ref_step_s, inputs=inputs)
         if i >= args.warmup:
             per_step.append((gbs, t))
     total_t = sum(t for _, t in per_step)
@@ -315,7 +327,7 @@ def run_ours(args):
     sampler = ClockSampler(bus) if rank == 0 else None
     stream = torch.cuda.Stream(device=device)
 
-    wl = Workload("bert_large", torch, device, 25, n_out=1, driver="hooks")
+    wl = Workload("bert_large", torch, device, 25, n_out=1, driver=args.driver, layers=args.layers)
     with torch.cuda.stream(stream):
         l0 = wl.red.launch_count()
         ms, t0, t1 = time_steps(torch, stream, lambda: wl.step(stream), args.steps, args.warmup, dist)
@@ -336,7 +348,7 @@ def run_ours(args):
             "frac": round(gbs / peak, 4),
             "traffic": traffic_for("bucket_reduce", wl.bytes / max(per_step_launches, 1)),
             "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-            "kernel": "bucket_reduce_kernel<float,4>", "launches_per_step": round(per_step_launches, 2),
+            "kernel": "bucket_reduce_tma_kernel<float, 4>", "launches_per_step": round(per_step_launches, 2),
             "bytes_per_launch_avg": int(wl.bytes / max(per_step_launches, 1)),
             "duration_source": "CUDA events over the timed region / launches (PDL back-to-back)",
             "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4)}
@@ -371,9 +383,13 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded N(0,1e-3) gradients generated on the device)",
-            "config": {"workload": "bert_large", "W": wl.W, "P": wl.P, "N": wl.N, "cap_mib": 25,
+            "config": {"workload": "bert_large" if args.layers is None else f"bert_large_{args.layers}layers",
+                       "W": wl.W, "P": wl.P, "N": wl.N, "cap_mib": 25,
                        "buckets": wl.B, "mode": "copy-back (n_out=1)",
-                       "driver": "begin_iteration + mark_ready over the stored straggler ready order",
+                       "driver": ("begin_iteration + mark_ready over the stored straggler ready order"
+                                  if args.driver == "hooks" and args.layers is None else
+                                  "begin_iteration + mark_ready, reverse order" if args.driver == "hooks" else
+                                  "one reduce_all launch per step"),
                        "bytes_per_step": wl.bytes,
                        "l2": "no flush: each step streams 8.0 GB, inputs 5.4 GB > 129 MB L2",
                        "parallelism": f"replicas only x{world}"},
@@ -499,6 +515,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=None, help="smaller BERT (profiling case)")
+    ap.add_argument("--driver", default="hooks", choices=["hooks", "all"])
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     args = ap.parse_args()

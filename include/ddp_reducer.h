@@ -164,11 +164,21 @@ int ddp_accumulate_nosync(ddp_ctx* ctx, void* const* acc, const void* const* g,
 
 enum ddp_option {
     DDP_OPT_DRY_RUN = 0,          /* 1: run the state machine, launch nothing (host tests) */
-    DDP_OPT_CTAS_PER_SM = 1,      /* persistent-grid CTAs per SM; 0 = occupancy maximum */
+    DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 = occupancy maximum */
     DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
-    DDP_OPT_BLOCK_THREADS = 3     /* 128 or 256 (default) */
+    DDP_OPT_BLOCK_THREADS = 3,    /* register-streaming kernel: 128 or 256 (default) */
+    DDP_OPT_KERNEL = 4,           /* 0: register-streaming kernel, 1 (default): bulk-copy (TMA) pipeline */
+    DDP_OPT_STAGES = 5,           /* bulk-copy kernel: ring depth, 2..8 (default 3) */
+    DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB) */
+    DDP_OPT_TMA_CTAS_PER_SM = 7   /* bulk-copy kernel: CTAs per SM, 1 (default) or 2 */
 };
 int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
+
+/* Read and clear the device status word of a bound context (synchronous:
+ * waits for the device).  0 = every bounded wait inside the kernels finished
+ * normally; a nonzero code names a wait that gave up after its time limit
+ * (the results of that launch are not to be trusted). */
+int ddp_get_device_status(ddp_ctx* ctx, int32_t* status);
 
 /* Kernel launches issued by this context since creation. */
 int ddp_get_launch_count(const ddp_ctx* ctx, int64_t* launches);

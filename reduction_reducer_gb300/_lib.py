@@ -26,6 +26,8 @@ STATUS = {
 }
 
 OPT_DRY_RUN, OPT_CTAS_PER_SM, OPT_PDL, OPT_BLOCK_THREADS = 0, 1, 2, 3
+OPT_KERNEL, OPT_STAGES, OPT_STAGE_BYTES, OPT_TMA_CTAS_PER_SM = 4, 5, 6, 7
+KERNEL_LDG, KERNEL_TMA = 0, 1
 
 
 class Locator(C.Structure):
@@ -47,6 +49,7 @@ SIGNATURES = {
     "ddp_accumulate_nosync": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
     "ddp_set_option": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
     "ddp_get_launch_count": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64)]),
+    "ddp_get_device_status": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32)]),
     "ddp_status_string": (C.c_char_p, [C.c_int]),
     "ddp_last_error": (C.c_char_p, [C.c_void_p]),
     "ddp_destroy": (None, [C.c_void_p]),

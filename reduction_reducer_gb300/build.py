@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libddpreducer.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["ddp_host.cpp", "ddp_kernels.cu"]
+SOURCES = ["ddp_host.cpp", "ddp_kernels.cu", "ddp_kernels_tma.cu"]
 
 
 def nvcc() -> str:
@@ -45,22 +45,24 @@ def _run(cmd, verbose):
     return r
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), lib_path: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile and link; returns the library path.  ``extra_flags`` are passed
+    to every nvcc compile (e.g. a -D tuning constant for a variant built at
+    ``lib_path`` in ``build_dir``)."""
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     jobs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *COMMON, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         jobs.append((cmd, obj))
     with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         list(ex.map(lambda j: _run(j[0], verbose), jobs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     _run([cc, *ARCH, "-shared", "-o", tmp, *[o for _, o in jobs], "-cudart", "static",
           "-Xlinker", "-z,defs", "-lpthread", "-ldl", "-lrt"], verbose)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

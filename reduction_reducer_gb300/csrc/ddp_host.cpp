@@ -64,6 +64,12 @@ struct ddp_ctx {
     bool pdl = true;
     int opt_ctas = 0;
     int opt_block = 256;
+    // Defaults from the GB300 sweep on BERT-large W=4: the bulk-copy pipeline
+    // with 3 stages of 32 KiB, one CTA per SM.
+    int opt_kernel = ddpk::KERNEL_TMA;
+    int opt_stages = 3;
+    int opt_stage_bytes = 32 * 1024;
+    int opt_tma_ctas = 1;
     ddpk::LaunchCfg cfg{};
     int acc_ctas = 1;
     int64_t launches = 0;
@@ -116,6 +122,10 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->cfg.block = c->opt_block;
     c->cfg.pdl = c->pdl;
     c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas : ddpk::reduce_max_ctas_per_sm(in, c->W, c->opt_block);
+    c->cfg.kernel = c->opt_kernel;
+    c->cfg.stages = c->opt_stages;
+    c->cfg.stage_bytes = c->opt_stage_bytes;
+    c->cfg.tma_ctas_per_sm = c->opt_tma_ctas;
     c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->opt_block);
     return DDP_OK;
 }
@@ -339,7 +349,8 @@ int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_aren
     const size_t b_src = up16(seg_src.size() * sizeof(void*));
     const size_t b_dst = up16(seg_dst.size() * sizeof(float*));
     const size_t b_vec = up16(std::max<size_t>(S, 1) * sizeof(int32_t));
-    const size_t bytes = b_off + b_src + b_dst + b_vec;
+    const size_t b_status = 16;
+    const size_t bytes = b_off + b_src + b_dst + b_vec + b_status;
     std::vector<unsigned char> host(bytes, 0);
     std::memcpy(host.data(), seg_off.data(), seg_off.size() * sizeof(int64_t));
     if (!seg_src.empty()) std::memcpy(host.data() + b_off, seg_src.data(), seg_src.size() * sizeof(void*));
@@ -361,6 +372,7 @@ int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_aren
     c->tab.seg_src = reinterpret_cast<const void* const*>(base + b_off);
     c->tab.seg_dst = reinterpret_cast<float* const*>(base + b_off + b_src);
     c->tab.seg_vec = reinterpret_cast<const int*>(base + b_off + b_src + b_dst);
+    c->tab.status = reinterpret_cast<int*>(base + b_off + b_src + b_dst + b_vec);
     c->bucket_seg = std::move(bucket_seg);
     c->W = W;
     c->n_out = n_out;
@@ -486,6 +498,24 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             c->pdl = value != 0;
             c->cfg.pdl = c->pdl;
             return DDP_OK;
+        case DDP_OPT_KERNEL:
+            if (value != ddpk::KERNEL_LDG && value != ddpk::KERNEL_TMA)
+                return fail(c, DDP_ERR_INVALID_ARG, "kernel must be 0 (register streaming) or 1 (bulk copy)");
+            c->opt_kernel = static_cast<int>(value);
+            return refresh_launch_cfg(c);
+        case DDP_OPT_STAGES:
+            if (value < 2 || value > 8) return fail(c, DDP_ERR_INVALID_ARG, "stages must be 2..8");
+            c->opt_stages = static_cast<int>(value);
+            return refresh_launch_cfg(c);
+        case DDP_OPT_STAGE_BYTES:
+            if (value < 4096 || value > 112 * 1024)
+                return fail(c, DDP_ERR_INVALID_ARG, "stage bytes must be 4 KiB..112 KiB");
+            c->opt_stage_bytes = static_cast<int>(value);
+            return refresh_launch_cfg(c);
+        case DDP_OPT_TMA_CTAS_PER_SM:
+            if (value < 1 || value > 2) return fail(c, DDP_ERR_INVALID_ARG, "bulk-copy CTAs per SM must be 1 or 2");
+            c->opt_tma_ctas = static_cast<int>(value);
+            return refresh_launch_cfg(c);
         case DDP_OPT_BLOCK_THREADS:
             if (value != 128 && value != 256)
                 return fail(c, DDP_ERR_INVALID_ARG, "block threads must be 128 or 256");
@@ -493,6 +523,22 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             return refresh_launch_cfg(c);
         default: return fail(c, DDP_ERR_INVALID_ARG, "unknown option");
     }
+}
+
+int ddp_get_device_status(ddp_ctx* c, int32_t* status) {
+    if (!c || !status) return DDP_ERR_INVALID_ARG;
+    *status = 0;
+    if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "device status before bind");
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpy(&v, c->tab.status, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "read device status");
+    if (v != 0) {
+        const int32_t zero = 0;
+        e = cudaMemcpy(c->tab.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(c, e, "clear device status");
+    }
+    *status = v;
+    return DDP_OK;
 }
 
 int ddp_get_launch_count(const ddp_ctx* c, int64_t* launches) {

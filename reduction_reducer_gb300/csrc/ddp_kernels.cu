@@ -36,144 +36,22 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ddp_device.cuh"
 #include "ddp_kernels.h"
 
 namespace ddpk {
 
 namespace {
 
+using namespace dev;
+
 constexpr int kMaxBlock = 256;
 
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ void pdl_trigger() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ float4 ld_stream(const float4* p) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ void st_stream(float* p, float4 v) {
-    __stcs(reinterpret_cast<float4*>(p), v);
-}
-
-// ------------------------------------------------------------------ element types
-
-// bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
-__device__ __forceinline__ float widen1(float x) { return x; }
-__device__ __forceinline__ float widen1(uint16_t x) {
-    return __uint_as_float(static_cast<uint32_t>(x) << 16);
-}
-
-template <typename Tin> struct Vec;
-
-template <> struct Vec<float> {
-    static constexpr int N = 4;          // elements per 16-byte load
-    using Raw = float4;
-    __device__ __forceinline__ static void unpack(const Raw& r, float (&f)[N]) {
-        f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
-    }
-};
-
-template <> struct Vec<uint16_t> {
-    static constexpr int N = 8;
-    using Raw = uint4;
-    __device__ __forceinline__ static void unpack(const Raw& r, float (&f)[N]) {
-        f[0] = __uint_as_float(r.x << 16); f[1] = __uint_as_float(r.x & 0xffff0000u);
-        f[2] = __uint_as_float(r.y << 16); f[3] = __uint_as_float(r.y & 0xffff0000u);
-        f[4] = __uint_as_float(r.z << 16); f[5] = __uint_as_float(r.z & 0xffff0000u);
-        f[6] = __uint_as_float(r.w << 16); f[7] = __uint_as_float(r.w & 0xffff0000u);
-    }
-};
-
-// ------------------------------------------------------------------ segment search
-
-// Largest s in [s0, s1) with off[s] <= x, given off[s0] <= x < off[s1].
-// 32-ary search: each round every lane tests one of 32 evenly spaced
-// candidates and a ballot picks the last one not above x.  Call with the
-// whole warp converged.
-__device__ __forceinline__ int find_segment(const long long* __restrict__ off, int s0, int s1,
-                                            long long x) {
-    const int lane = threadIdx.x & 31;
-    int lo = s0;
-    int n = s1 - s0;
-    while (n > 32) {
-        const int stride = (n + 31) >> 5;
-        const int idx = lo + lane * stride;
-        const bool le = idx < s1 && __ldg(off + idx) <= x;
-        const unsigned m = __ballot_sync(0xffffffffu, le);
-        lo += (31 - __clz(m)) * stride;
-        n = min(stride, s1 - lo);
-    }
-    const int idx = lo + lane;
-    const bool le = lane < n && __ldg(off + idx) <= x;
-    const unsigned m = __ballot_sync(0xffffffffu, le);
-    return lo + 31 - __clz(m);
-}
-
-// ------------------------------------------------------------------ reduce kernel
-
-struct ReduceParams {
-    const long long* seg_off;
-    const void* const* seg_src;
-    float* const* seg_dst;
-    const int* seg_vec;
-    float* arena;
-    long long base;     // start of slice 0 (lo rounded down to the vector width)
-    long long lo, hi;   // arena range of this launch
-    long long piece;    // elements per CTA, multiple of the vector width
-    int s0, s1;         // segment range of this launch
-    int W;
-    int n_out;
-    float inv_w;
-};
-
-// Scalar path for ragged heads/tails and segments whose pointers do not share
-// the arena's 16-byte phase.
-template <typename Tin>
-__device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* const* src,
-                                              float* const* dst, long long a0, long long x,
-                                              long long e, int W) {
-    for (long long a = x + threadIdx.x; a < e; a += blockDim.x) {
-        const long long j = a - a0;
-        float acc = widen1(src[0][j]);
-        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, widen1(src[r][j]));
-        const float m = __fmul_rn(acc, p.inv_w);
-        p.arena[a] = m;
-        for (int o = 0; o < p.n_out; ++o) dst[o][j] = m;
-    }
-}
-
-template <int N>
-__device__ __forceinline__ void store_vec(const ReduceParams& p, float* const* dst, long long a,
-                                          long long j, const float (&m)[N]) {
-#pragma unroll
-    for (int q = 0; q < N; q += 4)
-        st_stream(p.arena + a + q, make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]));
-    for (int o = 0; o < p.n_out; ++o) {
-        float* d = dst[o] + j;
-#pragma unroll
-        for (int q = 0; q < N; q += 4)
-            st_stream(d + q, make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]));
-    }
-}
+// Loads in flight per thread in the vector body (W x U); the unroll U of the
+// fixed-W bodies is derived from it.
+#ifndef DDP_LDG_MAX_LOADS
+#define DDP_LDG_MAX_LOADS 16
+#endif
 
 // Vector body, W known at compile time: all WC x U loads in flight at once.
 template <typename Tin, int WC, int U>
@@ -256,7 +134,8 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
     pdl_wait();
     using V = Vec<Tin>;
     constexpr int N = V::N;
-    constexpr int U = WC == 0 ? 1 : (WC >= 16 ? 1 : (16 / WC > 4 ? 4 : 16 / WC));
+    constexpr int U = WC == 0 ? 1
+                      : (WC >= DDP_LDG_MAX_LOADS ? 1 : (DDP_LDG_MAX_LOADS / WC > 4 ? 4 : DDP_LDG_MAX_LOADS / WC));
     const int W = WC > 0 ? WC : p.W;
 
     long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
@@ -275,14 +154,14 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
         const long long kb = (x + N - 1) / N;   // first whole vector
         const long long ke = e / N;             // one past the last whole vector
         if (__ldg(p.seg_vec + s) && kb < ke) {
-            reduce_scalar<Tin>(p, src, dst, a0, x, kb * N, W);
+            reduce_scalar<Tin>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x);
             if constexpr (WC > 0)
                 reduce_vec_fixed<Tin, WC, U>(p, src, dst, a0, kb, ke);
             else
                 reduce_vec_any<Tin>(p, src, dst, a0, kb, ke, W);
-            reduce_scalar<Tin>(p, src, dst, a0, ke * N, e, W);
+            reduce_scalar<Tin>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x);
         } else {
-            reduce_scalar<Tin>(p, src, dst, a0, x, e, W);
+            reduce_scalar<Tin>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x);
         }
         x = e;
         ++s;
@@ -439,12 +318,15 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
                           long long lo, long long hi, int s0, int s1, float inv_w,
                           const LaunchCfg& cfg, cudaStream_t stream, long long* launches) {
     if (hi <= lo || s1 <= s0) return cudaSuccess;
+    if (cfg.kernel == KERNEL_TMA)
+        return launch_reduce_tma(t, in, W, n_out, arena, lo, hi, s0, s1, inv_w, cfg, stream, launches);
     const int N = in == IN_F32 ? 4 : 8;
-    ReduceParams p;
+    ReduceParams p = {};
     p.seg_off = t.seg_off;
     p.seg_src = t.seg_src;
     p.seg_dst = t.seg_dst;
     p.seg_vec = t.seg_vec;
+    p.status = t.status;
     p.arena = arena;
     p.lo = lo;
     p.hi = hi;

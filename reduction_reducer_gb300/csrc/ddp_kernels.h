@@ -1,5 +1,5 @@
 // Internal interface between the host core (ddp_host.cpp) and the device
-// kernels (ddp_kernels.cu).  Not part of the public ABI.
+// kernels (ddp_kernels.cu, ddp_kernels_tma.cu).  Not part of the public ABI.
 #pragma once
 
 #include <cstdint>
@@ -14,19 +14,27 @@ namespace ddpk {
 // (strictly increasing; seg_off[S] = arena length); seg_src[s*W + r] points
 // at replica r's first element of the segment; seg_dst[s*n_out + o] at output
 // copy o's first element; seg_vec[s] != 0 when every pointer has the same
-// 16-byte phase as the arena, so 128-bit accesses line up.
+// 16-byte phase as the arena, so 128-bit accesses (and bulk copies) line up.
+// status is a device word the kernels set when a bounded wait gives up.
 struct SegTable {
     const long long* seg_off;
     const void* const* seg_src;
     float* const* seg_dst;
     const int* seg_vec;
+    int* status;
 };
+
+enum KernelKind { KERNEL_LDG = 0, KERNEL_TMA = 1 };
 
 struct LaunchCfg {
     int sms;           // multiprocessors on the device
-    int block;         // threads per CTA
-    int ctas_per_sm;   // persistent CTAs per SM
+    int block;         // threads per CTA (register-streaming kernel)
+    int ctas_per_sm;   // persistent CTAs per SM (register-streaming kernel)
     bool pdl;          // programmatic dependent launch
+    int kernel;        // KernelKind
+    int stages;        // bulk-copy kernel: ring depth
+    int stage_bytes;   // bulk-copy kernel: bytes of all replicas' tiles per stage
+    int tma_ctas_per_sm;
 };
 
 enum InType { IN_F32 = 0, IN_BF16 = 1 };
@@ -37,7 +45,7 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
                           long long lo, long long hi, int s0, int s1, float inv_w,
                           const LaunchCfg& cfg, cudaStream_t stream, long long* launches);
 
-// Largest number of resident CTAs per SM of the reduce kernel for (in, W, block).
+// Largest number of resident CTAs per SM of the register-streaming kernel.
 int reduce_max_ctas_per_sm(InType in, int W, int block);
 
 // One accumulation pair: acc[0..len) (+)= g[0..len).
@@ -52,5 +60,10 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const Laun
                               cudaStream_t stream, long long* launches);
 
 int accumulate_max_ctas_per_sm(int block);
+
+// Bulk-copy (TMA) pipelined variant of launch_reduce, in ddp_kernels_tma.cu.
+cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
+                              long long lo, long long hi, int s0, int s1, float inv_w,
+                              const LaunchCfg& cfg, cudaStream_t stream, long long* launches);
 
 }  // namespace ddpk

@@ -1,0 +1,343 @@
+// Bulk-copy (TMA) pipelined variant of the fused bucket pass, sm_103a.
+//
+// Same arithmetic and outputs as bucket_reduce_kernel in ddp_kernels.cu
+// (gather of the W replicas' per-parameter gradients, fp32 rank-order sum,
+// x fl32(1/W), bucket write, copy-back), with the loads moved off the
+// register file:
+//
+//   * one producer thread per CTA walks the CTA's slice of the launch and,
+//     for every aligned chunk of a segment, issues W one-dimensional bulk
+//     copies (cp.async.bulk, global -> shared) into one stage of a ring in
+//     shared memory; an mbarrier per stage counts the landed bytes;
+//   * eight consumer warps wait for a stage, sum the W tiles from shared
+//     memory in rank order, scale, and stream the means to the arena and
+//     the copy-back outputs with 128-bit evict-first stores, then release
+//     the stage through a second mbarrier;
+//   * with 3 stages of 64 KiB each CTA keeps up to ~190 KiB of loads in
+//     flight independently of register pressure, one CTA per SM.
+//
+// Ragged heads/tails and segments whose pointers do not share the arena's
+// 16-byte phase bypass the ring (consumers load them directly).  Every
+// mbarrier wait is bounded: after ~2 s it records a code in the device
+// status word and carries on, so a fault in the pipeline can never hang the
+// GPU; the producer waits (bounded) for all of its copies to land before the
+// CTA exits.
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ddp_device.cuh"
+#include "ddp_kernels.h"
+
+namespace ddpk {
+
+namespace {
+
+using namespace dev;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
+constexpr int kMaxDynSmem = 232448;                // 227 KiB opt-in per CTA
+constexpr int kHeaderBytes = 128;                  // mbarriers, ring starts after
+
+// status codes written by bounded waits
+constexpr int kStatusEmptyTimeout = 1;
+constexpr int kStatusDrainTimeout = 2;
+constexpr int kStatusFullTimeout = 3;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; give up
+// after kWaitCycles, record `code` and mark the thread failed, after which
+// it never waits again (so a broken pipeline costs one time limit per
+// thread, not one per chunk).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, int code, bool& failed) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (failed) return false;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) {
+            atomicExch(status, code);
+            failed = true;
+            return false;
+        }
+    }
+    return true;
+}
+
+// One-dimensional bulk copy global -> shared, completion counted in bytes
+// on the mbarrier.  src and dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Walk the CTA's slice [x, y) starting in segment s.  Aligned runs of
+// vector-capable segments are cut into chunks of at most p.tile elements
+// and handed to `body`; everything else goes to `scalar`.  Producer and
+// consumers both walk, so they see the same chunk sequence.
+template <int N, typename Body, typename Scalar>
+__device__ __forceinline__ void walk(const ReduceParams& p, int s, long long x, long long y, Body&& body,
+                                     Scalar&& scalar) {
+    while (x < y) {
+        const long long a0 = __ldg(p.seg_off + s);
+        const long long a1 = __ldg(p.seg_off + s + 1);
+        const long long e = a1 < y ? a1 : y;
+        const long long xb = (x + N - 1) / N * N;
+        const long long xe = e / N * N;
+        if (__ldg(p.seg_vec + s) && xb < xe) {
+            if (x < xb) scalar(s, a0, x, xb);
+            for (long long c = xb; c < xe; c += p.tile) {
+                const long long L = xe - c < p.tile ? xe - c : p.tile;
+                body(s, a0, c, L);
+            }
+            if (xe < e) scalar(s, a0, xe, e);
+        } else {
+            scalar(s, a0, x, e);
+        }
+        x = e;
+        ++s;
+    }
+}
+
+template <typename Tin, int WC>
+__global__ void __launch_bounds__(kThreads, 1)
+bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    using V = Vec<Tin>;
+    constexpr int N = V::N;
+    const int W = WC > 0 ? WC : p.W;
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + S;
+    Tin* ring = reinterpret_cast<Tin*>(smem + kHeaderBytes);
+    const long long stage_elems = static_cast<long long>(W) * p.tile;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();
+
+    long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
+    long long y = x + p.piece;
+    x = x < p.lo ? p.lo : x;
+    y = y > p.hi ? p.hi : y;
+    if (x >= y) return;   // whole CTA, before any copy is issued
+    const int s = find_segment(p.seg_off, p.s0, p.s1, x);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane != 0) return;
+        long long k = 0;
+        bool failed = false;
+        walk<N>(
+            p, s, x, y,
+            [&](int sg, long long a0, long long c, long long L) {
+                const int st = static_cast<int>(k % S);
+                const uint32_t use = static_cast<uint32_t>(k / S);
+                if (use > 0) mbar_wait(smem_u32(empty + st), (use - 1) & 1u, p.status, kStatusEmptyTimeout, failed);
+                const uint32_t bytes = static_cast<uint32_t>(L * sizeof(Tin));
+                const uint32_t fb = smem_u32(full + st);
+                mbar_expect_tx(fb, bytes * static_cast<uint32_t>(W));
+                const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * W;
+                Tin* dst = ring + st * stage_elems;
+                for (int r = 0; r < W; ++r)
+                    bulk_g2s(smem_u32(dst + static_cast<long long>(r) * p.tile), src[r] + (c - a0), bytes, fb);
+                ++k;
+            },
+            [](int, long long, long long, long long) {});
+        // every issued copy must land before the CTA may exit
+        for (long long j = k > S ? k - S : 0; j < k; ++j)
+            mbar_wait(smem_u32(full + j % S), static_cast<uint32_t>(j / S) & 1u, p.status, kStatusDrainTimeout, failed);
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int tc = threadIdx.x - 32;
+    constexpr int nct = kConsumerWarps * 32;
+    long long k = 0;
+    bool failed = false;
+    walk<N>(
+        p, s, x, y,
+        [&](int sg, long long a0, long long c, long long L) {
+            const int st = static_cast<int>(k % S);
+            const uint32_t use = static_cast<uint32_t>(k / S);
+            mbar_wait(smem_u32(full + st), use & 1u, p.status, kStatusFullTimeout, failed);
+            const Tin* base = ring + st * stage_elems;
+            float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
+            const int nv = static_cast<int>(L / N);
+            for (int v = tc; v < nv; v += nct) {
+                float acc[N], f[N];
+                V::unpack(*reinterpret_cast<const typename V::Raw*>(base + v * N), acc);
+                if constexpr (WC > 0) {
+#pragma unroll
+                    for (int r = 1; r < WC; ++r) {
+                        V::unpack(*reinterpret_cast<const typename V::Raw*>(base + r * p.tile + v * N), f);
+#pragma unroll
+                        for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+                    }
+                } else {
+                    for (int r = 1; r < W; ++r) {
+                        V::unpack(*reinterpret_cast<const typename V::Raw*>(base + static_cast<long long>(r) * p.tile + v * N), f);
+#pragma unroll
+                        for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < N; ++q) acc[q] = __fmul_rn(acc[q], p.inv_w);
+                store_vec<N>(p, dst, c + static_cast<long long>(v) * N, c - a0 + static_cast<long long>(v) * N, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(empty + st));
+            ++k;
+        },
+        [&](int sg, long long a0, long long lo, long long hi) {
+            const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * W;
+            float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
+            reduce_scalar<Tin>(p, src, dst, a0, lo, hi, W, tc, nct);
+        });
+}
+
+using TmaKernel = void (*)(ReduceParams);
+
+TmaKernel pick_tma(InType in, int W) {
+    if (in == IN_F32) {
+        switch (W) {
+            case 2: return bucket_reduce_tma_kernel<float, 2>;
+            case 4: return bucket_reduce_tma_kernel<float, 4>;
+            case 8: return bucket_reduce_tma_kernel<float, 8>;
+            case 16: return bucket_reduce_tma_kernel<float, 16>;
+            default: return bucket_reduce_tma_kernel<float, 0>;
+        }
+    }
+    switch (W) {
+        case 2: return bucket_reduce_tma_kernel<uint16_t, 2>;
+        case 4: return bucket_reduce_tma_kernel<uint16_t, 4>;
+        case 8: return bucket_reduce_tma_kernel<uint16_t, 8>;
+        case 16: return bucket_reduce_tma_kernel<uint16_t, 16>;
+        default: return bucket_reduce_tma_kernel<uint16_t, 0>;
+    }
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// The dynamic shared-memory limit is raised once per kernel and device.
+cudaError_t ensure_smem_attr(TmaKernel k) {
+    constexpr int kSlots = 64;
+    static TmaKernel done_k[kSlots];
+    static int done_dev[kSlots];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n_done; ++i)
+        if (done_k[i] == k && done_dev[i] == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e == cudaSuccess && n_done < kSlots) {
+        done_k[n_done] = k;
+        done_dev[n_done] = dev;
+        ++n_done;
+    }
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
+                              long long lo, long long hi, int s0, int s1, float inv_w,
+                              const LaunchCfg& cfg, cudaStream_t stream, long long* launches) {
+    if (hi <= lo || s1 <= s0) return cudaSuccess;
+    const int N = in == IN_F32 ? 4 : 8;
+    const int s_in = in == IN_F32 ? 4 : 2;
+    const int stages = cfg.stages < 2 ? 2 : cfg.stages;
+    long long tile = static_cast<long long>(cfg.stage_bytes) / (static_cast<long long>(W) * s_in) / N * N;
+    if (tile < N) tile = N;
+    while (tile > N && kHeaderBytes + static_cast<long long>(stages) * W * tile * s_in > kMaxDynSmem)
+        tile -= N;
+    const long long smem = kHeaderBytes + static_cast<long long>(stages) * W * tile * s_in;
+    if (smem > kMaxDynSmem || 2 * stages * 8 > kHeaderBytes) return cudaErrorInvalidValue;
+
+    ReduceParams p = {};
+    p.seg_off = t.seg_off;
+    p.seg_src = t.seg_src;
+    p.seg_dst = t.seg_dst;
+    p.seg_vec = t.seg_vec;
+    p.status = t.status;
+    p.arena = arena;
+    p.lo = lo;
+    p.hi = hi;
+    p.base = lo - lo % N;
+    p.s0 = s0;
+    p.s1 = s1;
+    p.W = W;
+    p.n_out = n_out;
+    p.inv_w = inv_w;
+    p.stages = stages;
+    p.tile = static_cast<int>(tile);
+    const long long span = hi - p.base;
+    long long grid = static_cast<long long>(cfg.sms) * (cfg.tma_ctas_per_sm > 0 ? cfg.tma_ctas_per_sm : 1);
+    grid = grid < ceil_div(span, tile) ? grid : ceil_div(span, tile);
+    if (grid < 1) grid = 1;
+    p.piece = ceil_div(ceil_div(span, grid), N) * N;
+    grid = ceil_div(span, p.piece);
+
+    TmaKernel k = pick_tma(in, W);
+    cudaError_t e = ensure_smem_attr(k);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = static_cast<size_t>(smem);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = cfg.pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&lc, k, p);
+    if (e == cudaSuccess && launches) ++*launches;
+    return e;
+}
+
+}  // namespace ddpk

@@ -186,6 +186,12 @@ class Reducer:
     def set_dry_run(self, on: bool = True):
         self.set_option(_lib.OPT_DRY_RUN, 1 if on else 0)
 
+    def device_status(self) -> int:
+        """Read and clear the kernels' device status word (synchronous)."""
+        st = C.c_int32()
+        self._check(self.lib.ddp_get_device_status(self._h, C.byref(st)))
+        return st.value
+
     def launch_count(self) -> int:
         n = C.c_int64()
         self._check(self.lib.ddp_get_launch_count(self._h, C.byref(n)))

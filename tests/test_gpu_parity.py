@@ -18,7 +18,7 @@ import torch
 from oracle.buckets import assign_buckets
 from oracle.nosync import accumulate_steps
 from oracle.reduce import reduce_buckets, replica_mean
-from reduction_reducer_gb300 import InvalidArg, Reducer
+from reduction_reducer_gb300 import InvalidArg, Reducer, _lib
 from workloads import gen, shapes
 
 from gpu_util import (bits_equal, first_mismatch, host_grads, host_to_device_views, layout,
@@ -64,8 +64,12 @@ def make_order(kind, numel, members, seed=0):
     raise ValueError(kind)
 
 
+def set_kernel(red, kernel):
+    red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_TMA if kernel == "tma" else _lib.KERNEL_LDG)
+
+
 def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_ready", odd=False,
-                 special=False, stream=None, iterations=1, out_odd=False):
+                 special=False, stream=None, iterations=1, out_odd=False, kernel="ldg"):
     elem = 4 if dtype == "f32" else 2
     flats, views, offs = host_grads(numel, W, dtype, odd=odd, special=special)
     members, locs = assign_buckets(numel, elem, cap)
@@ -73,6 +77,7 @@ def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_re
     flat_dev, grads_dev = host_to_device_views(flats, numel, offs, dtype, DEV)
 
     red = Reducer(numel, dtype, cap)
+    set_kernel(red, kernel)
     N = red.arena_numel()
     arena_whole, arena = guarded(N)
     out_offs, out_total = layout(numel, 64, out_odd)
@@ -104,6 +109,7 @@ def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_re
         back = flat_dev[r].view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else flat_dev[r].cpu().numpy()
         assert np.array_equal(back.view(np.uint8), flats[r].view(np.uint8))
     launches = red.launch_count()
+    assert red.device_status() == 0
     red.destroy()
     return launches
 
@@ -157,41 +163,51 @@ def test_replicas_identical_after_step():
 RAGGED = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 70001, 0, 9, 300007, 16, 31]
 
 
+KERNELS = ["ldg", "tma"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 16])
-def test_ragged_every_W(W, dtype):
-    full_compare(RAGGED, W, dtype, cap=64 * 1024, order="straggler", n_out=1)
+def test_ragged_every_W(W, dtype, kernel):
+    full_compare(RAGGED, W, dtype, cap=64 * 1024, order="straggler", n_out=1, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n_out", [0, 1, "W"])
-def test_output_modes(dtype, n_out):
+def test_output_modes(dtype, n_out, kernel):
     W = 4
-    full_compare(RAGGED, W, dtype, cap=32 * 1024, order="random", n_out=W if n_out == "W" else n_out)
+    full_compare(RAGGED, W, dtype, cap=32 * 1024, order="random", n_out=W if n_out == "W" else n_out,
+                 kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("W", [2, 3, 8])
-def test_misaligned_views(W, dtype):
+def test_misaligned_views(W, dtype, kernel):
     """Parameters at odd offsets of their buffers (no common 16-byte phase)
     take the scalar path; outputs at odd offsets too."""
-    full_compare(RAGGED, W, dtype, cap=16 * 1024, order="straggler", odd=True, out_odd=True)
+    full_compare(RAGGED, W, dtype, cap=16 * 1024, order="straggler", odd=True, out_odd=True, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_special_values(dtype):
-    full_compare(RAGGED, 4, dtype, cap=64 * 1024, special=True)
-    full_compare(RAGGED, 3, dtype, cap=64 * 1024, special=True)
+def test_special_values(dtype, kernel):
+    full_compare(RAGGED, 4, dtype, cap=64 * 1024, special=True, kernel=kernel)
+    full_compare(RAGGED, 3, dtype, cap=64 * 1024, special=True, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("mode", ["reduce_all", "reduce_bucket"])
-def test_explicit_launch_modes(mode):
-    full_compare(RAGGED, 8, "f32", cap=16 * 1024, mode=mode)
+def test_explicit_launch_modes(mode, kernel):
+    full_compare(RAGGED, 8, "f32", cap=16 * 1024, mode=mode, kernel=kernel)
 
 
-def test_repeated_iterations_and_side_stream():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_repeated_iterations_and_side_stream(kernel):
     s = torch.cuda.Stream()
-    full_compare(RAGGED, 4, "f32", cap=16 * 1024, iterations=3, stream=s)
+    full_compare(RAGGED, 4, "f32", cap=16 * 1024, iterations=3, stream=s, kernel=kernel)
 
 
 def test_cap_zero_per_gradient():
@@ -266,20 +282,23 @@ def test_empty_and_zero_length_models():
 
 # ---------------------------------------------------------------- reduced workloads, every element
 
-def test_resnet50_full_size_every_element():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_resnet50_full_size_every_element(kernel):
     numel = shapes.numels(shapes.resnet50())
-    full_compare(numel, 8, "f32", 25 * MIB, order="reverse", n_out=1)
+    full_compare(numel, 8, "f32", 25 * MIB, order="reverse", n_out=1, kernel=kernel)
 
 
-def test_bert_reduced_straggler_every_element():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bert_reduced_straggler_every_element(kernel):
     numel = shapes.numels(shapes.bert_large(layers=3, vocab=4096))
-    full_compare(numel, 4, "f32", 2 * MIB, order="straggler", n_out=1)
+    full_compare(numel, 4, "f32", 2 * MIB, order="straggler", n_out=1, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("cap_mib", [0, 1, 5, 25, 100])
-def test_gpt2_reduced_caps_every_element(cap_mib):
+def test_gpt2_reduced_caps_every_element(cap_mib, kernel):
     numel = shapes.numels(shapes.gpt2_medium(layers=2, vocab=3000, n_ctx=256))
-    full_compare(numel, 8, "bf16", cap_mib * MIB, order="reverse", n_out=1)
+    full_compare(numel, 8, "bf16", cap_mib * MIB, order="reverse", n_out=1, kernel=kernel)
 
 
 def test_nosync_small_every_element():
@@ -322,9 +341,10 @@ def device_replicas(numel, W, dtype, step=0):
     return flat, views, offs
 
 
-def full_size_run(numel, W, dtype, cap, order, mode="mark_ready"):
+def full_size_run(numel, W, dtype, cap, order, mode="mark_ready", kernel="ldg"):
     flat, views, offs = device_replicas(numel, W, dtype)
     red = Reducer(numel, dtype, cap)
+    set_kernel(red, kernel)
     arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
     out_offs, out_total = gen.packed_offsets(numel, 64)
     out_flat = torch.full((out_total,), float("nan"), device=DEV)
@@ -332,27 +352,31 @@ def full_size_run(numel, W, dtype, cap, order, mode="mark_ready"):
     run_path(red, views, arena, outs, order=order, mode=mode)
     n = sampled_check(numel, dtype, W, cap, flat, offs, arena, [(out_flat, out_offs)], 1)
     assert not torch.isnan(arena).any(), "arena not fully written"
+    assert red.device_status() == 0
     red.destroy()
     return n
 
 
-def test_bert_large_full_size_sampled():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bert_large_full_size_sampled(kernel):
     import os
     numel = shapes.numels(shapes.bert_large())
     path = os.path.join(os.path.dirname(__file__), "golden", "bert_large_ready_order.txt")
     order = [int(l) for l in open(path) if l.strip() and not l.startswith("#")]
-    assert full_size_run(numel, 4, "f32", 25 * MIB, order) > 100_000
+    assert full_size_run(numel, 4, "f32", 25 * MIB, order, kernel=kernel) > 100_000
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("cap_mib", [0, 1, 5, 25, 100])
-def test_gpt2_medium_full_size_sampled(cap_mib):
+def test_gpt2_medium_full_size_sampled(cap_mib, kernel):
     numel = shapes.numels(shapes.gpt2_medium())
-    assert full_size_run(numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel))) > 100_000
+    assert full_size_run(numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel)), kernel=kernel) > 100_000
 
 
-def test_bert_large_full_size_reduce_all_sampled():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bert_large_full_size_reduce_all_sampled(kernel):
     numel = shapes.numels(shapes.bert_large())
-    full_size_run(numel, 4, "f32", 25 * MIB, None, mode="reduce_all")
+    full_size_run(numel, 4, "f32", 25 * MIB, None, mode="reduce_all", kernel=kernel)
 
 
 def test_nosync_resnet50_full_size_sampled():
@@ -394,8 +418,9 @@ def test_nosync_resnet50_full_size_sampled():
     assert bits_equal(got, want), first_mismatch(got, want)
 
 
-def test_largest_tensor_64bit_offsets():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_largest_tensor_64bit_offsets(kernel):
     """One tensor of 2^31 + 37 bf16 elements (past 32-bit indexing) behind a
     small one, W = 2: sampled check including both ends."""
     numel = [1000, (1 << 31) + 37]
-    full_size_run(numel, 2, "bf16", 25 * MIB, [1, 0])
+    full_size_run(numel, 2, "bf16", 25 * MIB, [1, 0], kernel=kernel)
