@@ -160,6 +160,36 @@ int ddp_get_progress(const ddp_ctx* ctx, int32_t* next_bucket, int32_t* parked,
 int ddp_accumulate_nosync(ddp_ctx* ctx, void* const* acc, const void* const* g,
                           int32_t first_step, void* stream);
 
+/* ---------------------------------------------------------------- no allocation */
+
+/* The fused pass of ddp_reduce_all over every bucket, for callers that may not
+ * allocate device memory: code running while a CUDA stream is being captured
+ * in a mode that forbids cudaMalloc, code whose framework allocator already
+ * owns the device memory budget, and latency-critical loops where an
+ * allocation and its implicit device synchronisation are not allowed.  The
+ * pages have no counterpart of this call; it exists for such callers.
+ *
+ * It needs no ddp_bind: the caller passes the replicas' gradients and the
+ * outputs exactly as ddp_bind takes them (grads [W*P], bucket_arena, grad_out
+ * [n_out*P], n_out in {0, 1, W}), and the segment table that ddp_bind keeps in
+ * cudaMalloc'd memory lives here in one file-scope static device array of
+ * 256 KiB that every GPU which loads the library holds until the process
+ * exits.  The context's binding and iteration state are neither used nor
+ * changed.  No cudaMalloc, cudaFree or other allocating routine is called.
+ *   - Limit: one table entry per non-empty parameter of
+ *     8 + 8*W + 8*n_out + 4 bytes (plus 32 bytes); a layout that does not fit
+ *     in 256 KiB is rejected with DDP_ERR_INVALID_ARG before anything runs.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call copies its table into the shared array (the copy also zeroes
+ *     the status word) and the array keeps the last call's contents; calls
+ *     whose work can overlap on the GPU (other streams, other host threads)
+ *     race on it.  Calls on one stream are ordered and safe.
+ * Errors: INVALID_ARG, CUDA. */
+int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_arena,
+                           float* const* grad_out, int32_t n_out, void* stream);
+
 /* ---------------------------------------------------------------- options, info */
 
 enum ddp_option {

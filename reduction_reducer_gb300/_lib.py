@@ -50,6 +50,8 @@ SIGNATURES = {
     "ddp_set_option": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
     "ddp_get_launch_count": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64)]),
     "ddp_get_device_status": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32)]),
+    "ddp_reduce_all_noalloc": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.c_void_p,
+                                         C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
     "ddp_status_string": (C.c_char_p, [C.c_int]),
     "ddp_last_error": (C.c_char_p, [C.c_void_p]),
     "ddp_destroy": (None, [C.c_void_p]),

@@ -23,8 +23,11 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libddpreducer.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["ddp_host.cpp", "ddp_kernels.cu", "ddp_kernels_tma.cu"]
+# Size of the static device scratch of ddp_reduce_all_noalloc (256 KiB).
+NOALLOC_SCRATCH_BYTES = 256 * 1024
+COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I" + INCLUDE, "-I" + CSRC,
+          f"-DDDP_NOALLOC_SCRATCH_BYTES={NOALLOC_SCRATCH_BYTES}"]
+SOURCES = ["ddp_host.cpp", "ddp_kernels.cu", "ddp_kernels_tma.cu", "ddp_noalloc.cu"]
 
 
 def nvcc() -> str:

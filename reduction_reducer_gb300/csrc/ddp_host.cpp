@@ -554,3 +554,34 @@ void ddp_destroy(ddp_ctx* c) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- internal layout access
+// Read-only view of a context's bucket layout for other translation units of
+// the library (declared in ddp_layout.h).
+
+#include "ddp_layout.h"
+
+namespace ddp_internal {
+
+Layout layout(const ddp_ctx* c) {
+    Layout l;
+    l.P = c->P;
+    l.B = c->B;
+    l.elem = c->elem;
+    l.bf16 = c->dtype == DDP_BF16;
+    l.numel = c->numel.data();
+    l.loc = c->loc.data();
+    l.bucket_off = c->bucket_off.data();
+    l.members = &c->members;
+    return l;
+}
+
+}  // namespace ddp_internal
+
+namespace ddp_internal {
+
+void set_error(ddp_ctx* c, const std::string& msg) {
+    if (c) c->err = msg;
+}
+
+}  // namespace ddp_internal

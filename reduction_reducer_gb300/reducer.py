@@ -172,6 +172,28 @@ class Reducer:
         self._check(self.lib.ddp_get_progress(self._h, C.byref(nxt), parked, C.byref(n)))
         return nxt.value, [parked[i] for i in range(n.value)]
 
+    # ---------------------------------------------------------------- no allocation
+    def reduce_all_noalloc(self, grads, bucket_arena, grad_out=None, stream=None):
+        """Every bucket in one pass without any device allocation: for callers
+        that may not call cudaMalloc (stream capture that forbids it, a
+        framework allocator owning the memory budget, latency-critical loops).
+        Arguments as in ``bind``; the table goes to the library's static
+        device scratch (256 KiB), shared by all calls.  The first call on a
+        device must come before any stream capture."""
+        W = len(grads)
+        flat = [_ptr(t) for rep in grads for t in rep]
+        if grad_out is None:
+            outs = []
+        elif len(grad_out) == self.P and (self.P == 0 or not isinstance(grad_out[0], (list, tuple))):
+            outs = [grad_out]
+        else:
+            outs = list(grad_out)
+        out_flat = [_ptr(t) for o in outs for t in o]
+        gp = _ptr_array(flat)
+        op = _ptr_array(out_flat) if outs else None
+        self._check(self.lib.ddp_reduce_all_noalloc(self._h, W, gp, _ptr(bucket_arena), op, len(outs),
+                                                    _stream(stream)))
+
     # ---------------------------------------------------------------- no_sync
     def accumulate_nosync(self, acc, g, first_step: bool, stream=None):
         """acc, g: W lists of P fp32 tensors."""
