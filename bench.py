@@ -181,10 +181,15 @@ class Workload:
         else:
             self.order = gen.reverse_order(self.P)
         self.bytes = view_bytes(self.W, self.N, self.s_in, n_out)
+        import ctypes
+        self._order_c = (ctypes.c_int32 * len(self.order))(*self.order)
 
     def step(self, stream):
         red = self.red
-        if self.driver == "hooks":
+        if self.driver == "hooks":          # the ready order reported in one call
+            red.begin_iteration()
+            red.mark_ready_many(self._order_c, stream)
+        elif self.driver == "events":       # one mark_ready call per event
             red.begin_iteration()
             for v in self.order:
                 red.mark_ready(v, stream)
@@ -218,6 +223,14 @@ def time_steps(torch, stream, fn, steps, warmup, dist=None):
         ms = float(t.item())
         dist.barrier()
     return ms, t0, t1
+
+
+def kernel_name(wl) -> str:
+    from reduction_reducer_gb300 import _lib
+    k = wl.red.get_option(_lib.OPT_QUERY_KERNEL)
+    t = "float" if wl.dtype == "f32" else "uint16_t"
+    return (f"bucket_reduce_tma_kernel<{t}, {wl.W}>" if k == _lib.KERNEL_TMA
+            else f"bucket_reduce_kernel<{t}, {wl.W}>")
 
 
 def traffic_for(kernel_key, alg_bytes_per_launch):
@@ -354,7 +367,7 @@ def run_ours(args):
             "frac": round(gbs / peak, 4),
             "traffic": traffic_for("bucket_reduce", wl.bytes / max(per_step_launches, 1)),
             "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-            "kernel": "bucket_reduce_tma_kernel<float, 4>", "launches_per_step": round(per_step_launches, 2),
+            "kernel": kernel_name(wl), "launches_per_step": round(per_step_launches, 2),
             "bytes_per_launch_avg": int(wl.bytes / max(per_step_launches, 1)),
             "duration_source": "CUDA events over the timed region / launches (PDL back-to-back)",
             "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4)}
@@ -392,10 +405,11 @@ def run_ours(args):
             "config": {"workload": "bert_large" if args.layers is None else f"bert_large_{args.layers}layers",
                        "W": wl.W, "P": wl.P, "N": wl.N, "cap_mib": 25,
                        "buckets": wl.B, "mode": "copy-back (n_out=1)",
-                       "driver": ("begin_iteration + mark_ready over the stored straggler ready order"
-                                  if args.driver == "hooks" and args.layers is None else
-                                  "begin_iteration + mark_ready, reverse order" if args.driver == "hooks" else
-                                  "one reduce_all launch per step"),
+                       "driver": {"hooks": "begin_iteration + mark_ready_many (one call, every ready event in order)",
+                                  "events": "begin_iteration + one mark_ready call per ready event",
+                                  "all": "one reduce_all launch per step"}[args.driver]
+                                 + (", stored straggler ready order" if args.layers is None and args.driver != "all"
+                                    else ", reverse order" if args.driver != "all" else ""),
                        "bytes_per_step": wl.bytes,
                        "l2": "no flush: each step streams 8.0 GB, inputs 5.4 GB > 129 MB L2",
                        "parallelism": f"replicas only x{world}"},
@@ -446,12 +460,16 @@ def extra_configs(torch, device, stream, args, dist, keep):
             ms, _, _ = time_steps(torch, stream, lambda: wl.step(stream), steps, warm, dist)
         t = ms / steps
         out[key] = {"gbs": round(wl.bytes / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4),
-                    "bytes_per_step": wl.bytes, "buckets": wl.B, "W": wl.W,
+                    "bytes_per_step": wl.bytes, "buckets": wl.B, "W": wl.W, "kernel": kernel_name(wl),
                     "grad_elems_per_s": round(wl.W * wl.N / (t * 1e-3), 1), "note": note}
 
     # BERT-large, one persistent launch over all buckets (kernel alone)
     keep.driver = "all"
     timed(keep, "bert_large_reduce_all", "one reduce_all launch per step")
+    # BERT-large, one Python mark_ready call per ready event: each launch waits
+    # for the previous one (foreign work could sit between calls)
+    keep.driver = "events"
+    timed(keep, "bert_large_event_calls", "one mark_ready call per event (launches wait for their predecessor)")
     keep.driver = "hooks"
     # BERT-large as-view: replicas laid out as buckets, no copy-back
     wl = Workload("bert_large", torch, device, 25, n_out=0, driver="hooks", layout="buckets")
@@ -522,7 +540,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--layers", type=int, default=None, help="smaller BERT (profiling case)")
-    ap.add_argument("--driver", default="hooks", choices=["hooks", "all"])
+    ap.add_argument("--driver", default="hooks", choices=["hooks", "events", "all"])
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     args = ap.parse_args()

@@ -132,6 +132,20 @@ int ddp_abort_iteration(ddp_ctx* ctx);
 int ddp_mark_ready(ddp_ctx* ctx, int32_t var, int32_t* launched, int32_t* n_launched,
                    void* stream);
 
+/* A batch of ready events, processed in order exactly as that many
+ * ddp_mark_ready calls would be (an autograd engine reports its hooks one by
+ * one; a batch serves callers that know the order up front, like the one-GPU
+ * emulation whose replicas' gradients are all resident).  The gradients of
+ * every listed variable must be final on `stream` when the call is made.
+ * Launches after the first one of the call follow it directly on the stream
+ * (nothing else can be enqueued in between), so they start without waiting
+ * for it and wait only before exiting.
+ *   vars    host array [n] of variable indices
+ *   n_done  receives the number of events processed (all of them on success;
+ *           on error, the failing event's index; earlier events stay applied)
+ * Errors: as ddp_mark_ready. */
+int ddp_mark_ready_many(ddp_ctx* ctx, const int32_t* vars, int32_t n, int32_t* n_done, void* stream);
+
 /* Explicit launch of bucket `bucket`, which must be the next one (else
  * OUT_OF_ORDER): its members count as ready, it is launched, and any parked
  * buckets right after it follow in the same launch. */
@@ -197,12 +211,27 @@ enum ddp_option {
     DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 = occupancy maximum */
     DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
     DDP_OPT_BLOCK_THREADS = 3,    /* register-streaming kernel: 128 or 256 (default) */
-    DDP_OPT_KERNEL = 4,           /* 0: register-streaming kernel, 1 (default): bulk-copy (TMA) pipeline */
+    DDP_OPT_KERNEL = 4,           /* 0: register-streaming kernel, 1: bulk-copy (TMA) pipeline,
+                                     2 (default): per context, bulk copy when the median bucket has at
+                                     least DDP_OPT_AUTO_MIN_ELEMS elements, register streaming below */
     DDP_OPT_STAGES = 5,           /* bulk-copy kernel: ring depth, 2..8 (default 3) */
     DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB) */
-    DDP_OPT_TMA_CTAS_PER_SM = 7   /* bulk-copy kernel: CTAs per SM, 1 (default) or 2 */
+    DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernel: CTAs per SM, 1 (default) or 2 */
+    DDP_OPT_AUTO_MIN_ELEMS = 8,   /* kernel 2: median bucket length (elements) from which the bulk-copy
+                                     kernel is used (default 2^20) */
+    DDP_OPT_CHAINED = 9,          /* 1: chained launches (default 0).  The caller guarantees that every
+                                     gradient of an iteration is final before its first launch and that
+                                     nothing else is enqueued on the stream until its last launch (true
+                                     when the replicas' gradients are resident before the iteration, not
+                                     when backward kernels run between hooks).  Then a launch that follows
+                                     the iteration's previous launch on the same stream starts at once and
+                                     waits for it only before exiting; stream order still holds for any
+                                     work after the iteration. */
+    DDP_OPT_QUERY_KERNEL = 10     /* read only (ddp_get_option): kernel the bound context launches,
+                                     0 or 1; -1 before ddp_bind */
 };
 int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
+int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);
 
 /* Read and clear the device status word of a bound context (synchronous:
  * waits for the device).  0 = every bounded wait inside the kernels finished

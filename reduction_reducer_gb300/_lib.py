@@ -27,7 +27,8 @@ STATUS = {
 
 OPT_DRY_RUN, OPT_CTAS_PER_SM, OPT_PDL, OPT_BLOCK_THREADS = 0, 1, 2, 3
 OPT_KERNEL, OPT_STAGES, OPT_STAGE_BYTES, OPT_TMA_CTAS_PER_SM = 4, 5, 6, 7
-KERNEL_LDG, KERNEL_TMA = 0, 1
+OPT_AUTO_MIN_ELEMS, OPT_CHAINED, OPT_QUERY_KERNEL = 8, 9, 10
+KERNEL_LDG, KERNEL_TMA, KERNEL_AUTO = 0, 1, 2
 
 
 class Locator(C.Structure):
@@ -43,11 +44,13 @@ SIGNATURES = {
     "ddp_begin_iteration": (C.c_int, [C.c_void_p]),
     "ddp_abort_iteration": (C.c_int, [C.c_void_p]),
     "ddp_mark_ready": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.c_void_p]),
+    "ddp_mark_ready_many": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.c_int32, C.POINTER(C.c_int32), C.c_void_p]),
     "ddp_reduce_bucket": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p]),
     "ddp_reduce_all": (C.c_int, [C.c_void_p, C.c_void_p]),
     "ddp_get_progress": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "ddp_accumulate_nosync": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
     "ddp_set_option": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
+    "ddp_get_option": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64)]),
     "ddp_get_launch_count": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64)]),
     "ddp_get_device_status": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32)]),
     "ddp_reduce_all_noalloc": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.c_void_p,

@@ -115,7 +115,24 @@ struct ReduceParams {
     float inv_w;
     int stages;         // pipelined kernel: ring depth
     int tile;           // pipelined kernel: elements per replica per stage
+    int chain;          // 1: follows a launch of the same iteration (see pdl_enter)
 };
+
+// Entry/exit ordering with the previous launch in the stream.
+//   chain == 0: wait for every earlier grid, then let the successor start;
+//   chain == 1: the previous launch is this iteration's own bucket kernel on
+//               the same stream (disjoint data) and the caller guarantees that
+//               nothing else runs on the stream during the iteration: start at
+//               once, and wait for the predecessor only before exiting, so
+//               this grid still completes after everything before it.
+__device__ __forceinline__ void pdl_enter(int chain) {
+    if (!chain) pdl_wait();
+    pdl_trigger();
+}
+
+__device__ __forceinline__ void pdl_exit(int chain) {
+    if (chain) pdl_wait();
+}
 
 // Rank-order fp32 mean of one element, scalar path (heads, tails, segments
 // whose pointers do not share the arena's 16-byte phase).

@@ -64,12 +64,20 @@ struct ddp_ctx {
     bool pdl = true;
     int opt_ctas = 0;
     int opt_block = 256;
-    // Defaults from the GB300 sweep on BERT-large W=4: the bulk-copy pipeline
-    // with 3 stages of 32 KiB, one CTA per SM.
-    int opt_kernel = ddpk::KERNEL_TMA;
+    // Defaults from the GB300 sweeps: the kernel is chosen per context from
+    // the median bucket length (bulk-copy pipeline with 3 stages of 32 KiB,
+    // one CTA per SM, from 2^20 elements up; register streaming below, where
+    // launches are too small to fill the ring).  One kernel for all launches
+    // of a context, so consecutive launches can overlap.
+    int opt_kernel = ddpk::KERNEL_AUTO;
     int opt_stages = 3;
     int opt_stage_bytes = 32 * 1024;
     int opt_tma_ctas = 1;
+    long long opt_auto_min = 1LL << 20;
+    bool opt_chain = false;
+    int64_t iter_launches = 0;      // launches issued in the current iteration
+    void* iter_stream = nullptr;    // stream of the last of them
+    int64_t call_launches = 0;      // launches issued by the current API call
     ddpk::LaunchCfg cfg{};
     int acc_ctas = 1;
     int64_t launches = 0;
@@ -98,6 +106,7 @@ void reset_iteration(ddp_ctx* c) {
 void start_iteration(ddp_ctx* c) {
     reset_iteration(c);
     c->active = c->B > 0;
+    c->iter_launches = 0;
 }
 
 // Starts an iteration implicitly when the previous one has finished.
@@ -122,10 +131,22 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->cfg.block = c->opt_block;
     c->cfg.pdl = c->pdl;
     c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas : ddpk::reduce_max_ctas_per_sm(in, c->W, c->opt_block);
-    c->cfg.kernel = c->opt_kernel;
+    if (c->opt_kernel == ddpk::KERNEL_AUTO) {
+        std::vector<int64_t> lens;
+        for (int32_t b = 0; b < c->B; ++b) lens.push_back(c->bucket_off[b + 1] - c->bucket_off[b]);
+        int64_t median = 0;
+        if (!lens.empty()) {
+            std::nth_element(lens.begin(), lens.begin() + lens.size() / 2, lens.end());
+            median = lens[lens.size() / 2];
+        }
+        c->cfg.kernel = median >= c->opt_auto_min ? ddpk::KERNEL_TMA : ddpk::KERNEL_LDG;
+    } else {
+        c->cfg.kernel = c->opt_kernel;
+    }
     c->cfg.stages = c->opt_stages;
     c->cfg.stage_bytes = c->opt_stage_bytes;
     c->cfg.tma_ctas_per_sm = c->opt_tma_ctas;
+
     c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->opt_block);
     return DDP_OK;
 }
@@ -148,10 +169,21 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
     int st = check_device(c);
     if (st != DDP_OK) return st;
     const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
+    ddpk::LaunchCfg cfg = c->cfg;
+    // Chained launches: a launch that directly follows this iteration's
+    // previous launch on the same stream need not wait for it when nothing
+    // else can sit between them -- always within one API call (the call
+    // enqueues only its own launches), across calls only when the caller
+    // opted in (DDP_OPT_CHAINED).
+    const bool follows_own = c->iter_launches > 0 && stream == c->iter_stream;
+    cfg.chain = c->pdl && follows_own && (c->call_launches > 0 || c->opt_chain) ? 1 : 0;
     long long n = 0;
     cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, lo, hi, s0, s1, c->inv_w,
-                                        c->cfg, static_cast<cudaStream_t>(stream), &n);
+                                        cfg, static_cast<cudaStream_t>(stream), &n);
     c->launches += n;
+    c->iter_launches += n;
+    c->call_launches += n;
+    c->iter_stream = stream;
     if (e != cudaSuccess) return cuda_fail(c, e, "bucket reduce launch");
     return DDP_OK;
 }
@@ -402,6 +434,7 @@ int ddp_abort_iteration(ddp_ctx* c) {
 
 int ddp_mark_ready(ddp_ctx* c, int32_t var, int32_t* launched, int32_t* n_launched, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
+    c->call_launches = 0;
     if (n_launched) *n_launched = 0;
     if (var < 0 || var >= c->P) return fail(c, DDP_ERR_INVALID_ARG, "variable index out of range");
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "mark_ready before bind");
@@ -413,8 +446,32 @@ int ddp_mark_ready(ddp_ctx* c, int32_t var, int32_t* launched, int32_t* n_launch
     return DDP_OK;
 }
 
+int ddp_mark_ready_many(ddp_ctx* c, const int32_t* vars, int32_t n, int32_t* n_done, void* stream) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (n_done) *n_done = 0;
+    if (n < 0 || (n > 0 && !vars)) return fail(c, DDP_ERR_INVALID_ARG, "bad event list");
+    if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "mark_ready_many before bind");
+    c->call_launches = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t var = vars[i];
+        if (var < 0 || var >= c->P) return fail(c, DDP_ERR_INVALID_ARG, "variable index out of range at event " + std::to_string(i));
+        ensure_started(c);
+        if (c->ready[var])
+            return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready at event " + std::to_string(i));
+        c->ready[var] = 1;
+        const int32_t b = c->loc[var].bucket;
+        if (--c->pending[b] == 0 && b == c->next) {
+            const int st = release(c, nullptr, nullptr, stream);
+            if (st != DDP_OK) return st;
+        }
+        if (n_done) *n_done = i + 1;
+    }
+    return DDP_OK;
+}
+
 int ddp_reduce_bucket(ddp_ctx* c, int32_t bucket, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
+    c->call_launches = 0;
     if (bucket < 0 || bucket >= c->B) return fail(c, DDP_ERR_INVALID_ARG, "bucket index out of range");
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "reduce_bucket before bind");
     ensure_started(c);
@@ -428,6 +485,7 @@ int ddp_reduce_bucket(ddp_ctx* c, int32_t bucket, void* stream) {
 
 int ddp_reduce_all(ddp_ctx* c, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
+    c->call_launches = 0;
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "reduce_all before bind");
     ensure_started(c);
     const int32_t first = c->next;
@@ -498,9 +556,18 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             c->pdl = value != 0;
             c->cfg.pdl = c->pdl;
             return DDP_OK;
+        case DDP_OPT_AUTO_MIN_ELEMS:
+            if (value < 0) return fail(c, DDP_ERR_INVALID_ARG, "auto threshold must be >= 0");
+            c->opt_auto_min = value;
+            return refresh_launch_cfg(c);
+        case DDP_OPT_CHAINED:
+            c->opt_chain = value != 0;
+            return DDP_OK;
+        case DDP_OPT_QUERY_KERNEL:
+            return fail(c, DDP_ERR_INVALID_ARG, "DDP_OPT_QUERY_KERNEL is read with ddp_get_option");
         case DDP_OPT_KERNEL:
-            if (value != ddpk::KERNEL_LDG && value != ddpk::KERNEL_TMA)
-                return fail(c, DDP_ERR_INVALID_ARG, "kernel must be 0 (register streaming) or 1 (bulk copy)");
+            if (value != ddpk::KERNEL_LDG && value != ddpk::KERNEL_TMA && value != ddpk::KERNEL_AUTO)
+                return fail(c, DDP_ERR_INVALID_ARG, "kernel must be 0 (register streaming), 1 (bulk copy) or 2 (by size)");
             c->opt_kernel = static_cast<int>(value);
             return refresh_launch_cfg(c);
         case DDP_OPT_STAGES:
@@ -539,6 +606,24 @@ int ddp_get_device_status(ddp_ctx* c, int32_t* status) {
     }
     *status = v;
     return DDP_OK;
+}
+
+int ddp_get_option(const ddp_ctx* c, int32_t option, int64_t* value) {
+    if (!c || !value) return DDP_ERR_INVALID_ARG;
+    switch (option) {
+        case DDP_OPT_DRY_RUN: *value = c->dry; return DDP_OK;
+        case DDP_OPT_CTAS_PER_SM: *value = c->opt_ctas; return DDP_OK;
+        case DDP_OPT_PDL: *value = c->pdl; return DDP_OK;
+        case DDP_OPT_BLOCK_THREADS: *value = c->opt_block; return DDP_OK;
+        case DDP_OPT_KERNEL: *value = c->opt_kernel; return DDP_OK;
+        case DDP_OPT_STAGES: *value = c->opt_stages; return DDP_OK;
+        case DDP_OPT_STAGE_BYTES: *value = c->opt_stage_bytes; return DDP_OK;
+        case DDP_OPT_TMA_CTAS_PER_SM: *value = c->opt_tma_ctas; return DDP_OK;
+        case DDP_OPT_AUTO_MIN_ELEMS: *value = c->opt_auto_min; return DDP_OK;
+        case DDP_OPT_CHAINED: *value = c->opt_chain; return DDP_OK;
+        case DDP_OPT_QUERY_KERNEL: *value = c->bound ? c->cfg.kernel : -1; return DDP_OK;
+        default: return DDP_ERR_INVALID_ARG;
+    }
 }
 
 int ddp_get_launch_count(const ddp_ctx* c, int64_t* launches) {

@@ -47,11 +47,11 @@ using namespace dev;
 
 constexpr int kMaxBlock = 256;
 
-// Loads in flight per thread in the vector body (W x U); the unroll U of the
-// fixed-W bodies is derived from it.
-#ifndef DDP_LDG_MAX_LOADS
-#define DDP_LDG_MAX_LOADS 16
-#endif
+// Vectors per replica in flight per thread in the fixed-W vector body
+// (W x U loads issued before the first add).  U = 2 measured best on GB300
+// for W = 4 and W = 8; W = 16 uses 1 to stay within registers.
+template <int WC>
+__host__ __device__ constexpr int unroll_for() { return WC <= 2 ? 4 : (WC <= 8 ? 2 : 1); }
 
 // Vector body, W known at compile time: all WC x U loads in flight at once.
 template <typename Tin, int WC, int U>
@@ -130,19 +130,20 @@ __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin*
 template <typename Tin, int WC>
 __global__ void __launch_bounds__(kMaxBlock)
 bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
-    pdl_trigger();
-    pdl_wait();
+    pdl_enter(p.chain);
     using V = Vec<Tin>;
     constexpr int N = V::N;
-    constexpr int U = WC == 0 ? 1
-                      : (WC >= DDP_LDG_MAX_LOADS ? 1 : (DDP_LDG_MAX_LOADS / WC > 4 ? 4 : DDP_LDG_MAX_LOADS / WC));
+    constexpr int U = WC == 0 ? 1 : unroll_for<WC>();
     const int W = WC > 0 ? WC : p.W;
 
     long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
     long long y = x + p.piece;
     x = x < p.lo ? p.lo : x;
     y = y > p.hi ? p.hi : y;
-    if (x >= y) return;   // whole CTA leaves together
+    if (x >= y) {   // whole CTA leaves together
+        if (threadIdx.x == 0) pdl_exit(p.chain);
+        return;
+    }
 
     int s = find_segment(p.seg_off, p.s0, p.s1, x);
     while (x < y) {
@@ -166,6 +167,7 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
         x = e;
         ++s;
     }
+    if (threadIdx.x == 0) pdl_exit(p.chain);
 }
 
 // ------------------------------------------------------------------ accumulate kernel
@@ -184,6 +186,7 @@ struct AccParams {
     long long piece;   // elements per CTA, multiple of 4
     int npairs;
     int first;
+    int chain;         // 1: follows this call's previous accumulate launch
     AccPairDev pair[kMaxAccPairs];
 };
 
@@ -207,12 +210,14 @@ __device__ __forceinline__ int find_pair(const AccParams& p, long long x) {
 
 __global__ void __launch_bounds__(kMaxBlock)
 accumulate_kernel(const __grid_constant__ AccParams p) {
-    pdl_trigger();
-    pdl_wait();
+    pdl_enter(p.chain);
     long long x = static_cast<long long>(blockIdx.x) * p.piece;
     long long y = x + p.piece;
     y = y > p.total ? p.total : y;
-    if (x >= y) return;
+    if (x >= y) {
+        if (threadIdx.x == 0) pdl_exit(p.chain);
+        return;
+    }
     int i = find_pair(p, x);
     const long long step = blockDim.x;
     while (x < y && i < p.npairs) {
@@ -228,23 +233,28 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
             const long long sc_end = vec && kb < ke ? kb * 4 : e;
             for (long long a = x + threadIdx.x; a < sc_end; a += step)
                 acc[a] = p.first ? g[a] : __fadd_rn(acc[a], g[a]);
-            for (long long k = kb + threadIdx.x; k < ke; k += 2 * step) {
-                const long long k2 = k + step;
-                const float4 g0 = ld_stream(reinterpret_cast<const float4*>(g + 4 * k));
-                float4 g1 = g0;
-                if (k2 < ke) g1 = ld_stream(reinterpret_cast<const float4*>(g + 4 * k2));
-                if (p.first) {
-                    st_stream(acc + 4 * k, g0);
-                    if (k2 < ke) st_stream(acc + 4 * k2, g1);
-                } else {
-                    const float4 c0 = __ldcs(reinterpret_cast<const float4*>(acc + 4 * k));
-                    float4 c1 = c0;
-                    if (k2 < ke) c1 = __ldcs(reinterpret_cast<const float4*>(acc + 4 * k2));
-                    st_stream(acc + 4 * k, make_float4(__fadd_rn(c0.x, g0.x), __fadd_rn(c0.y, g0.y),
-                                                       __fadd_rn(c0.z, g0.z), __fadd_rn(c0.w, g0.w)));
-                    if (k2 < ke)
-                        st_stream(acc + 4 * k2, make_float4(__fadd_rn(c1.x, g1.x), __fadd_rn(c1.y, g1.y),
-                                                            __fadd_rn(c1.z, g1.z), __fadd_rn(c1.w, g1.w)));
+            constexpr int UA = 4;   // vectors per thread per iteration: 2 x 4 loads in flight
+            for (long long k = kb + threadIdx.x; k < ke; k += UA * step) {
+                float4 gv[UA], cv[UA];
+#pragma unroll
+                for (int u = 0; u < UA; ++u) {
+                    const long long kk = k + u * step;
+                    if (kk < ke) {
+                        gv[u] = ld_stream(reinterpret_cast<const float4*>(g + 4 * kk));
+                        if (!p.first) cv[u] = __ldcs(reinterpret_cast<const float4*>(acc + 4 * kk));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < UA; ++u) {
+                    const long long kk = k + u * step;
+                    if (kk < ke) {
+                        if (p.first) {
+                            st_stream(acc + 4 * kk, gv[u]);
+                        } else {
+                            st_stream(acc + 4 * kk, make_float4(__fadd_rn(cv[u].x, gv[u].x), __fadd_rn(cv[u].y, gv[u].y),
+                                                                __fadd_rn(cv[u].z, gv[u].z), __fadd_rn(cv[u].w, gv[u].w)));
+                        }
+                    }
                 }
             }
             if (vec && kb < ke)
@@ -256,6 +266,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
         ++i;
         if (i < p.npairs && p.pair[i].off > x) x = p.pair[i].off;
     }
+    if (threadIdx.x == 0) pdl_exit(p.chain);
 }
 
 // ------------------------------------------------------------------ launch helpers
@@ -336,6 +347,7 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
     p.W = W;
     p.n_out = n_out;
     p.inv_w = inv_w;
+    p.chain = cfg.chain;
     // One slice per CTA, at least two vectors per thread so tiny ranges use
     // few CTAs; slices are multiples of the vector width so no vector is split.
     const long long span = hi - p.base;
@@ -354,9 +366,13 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const Laun
                               cudaStream_t stream, long long* launches) {
     thread_local AccParams p;   // ~32 KiB: kept off the stack, one per host thread
     int i = 0;
+    int issued = 0;
     while (i < n) {
         p.npairs = 0;
         p.first = first;
+        // launches after the first of this call directly follow it on the
+        // stream and touch other pairs: no need to wait for it on entry
+        p.chain = cfg.pdl && issued > 0 ? 1 : 0;
         long long off = 0;
         while (i < n && p.npairs < kMaxAccPairs) {
             if (pairs[i].len > 0) {
@@ -379,6 +395,7 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const Laun
         grid = ceil_div(off, p.piece);
         cudaError_t err = launch(accumulate_kernel, static_cast<int>(grid), cfg.block, p, cfg.pdl, stream);
         if (err != cudaSuccess) return err;
+        ++issued;
         if (launches) ++*launches;
     }
     return cudaSuccess;

@@ -24,7 +24,8 @@ struct SegTable {
     int* status;
 };
 
-enum KernelKind { KERNEL_LDG = 0, KERNEL_TMA = 1 };
+// KERNEL_AUTO is resolved per context by the host core (median bucket size).
+enum KernelKind { KERNEL_LDG = 0, KERNEL_TMA = 1, KERNEL_AUTO = 2 };
 
 struct LaunchCfg {
     int sms;           // multiprocessors on the device
@@ -35,6 +36,7 @@ struct LaunchCfg {
     int stages;        // bulk-copy kernel: ring depth
     int stage_bytes;   // bulk-copy kernel: bytes of all replicas' tiles per stage
     int tma_ctas_per_sm;
+    int chain;                  // per launch: see pdl_enter in ddp_device.cuh
 };
 
 enum InType { IN_F32 = 0, IN_BF16 = 1 };

@@ -148,7 +148,6 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(full + i), 1);
@@ -157,13 +156,16 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
         fence_barrier_init();
     }
     __syncthreads();
-    pdl_wait();
+    pdl_enter(p.chain);
 
     long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
     long long y = x + p.piece;
     x = x < p.lo ? p.lo : x;
     y = y > p.hi ? p.hi : y;
-    if (x >= y) return;   // whole CTA, before any copy is issued
+    if (x >= y) {   // whole CTA, before any copy is issued
+        if (threadIdx.x == 0) pdl_exit(p.chain);
+        return;
+    }
     const int s = find_segment(p.seg_off, p.s0, p.s1, x);
 
     if (warp == 0) {
@@ -190,6 +192,7 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
         // every issued copy must land before the CTA may exit
         for (long long j = k > S ? k - S : 0; j < k; ++j)
             mbar_wait(smem_u32(full + j % S), static_cast<uint32_t>(j / S) & 1u, p.status, kStatusDrainTimeout, failed);
+        pdl_exit(p.chain);
         return;
     }
 
@@ -274,6 +277,10 @@ cudaError_t ensure_smem_attr(TmaKernel k) {
     for (int i = 0; i < n_done; ++i)
         if (done_k[i] == k && done_dev[i] == dev) return cudaSuccess;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    // Prefer the largest shared-memory carveout so that the next launch's
+    // CTAs (programmatic dependent launch) fit beside this one's.
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && n_done < kSlots) {
         done_k[n_done] = k;
         done_dev[n_done] = dev;
@@ -315,6 +322,7 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     p.inv_w = inv_w;
     p.stages = stages;
     p.tile = static_cast<int>(tile);
+    p.chain = cfg.chain;
     const long long span = hi - p.base;
     long long grid = static_cast<long long>(cfg.sms) * (cfg.tma_ctas_per_sm > 0 ? cfg.tma_ctas_per_sm : 1);
     grid = grid < ceil_div(span, tile) ? grid : ceil_div(span, tile);

@@ -160,6 +160,14 @@ class Reducer:
         self._check(self.lib.ddp_mark_ready(self._h, int(var), self._launched, C.byref(n), _stream(stream)))
         return [self._launched[i] for i in range(n.value)]
 
+    def mark_ready_many(self, vars_, stream=None):
+        """Ready events in order, in one call; returns how many were processed."""
+        n = len(vars_)
+        arr = vars_ if isinstance(vars_, C.Array) else (C.c_int32 * max(n, 1))(*vars_)
+        done = C.c_int32()
+        self._check(self.lib.ddp_mark_ready_many(self._h, arr, n, C.byref(done), _stream(stream)))
+        return done.value
+
     def reduce_bucket(self, bucket: int, stream=None):
         self._check(self.lib.ddp_reduce_bucket(self._h, int(bucket), _stream(stream)))
 
@@ -204,6 +212,11 @@ class Reducer:
     # ---------------------------------------------------------------- options
     def set_option(self, option: int, value: int):
         self._check(self.lib.ddp_set_option(self._h, int(option), int(value)))
+
+    def get_option(self, option: int) -> int:
+        v = C.c_int64()
+        self._check(self.lib.ddp_get_option(self._h, int(option), C.byref(v)))
+        return v.value
 
     def set_dry_run(self, on: bool = True):
         self.set_option(_lib.OPT_DRY_RUN, 1 if on else 0)

@@ -83,12 +83,15 @@ def host_grads(numel, W, dtype, step=0, align=64, odd=False, special=False, seed
 
 
 def run_path(red: Reducer, grads_dev, arena, outs, order=None, mode="mark_ready", stream=None):
-    """Bind and run one iteration; mode: mark_ready | reduce_all | reduce_bucket."""
+    """Bind and run one iteration; mode: mark_ready | mark_ready_many |
+    reduce_all | reduce_bucket."""
     red.bind(grads_dev, arena, outs)
     red.begin_iteration()
     if mode == "mark_ready":
         for v in order:
             red.mark_ready(v, stream)
+    elif mode == "mark_ready_many":
+        assert red.mark_ready_many(list(order), stream) == len(order)
     elif mode == "reduce_all":
         red.reduce_all(stream)
     elif mode == "reduce_bucket":

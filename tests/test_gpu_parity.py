@@ -65,7 +65,15 @@ def make_order(kind, numel, members, seed=0):
 
 
 def set_kernel(red, kernel):
-    red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_TMA if kernel == "tma" else _lib.KERNEL_LDG)
+    """ldg | tma | auto (size-based choice) | chained (bulk copy + chained launches)."""
+    if kernel == "chained":
+        red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_TMA)
+        red.set_option(_lib.OPT_CHAINED, 1)
+    elif kernel == "auto":
+        red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_AUTO)
+        red.set_option(_lib.OPT_AUTO_MIN_ELEMS, 50_000)
+    else:
+        red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_TMA if kernel == "tma" else _lib.KERNEL_LDG)
 
 
 def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_ready", odd=False,
@@ -163,7 +171,7 @@ def test_replicas_identical_after_step():
 RAGGED = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 70001, 0, 9, 300007, 16, 31]
 
 
-KERNELS = ["ldg", "tma"]
+KERNELS = ["ldg", "tma", "auto", "chained"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -196,6 +204,16 @@ def test_misaligned_views(W, dtype, kernel):
 def test_special_values(dtype, kernel):
     full_compare(RAGGED, 4, dtype, cap=64 * 1024, special=True, kernel=kernel)
     full_compare(RAGGED, 3, dtype, cap=64 * 1024, special=True, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [3, 4, 8])
+def test_mark_ready_many(W, dtype, kernel):
+    """A whole ready order in one call: launches after the first chain."""
+    full_compare(RAGGED, W, dtype, cap=16 * 1024, order="straggler", mode="mark_ready_many", kernel=kernel,
+                 iterations=2)
+    full_compare(RAGGED, W, dtype, cap=0, order="random", mode="mark_ready_many", kernel=kernel)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -344,7 +362,8 @@ def device_replicas(numel, W, dtype, step=0):
 def full_size_run(numel, W, dtype, cap, order, mode="mark_ready", kernel="ldg"):
     flat, views, offs = device_replicas(numel, W, dtype)
     red = Reducer(numel, dtype, cap)
-    set_kernel(red, kernel)
+    if kernel is not None:        # None: the library's defaults
+        set_kernel(red, kernel)
     arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
     out_offs, out_total = gen.packed_offsets(numel, 64)
     out_flat = torch.full((out_total,), float("nan"), device=DEV)
@@ -366,11 +385,22 @@ def test_bert_large_full_size_sampled(kernel):
     assert full_size_run(numel, 4, "f32", 25 * MIB, order, kernel=kernel) > 100_000
 
 
+def test_bert_large_full_size_bench_configuration():
+    """Exactly what bench.py times: library defaults, the stored straggler
+    order reported in one mark_ready_many call, one copy-back."""
+    import os
+    numel = shapes.numels(shapes.bert_large())
+    path = os.path.join(os.path.dirname(__file__), "golden", "bert_large_ready_order.txt")
+    order = [int(l) for l in open(path) if l.strip() and not l.startswith("#")]
+    assert full_size_run(numel, 4, "f32", 25 * MIB, order, mode="mark_ready_many", kernel=None) > 100_000
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("cap_mib", [0, 1, 5, 25, 100])
 def test_gpt2_medium_full_size_sampled(cap_mib, kernel):
     numel = shapes.numels(shapes.gpt2_medium())
-    assert full_size_run(numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel)), kernel=kernel) > 100_000
+    assert full_size_run(numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel)), kernel=kernel,
+                         mode="mark_ready_many") > 100_000
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -424,3 +454,22 @@ def test_largest_tensor_64bit_offsets(kernel):
     small one, W = 2: sampled check including both ends."""
     numel = [1000, (1 << 31) + 37]
     full_size_run(numel, 2, "bf16", 25 * MIB, [1, 0], kernel=kernel)
+
+
+def test_automatic_kernel_choice():
+    """Default kernel choice per context: the bulk-copy pipeline when the
+    median bucket has >= 2^20 elements (BERT-large, 25 MiB buckets), register
+    streaming for per-gradient buckets (GPT-2-medium at cap 0)."""
+    def chosen(numel, dtype, cap):
+        red = Reducer(numel, dtype, cap)
+        assert red.get_option(_lib.OPT_QUERY_KERNEL) == -1
+        W = 2
+        offs, total = gen.packed_offsets(numel, 64)
+        flat = [torch.zeros(total, dtype=torch.float32 if dtype == "f32" else torch.bfloat16, device=DEV) for _ in range(W)]
+        grads = [[f[o:o + n] for o, n in zip(offs, numel)] for f in flat]
+        red.bind(grads, torch.empty(red.arena_numel(), device=DEV), None)
+        k = red.get_option(_lib.OPT_QUERY_KERNEL)
+        red.destroy()
+        return k
+    assert chosen(shapes.numels(shapes.bert_large()), "f32", 25 * MIB) == _lib.KERNEL_TMA
+    assert chosen(shapes.numels(shapes.gpt2_medium()), "bf16", 0) == _lib.KERNEL_LDG

@@ -185,3 +185,34 @@ def test_explicit_launch_matches_oracle(lib):
     assert red.get_progress() == (sm.next, sm.parked())
     red.reduce_all(); sm.launch_rest()
     assert red.get_progress() == (sm.next, sm.parked())
+
+
+def test_mark_ready_many_matches_oracle(lib):
+    """The batch call is the same state machine: same launches and parked
+    sets as one mark_ready per event, on every permutation of a tiny list."""
+    numel = [3, 0, 2, 5, 1, 4]
+    members, _ = assign_buckets(numel, 1, 3)
+    red = _make(numel, "f32", 12)
+    red.set_dry_run(True)
+    for order in itertools.permutations(range(len(numel))):
+        red.begin_iteration()
+        k = 3
+        assert red.mark_ready_many(list(order[:k])) == k
+        sm = ReadinessOracle(members)
+        sm.begin_iteration()
+        for v in order[:k]:
+            sm.mark_ready(v)
+        assert red.get_progress() == (sm.next, sm.parked()), order
+        assert red.mark_ready_many(list(order[k:])) == len(order) - k
+        assert red.get_progress() == (len(members), [])
+
+
+def test_mark_ready_many_error_stops_at_event(lib):
+    from reduction_reducer_gb300 import AlreadyReady
+    red = _make([1, 1, 1, 1], "f32", 4)
+    red.set_dry_run(True)
+    red.begin_iteration()
+    with pytest.raises(AlreadyReady):
+        red.mark_ready_many([3, 2, 3, 1])
+    # events before the failing one stay applied: buckets 0 and 1 are out
+    assert red.get_progress() == (2, [])
