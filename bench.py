@@ -201,6 +201,14 @@ class Workload:
         self.flat = self.grads = self.arena = self.out_flat = None
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """Largest value over the process group (the slowest rank's time)."""
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def time_steps(torch, stream, fn, steps, warmup, dist=None):
     for _ in range(warmup):
         fn()
@@ -218,9 +226,7 @@ def time_steps(torch, stream, fn, steps, warmup, dist=None):
     t1 = time.time()
     ms = start.elapsed_time(end)
     if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, "cuda")
         dist.barrier()
     return ms, t0, t1
 
@@ -321,6 +327,18 @@ def run_reference(args):
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_nosync_only(args):
+    """The no_sync workload alone (ResNet-50, W=16, K micro-steps + reduce):
+    a compact case for profiling the accumulate kernel."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=device)
+    res = nosync_config(torch, device, stream, args.steps, args.warmup, None, K=args.nosync_k)
+    print(json.dumps({"workload": f"nosync_resnet50_w16_k{args.nosync_k}", **res}), flush=True)
     return 0
 
 
@@ -425,28 +443,65 @@ def run_ours(args):
 
 
 def measure_e2e(torch, wl, stream, steps, dist):
-    """Same metric through the public API with host buffers: every step copies
-    the W replicas' gradients from pinned host memory, runs the iteration and
-    reads the averaged gradients back to pinned host memory."""
+    """Same metric through the public API with host buffers.  Every step
+    copies the W replicas' gradients from pinned host memory and reads the
+    averaged gradients back to pinned host memory, pipelined per bucket the
+    way DDP overlaps communication with the backward pass: bucket b's slices
+    go up on a copy stream, its ready events are reported as soon as they
+    have landed (one mark_ready_many call per bucket), and its averaged
+    slice comes back on a second copy stream while later buckets are still
+    in flight."""
+    import ctypes
     host_in = [torch.empty(f.numel(), dtype=f.dtype, pin_memory=True) for f in wl.flat]
     for h, f in zip(host_in, wl.flat):
         h.copy_(f)
     host_out = torch.empty(wl.out_flat.numel(), dtype=torch.float32, pin_memory=True)
-    h2d = sum(f.numel() * f.element_size() for f in wl.flat)
-    d2h = host_out.numel() * 4
+    h2d_stream = torch.cuda.Stream(device=stream.device)
+    d2h_stream = torch.cuda.Stream(device=stream.device)
+    out_offs, _ = gen.packed_offsets(wl.numel, 64)
+    buckets = []
+    for members in wl.red.get_members():
+        lo_v, hi_v = min(members), max(members)
+        lo, hi = wl.offs[lo_v], wl.offs[hi_v] + wl.numel[hi_v]          # replica slice (registration order)
+        olo, ohi = out_offs[lo_v], out_offs[hi_v] + wl.numel[hi_v]      # copy-back slice
+        vars_c = (ctypes.c_int32 * len(members))(*members)
+        buckets.append((lo, hi, olo, ohi, vars_c, len(members)))
+    h2d = sum((hi - lo) * f.element_size() for (lo, hi, *_) in buckets for f in wl.flat)
+    d2h = sum((ohi - olo) * 4 for (_, _, olo, ohi, *_) in buckets)
+    ev_in = [torch.cuda.Event() for _ in buckets]
+    ev_red = [torch.cuda.Event() for _ in buckets]
+    red = wl.red
 
     def one():
-        for h, f in zip(host_in, wl.flat):
-            f.copy_(h, non_blocking=True)
-        wl.step(stream)
-        host_out.copy_(wl.out_flat, non_blocking=True)
+        begin = torch.cuda.Event()
+        begin.record(stream)
+        h2d_stream.wait_event(begin)
+        with torch.cuda.stream(h2d_stream):
+            for b, (lo, hi, *_rest) in enumerate(buckets):
+                for h, f in zip(host_in, wl.flat):
+                    f[lo:hi].copy_(h[lo:hi], non_blocking=True)
+                ev_in[b].record(h2d_stream)
+        red.begin_iteration()
+        for b, (lo, hi, olo, ohi, vars_c, n) in enumerate(buckets):
+            stream.wait_event(ev_in[b])
+            red.mark_ready_many(vars_c, stream)
+            ev_red[b].record(stream)
+            d2h_stream.wait_event(ev_red[b])
+            with torch.cuda.stream(d2h_stream):
+                host_out[olo:ohi].copy_(wl.out_flat[olo:ohi], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(d2h_stream)
+        stream.wait_event(done)
 
     with torch.cuda.stream(stream):
         ms, _, _ = time_steps(torch, stream, one, steps, 1, dist)
     ms_step = ms / steps
     return {"value": round(wl.bytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "algorithmic bytes of the step / (H2D of replica gradients + iteration + D2H of averaged gradients)"}
+            "h2d_gbs": round(h2d / (ms_step * 1e-3) / 1e9, 1),
+            "note": ("algorithmic bytes of the step / time of a step that copies the replicas' gradients "
+                     "host->device per bucket, reduces each bucket as it lands (mark_ready_many per bucket) "
+                     "and copies its averaged gradients back; pinned host buffers, copies on two streams")}
 
 
 def extra_configs(torch, device, stream, args, dist, keep):
@@ -489,10 +544,10 @@ def extra_configs(torch, device, stream, args, dist, keep):
     return out
 
 
-def nosync_config(torch, device, stream, steps, warm, dist):
+def nosync_config(torch, device, stream, steps, warm, dist, K=8):
     from reduction_reducer_gb300 import Reducer
     numel = shapes.numels(shapes.resnet50())
-    W, K = 16, 8
+    W = 16
     N = sum(numel)
     offs, total = gen.packed_offsets(numel, 64)
     fresh = [[gen.draw_flat_torch(total, r, k, "f32", device) for r in range(W)] for k in range(K)]
@@ -503,17 +558,20 @@ def nosync_config(torch, device, stream, steps, warm, dist):
     arena = torch.empty(red.arena_numel(), device=device)
     out_flat = torch.empty(total, device=device)
     red.bind(acc, arena, [out_flat[o:o + n] for o, n in zip(offs, numel)])
+    import ctypes
     order = gen.reverse_order(len(numel))
+    order_c = (ctypes.c_int32 * len(order))(*order)
+    acc_p = red.pointers(acc)                       # marshalled once, reused every call
+    fresh_p = [red.pointers(fv) for fv in fresh_v]
 
     def cycle():
         for k in range(K):
-            red.accumulate_nosync(acc, fresh_v[k], first_step=(k == 0), stream=stream)
+            red.accumulate_nosync(acc_p, fresh_p[k], first_step=(k == 0), stream=stream)
         red.begin_iteration()
-        for v in order:
-            red.mark_ready(v, stream)
+        red.mark_ready_many(order_c, stream)
 
     def acc_only():
-        red.accumulate_nosync(acc, fresh_v[1], first_step=False, stream=stream)
+        red.accumulate_nosync(acc_p, fresh_p[1 % K], first_step=False, stream=stream)
 
     with torch.cuda.stream(stream):
         ms, _, _ = time_steps(torch, stream, cycle, steps, warm, dist)
@@ -524,7 +582,8 @@ def nosync_config(torch, device, stream, steps, warm, dist):
            "bytes_per_cycle": cycle_bytes, "W": W, "K": K,
            "accumulate_gbs": round(3 * W * N * 4 / (ms_acc / steps * 1e-3) / 1e9, 1),
            "accumulate_ms": round(ms_acc / steps, 4),
-           "note": "K accumulate micro-steps (first one a copy) + one hook-driven reduce"}
+           "kernel": ("bulk copy" if red.get_option(10) == 1 else "register streaming"),
+           "note": "K accumulate micro-steps (first one a copy) + one reduce (mark_ready_many)"}
     red.destroy()
     return res
 
@@ -540,12 +599,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--layers", type=int, default=None, help="smaller BERT (profiling case)")
+    ap.add_argument("--workload", default="bert_large", choices=["bert_large", "nosync_resnet50"],
+                    help="nosync_resnet50: the no_sync workload alone (profiling case)")
+    ap.add_argument("--nosync-k", type=int, default=8, help="micro-steps of --workload nosync_resnet50")
     ap.add_argument("--driver", default="hooks", choices=["hooks", "events", "all"])
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "nosync_resnet50":
+        return run_nosync_only(args)
     return run_ours(args)
 
 

@@ -164,5 +164,50 @@ __device__ __forceinline__ void store_vec(const ReduceParams& p, float* const* d
     }
 }
 
+// ------------------------------------------------------------------ accumulate parameters
+
+// The (acc, g) pairs of one accumulate launch travel in the kernel's
+// parameter block (32 B each; the block stays under 32 KiB).
+constexpr int kMaxAccPairs = 1000;
+
+struct AccPairDev {
+    const float* g;
+    float* acc;
+    long long off;   // start in the launch's flat space (multiple of 4)
+    long long len;
+};
+
+struct AccParams {
+    long long total;   // flat extent (last pair's padded end)
+    long long piece;   // elements per CTA, multiple of 4
+    int npairs;
+    int first;         // 1: acc = g; 0: acc = fl32(acc + g)
+    int chain;         // 1: follows this call's previous accumulate launch
+    int stages;        // bulk-copy variant: ring depth
+    int tile;          // bulk-copy variant: elements per operand per stage (multiple of 4)
+    int* status;       // bulk-copy variant: device status word
+    AccPairDev pair[kMaxAccPairs];
+};
+
+// Largest i with pair[i].off <= x (pair[0].off = 0 <= x); 32-ary warp-ballot
+// search over the pairs' flat offsets.  Call with the whole warp converged.
+__device__ __forceinline__ int find_pair(const AccParams& p, long long x) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0;
+    int n = p.npairs;
+    while (n > 32) {
+        const int stride = (n + 31) >> 5;
+        const int idx = lo + lane * stride;
+        const bool le = idx < p.npairs && p.pair[idx].off <= x;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        lo += (31 - __clz(m)) * stride;
+        n = min(stride, p.npairs - lo);
+    }
+    const int idx = lo + lane;
+    const bool le = lane < n && p.pair[idx].off <= x;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    return lo + 31 - __clz(m);
+}
+
 }  // namespace dev
 }  // namespace ddpk

@@ -146,6 +146,7 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->cfg.stages = c->opt_stages;
     c->cfg.stage_bytes = c->opt_stage_bytes;
     c->cfg.tma_ctas_per_sm = c->opt_tma_ctas;
+    c->cfg.status = c->tab.status;
 
     c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->opt_block);
     return DDP_OK;

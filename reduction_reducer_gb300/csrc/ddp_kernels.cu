@@ -172,42 +172,6 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
 
 // ------------------------------------------------------------------ accumulate kernel
 
-constexpr int kMaxAccPairs = 1000;   // 32 B each: the parameter block stays < 32 KiB
-
-struct AccPairDev {
-    const float* g;
-    float* acc;
-    long long off;   // start in the launch's flat space (multiple of 4)
-    long long len;
-};
-
-struct AccParams {
-    long long total;   // flat extent (last pair's padded end)
-    long long piece;   // elements per CTA, multiple of 4
-    int npairs;
-    int first;
-    int chain;         // 1: follows this call's previous accumulate launch
-    AccPairDev pair[kMaxAccPairs];
-};
-
-__device__ __forceinline__ int find_pair(const AccParams& p, long long x) {
-    const int lane = threadIdx.x & 31;
-    int lo = 0;
-    int n = p.npairs;
-    while (n > 32) {
-        const int stride = (n + 31) >> 5;
-        const int idx = lo + lane * stride;
-        const bool le = idx < p.npairs && p.pair[idx].off <= x;
-        const unsigned m = __ballot_sync(0xffffffffu, le);
-        lo += (31 - __clz(m)) * stride;
-        n = min(stride, p.npairs - lo);
-    }
-    const int idx = lo + lane;
-    const bool le = lane < n && p.pair[idx].off <= x;
-    const unsigned m = __ballot_sync(0xffffffffu, le);
-    return lo + 31 - __clz(m);
-}
-
 __global__ void __launch_bounds__(kMaxBlock)
 accumulate_kernel(const __grid_constant__ AccParams p) {
     pdl_enter(p.chain);
@@ -364,6 +328,7 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
 
 cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
                               cudaStream_t stream, long long* launches) {
+    if (cfg.kernel == KERNEL_TMA) return launch_accumulate_tma(pairs, n, first, cfg, stream, launches);
     thread_local AccParams p;   // ~32 KiB: kept off the stack, one per host thread
     int i = 0;
     int issued = 0;

@@ -37,6 +37,7 @@ struct LaunchCfg {
     int stage_bytes;   // bulk-copy kernel: bytes of all replicas' tiles per stage
     int tma_ctas_per_sm;
     int chain;                  // per launch: see pdl_enter in ddp_device.cuh
+    int* status;                // device status word of the binding (bulk-copy kernels)
 };
 
 enum InType { IN_F32 = 0, IN_BF16 = 1 };
@@ -57,11 +58,16 @@ struct AccPair {
     long long len;
 };
 
-// acc = g (first != 0) or acc = fl32(acc + g) for every pair.
+// acc = g (first != 0) or acc = fl32(acc + g) for every pair; the bulk-copy
+// variant when cfg.kernel is KERNEL_TMA.
 cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
                               cudaStream_t stream, long long* launches);
 
 int accumulate_max_ctas_per_sm(int block);
+
+// Bulk-copy (TMA) pipelined variant of launch_accumulate, in ddp_kernels_tma.cu.
+cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+                                  cudaStream_t stream, long long* launches);
 
 // Bulk-copy (TMA) pipelined variant of launch_reduce, in ddp_kernels_tma.cu.
 cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,

@@ -242,6 +242,133 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
         });
 }
 
+// ------------------------------------------------------------------ accumulate
+
+// Walk the CTA's slice [x, y) of an accumulate launch's flat space starting
+// at pair i: aligned runs of 16-byte-aligned pairs in chunks of at most
+// p.tile elements go to `body(i, c, L)`, the rest to `scalar(i, lo, hi)`.
+// Padding between pairs (each pair starts at a multiple of 4) is skipped.
+template <typename Body, typename Scalar>
+__device__ __forceinline__ void walk_pairs(const AccParams& p, int i, long long x, long long y, Body&& body,
+                                           Scalar&& scalar) {
+    while (x < y && i < p.npairs) {
+        const AccPairDev& q = p.pair[i];
+        const long long end = q.off + q.len;
+        const long long e = end < y ? end : y;
+        if (x < e) {
+            const bool vec = ((reinterpret_cast<uintptr_t>(q.g) | reinterpret_cast<uintptr_t>(q.acc)) & 15u) == 0;
+            const long long xb = (x + 3) / 4 * 4;
+            const long long xe = e / 4 * 4;
+            if (vec && xb < xe) {
+                if (x < xb) scalar(i, x, xb);
+                for (long long c = xb; c < xe; c += p.tile) body(i, c, xe - c < p.tile ? xe - c : p.tile);
+                if (xe < e) scalar(i, xe, e);
+            } else {
+                scalar(i, x, e);
+            }
+        }
+        x = end > x ? end : x;
+        ++i;
+        if (i < p.npairs && p.pair[i].off > x) x = p.pair[i].off;
+    }
+}
+
+// no_sync micro-step through the bulk-copy ring: per chunk, the producer
+// copies the g tile (and, after the first step, the acc tile) into a stage;
+// consumers add in fp32 (acc + g, or take g) and store acc with 128-bit
+// evict-first stores.
+__global__ void __launch_bounds__(kThreads, 1)
+accumulate_tma_kernel(const __grid_constant__ AccParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + S;
+    float* ring = reinterpret_cast<float*>(smem + kHeaderBytes);
+    const long long stage_elems = 2LL * p.tile;   // [g tile | acc tile]
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_enter(p.chain);
+
+    long long x = static_cast<long long>(blockIdx.x) * p.piece;
+    long long y = x + p.piece;
+    y = y > p.total ? p.total : y;
+    if (x >= y) {
+        if (threadIdx.x == 0) pdl_exit(p.chain);
+        return;
+    }
+    const int i0 = find_pair(p, x);
+
+    if (warp == 0) {
+        if (lane != 0) return;
+        long long k = 0;
+        bool failed = false;
+        walk_pairs(
+            p, i0, x, y,
+            [&](int i, long long c, long long L) {
+                const int st = static_cast<int>(k % S);
+                const uint32_t use = static_cast<uint32_t>(k / S);
+                if (use > 0) mbar_wait(smem_u32(empty + st), (use - 1) & 1u, p.status, kStatusEmptyTimeout, failed);
+                const uint32_t bytes = static_cast<uint32_t>(L * sizeof(float));
+                const uint32_t fb = smem_u32(full + st);
+                mbar_expect_tx(fb, p.first ? bytes : 2u * bytes);
+                const AccPairDev& q = p.pair[i];
+                float* dst = ring + st * stage_elems;
+                bulk_g2s(smem_u32(dst), q.g + (c - q.off), bytes, fb);
+                if (!p.first) bulk_g2s(smem_u32(dst + p.tile), q.acc + (c - q.off), bytes, fb);
+                ++k;
+            },
+            [](int, long long, long long) {});
+        for (long long j = k > S ? k - S : 0; j < k; ++j)
+            mbar_wait(smem_u32(full + j % S), static_cast<uint32_t>(j / S) & 1u, p.status, kStatusDrainTimeout, failed);
+        pdl_exit(p.chain);
+        return;
+    }
+
+    const int tc = threadIdx.x - 32;
+    constexpr int nct = kConsumerWarps * 32;
+    long long k = 0;
+    bool failed = false;
+    walk_pairs(
+        p, i0, x, y,
+        [&](int i, long long c, long long L) {
+            const int st = static_cast<int>(k % S);
+            const uint32_t use = static_cast<uint32_t>(k / S);
+            mbar_wait(smem_u32(full + st), use & 1u, p.status, kStatusFullTimeout, failed);
+            const float* gt = ring + st * stage_elems;
+            const float* at = gt + p.tile;
+            float* acc = p.pair[i].acc + (c - p.pair[i].off);
+            const int nv = static_cast<int>(L / 4);
+            for (int v = tc; v < nv; v += nct) {
+                const float4 g = *reinterpret_cast<const float4*>(gt + 4 * v);
+                if (p.first) {
+                    st_stream(acc + 4 * v, g);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4*>(at + 4 * v);
+                    st_stream(acc + 4 * v, make_float4(__fadd_rn(a.x, g.x), __fadd_rn(a.y, g.y),
+                                                       __fadd_rn(a.z, g.z), __fadd_rn(a.w, g.w)));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(empty + st));
+            ++k;
+        },
+        [&](int i, long long lo, long long hi) {
+            const AccPairDev& q = p.pair[i];
+            for (long long a = lo + tc; a < hi; a += nct) {
+                const long long j = a - q.off;
+                q.acc[j] = p.first ? q.g[j] : __fadd_rn(q.acc[j], q.g[j]);
+            }
+        });
+}
+
 using TmaKernel = void (*)(ReduceParams);
 
 TmaKernel pick_tma(InType in, int W) {
@@ -266,9 +393,10 @@ TmaKernel pick_tma(InType in, int W) {
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // The dynamic shared-memory limit is raised once per kernel and device.
-cudaError_t ensure_smem_attr(TmaKernel k) {
+template <typename K>
+cudaError_t ensure_smem_attr(K k) {
     constexpr int kSlots = 64;
-    static TmaKernel done_k[kSlots];
+    static K done_k[kSlots];
     static int done_dev[kSlots];
     static int n_done = 0;
     int dev = 0;
@@ -290,6 +418,63 @@ cudaError_t ensure_smem_attr(TmaKernel k) {
 }
 
 }  // namespace
+
+cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+                                  cudaStream_t stream, long long* launches) {
+    thread_local AccParams p;   // ~32 KiB: kept off the stack, one per host thread
+    const int stages = cfg.stages < 2 ? 2 : cfg.stages;
+    long long tile = static_cast<long long>(cfg.stage_bytes) / (2 * static_cast<long long>(sizeof(float))) / 4 * 4;
+    if (tile < 4) tile = 4;
+    while (tile > 4 && kHeaderBytes + stages * 2 * tile * static_cast<long long>(sizeof(float)) > kMaxDynSmem) tile -= 4;
+    const long long smem = kHeaderBytes + stages * 2 * tile * static_cast<long long>(sizeof(float));
+    if (smem > kMaxDynSmem || 2 * stages * 8 > kHeaderBytes) return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem_attr(accumulate_tma_kernel);
+    if (e != cudaSuccess) return e;
+    int i = 0;
+    int issued = 0;
+    while (i < n) {
+        p.npairs = 0;
+        p.first = first;
+        p.chain = cfg.pdl && issued > 0 ? 1 : 0;
+        p.stages = stages;
+        p.tile = static_cast<int>(tile);
+        p.status = cfg.status;
+        long long off = 0;
+        while (i < n && p.npairs < kMaxAccPairs) {
+            if (pairs[i].len > 0) {
+                AccPairDev& d = p.pair[p.npairs++];
+                d.g = pairs[i].g;
+                d.acc = pairs[i].acc;
+                d.off = off;
+                d.len = pairs[i].len;
+                off += (pairs[i].len + 3) / 4 * 4;
+            }
+            ++i;
+        }
+        if (p.npairs == 0) continue;
+        p.total = off;
+        long long grid = static_cast<long long>(cfg.sms) * (cfg.tma_ctas_per_sm > 0 ? cfg.tma_ctas_per_sm : 1);
+        grid = grid < ceil_div(off, tile) ? grid : ceil_div(off, tile);
+        if (grid < 1) grid = 1;
+        p.piece = ceil_div(ceil_div(off, grid), 4) * 4;
+        grid = ceil_div(off, p.piece);
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(static_cast<unsigned>(grid));
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = static_cast<size_t>(smem);
+        lc.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = attr;
+        lc.numAttrs = cfg.pdl ? 1 : 0;
+        e = cudaLaunchKernelEx(&lc, accumulate_tma_kernel, p);
+        if (e != cudaSuccess) return e;
+        ++issued;
+        if (launches) ++*launches;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
                               long long lo, long long hi, int s0, int s1, float inv_w,

@@ -203,10 +203,16 @@ class Reducer:
                                                     _stream(stream)))
 
     # ---------------------------------------------------------------- no_sync
+    @staticmethod
+    def pointers(replicas):
+        """W lists of P tensors -> a reusable array of W*P device addresses
+        (marshalling done once instead of on every call)."""
+        return _ptr_array([_ptr(t) for rep in replicas for t in rep])
+
     def accumulate_nosync(self, acc, g, first_step: bool, stream=None):
-        """acc, g: W lists of P fp32 tensors."""
-        a = _ptr_array([_ptr(t) for rep in acc for t in rep])
-        b = _ptr_array([_ptr(t) for rep in g for t in rep])
+        """acc, g: W lists of P fp32 tensors, or arrays from ``pointers``."""
+        a = acc if isinstance(acc, C.Array) else self.pointers(acc)
+        b = g if isinstance(g, C.Array) else self.pointers(g)
         self._check(self.lib.ddp_accumulate_nosync(self._h, a, b, 1 if first_step else 0, _stream(stream)))
 
     # ---------------------------------------------------------------- options

@@ -319,7 +319,8 @@ def test_gpt2_reduced_caps_every_element(cap_mib, kernel):
     full_compare(numel, 8, "bf16", cap_mib * MIB, order="reverse", n_out=1, kernel=kernel)
 
 
-def test_nosync_small_every_element():
+@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+def test_nosync_small_every_element(kernel):
     numel = RAGGED
     W, K = 3, 4
     steps_np = [host_grads(numel, W, "f32", step=k)[1] for k in range(K)]
@@ -333,6 +334,7 @@ def test_nosync_small_every_element():
         dev_steps.append(host_to_device_views(fl, numel, offs, "f32", DEV)[1])
     acc_dev = [[torch.full((n,), float("nan"), device=DEV) for n in numel] for _ in range(W)]
     red = Reducer(numel, "f32", 64 * 1024)
+    set_kernel(red, kernel)
     arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
     outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
     red.bind(acc_dev, arena, outs)
@@ -342,6 +344,7 @@ def test_nosync_small_every_element():
     for v in gen.reverse_order(len(numel)):
         red.mark_ready(v)
     torch.cuda.synchronize()
+    assert red.device_status() == 0
     for r in range(W):
         for v in range(len(numel)):
             assert bits_equal(acc_dev[r][v].cpu().numpy(), acc_np[r][v])
@@ -473,3 +476,28 @@ def test_automatic_kernel_choice():
         return k
     assert chosen(shapes.numels(shapes.bert_large()), "f32", 25 * MIB) == _lib.KERNEL_TMA
     assert chosen(shapes.numels(shapes.gpt2_medium()), "bf16", 0) == _lib.KERNEL_LDG
+
+
+@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+def test_nosync_misaligned_and_special(kernel):
+    """Accumulators and gradients at odd offsets (no 16-byte alignment) and
+    special values: scalar paths, first step copies bits (incl. -0.0)."""
+    numel = RAGGED
+    W, K = 2, 3
+    steps = [host_grads(numel, W, "f32", step=k, odd=True, special=True) for k in range(K)]
+    offs = steps[0][2]
+    acc_np = [accumulate_steps([steps[k][1][r] for k in range(K)]) for r in range(W)]
+    dev_steps = [host_to_device_views(steps[k][0], numel, offs, "f32", DEV)[1] for k in range(K)]
+    acc_off, acc_total = layout(numel, 64, odd=True)
+    acc_flat = [torch.full((acc_total,), float("nan"), device=DEV) for _ in range(W)]
+    acc_dev = [[f[o:o + n] for o, n in zip(acc_off, numel)] for f in acc_flat]
+    red = Reducer(numel, "f32", 64 * 1024)
+    set_kernel(red, kernel)
+    red.bind(acc_dev, torch.empty(red.arena_numel() + 4, device=DEV), None)
+    for k in range(K):
+        red.accumulate_nosync(acc_dev, dev_steps[k], first_step=(k == 0))
+    torch.cuda.synchronize()
+    assert red.device_status() == 0
+    for r in range(W):
+        for v in range(len(numel)):
+            assert bits_equal(acc_dev[r][v].cpu().numpy(), acc_np[r][v]), (r, v)
