@@ -442,7 +442,7 @@ def run_ours(args):
     return 0
 
 
-def measure_e2e(torch, wl, stream, steps, dist):
+def measure_e2e(torch, wl, stream, steps, dist, n_h2d=2, n_d2h=1):
     """Same metric through the public API with host buffers.  Every step
     copies the W replicas' gradients from pinned host memory and reads the
     averaged gradients back to pinned host memory, pipelined per bucket the
@@ -456,8 +456,9 @@ def measure_e2e(torch, wl, stream, steps, dist):
     for h, f in zip(host_in, wl.flat):
         h.copy_(f)
     host_out = torch.empty(wl.out_flat.numel(), dtype=torch.float32, pin_memory=True)
-    h2d_stream = torch.cuda.Stream(device=stream.device)
-    d2h_stream = torch.cuda.Stream(device=stream.device)
+    # several copy streams: one copy engine alone does not fill the host link
+    h2d_streams = [torch.cuda.Stream(device=stream.device) for _ in range(n_h2d)]
+    d2h_streams = [torch.cuda.Stream(device=stream.device) for _ in range(n_d2h)]
     out_offs, _ = gen.packed_offsets(wl.numel, 64)
     buckets = []
     for members in wl.red.get_members():
@@ -468,30 +469,35 @@ def measure_e2e(torch, wl, stream, steps, dist):
         buckets.append((lo, hi, olo, ohi, vars_c, len(members)))
     h2d = sum((hi - lo) * f.element_size() for (lo, hi, *_) in buckets for f in wl.flat)
     d2h = sum((ohi - olo) * 4 for (_, _, olo, ohi, *_) in buckets)
-    ev_in = [torch.cuda.Event() for _ in buckets]
+    ev_in = [[torch.cuda.Event() for _ in h2d_streams] for _ in buckets]
     ev_red = [torch.cuda.Event() for _ in buckets]
     red = wl.red
 
     def one():
         begin = torch.cuda.Event()
         begin.record(stream)
-        h2d_stream.wait_event(begin)
-        with torch.cuda.stream(h2d_stream):
-            for b, (lo, hi, *_rest) in enumerate(buckets):
-                for h, f in zip(host_in, wl.flat):
+        for hs in h2d_streams:
+            hs.wait_event(begin)
+        for b, (lo, hi, *_rest) in enumerate(buckets):
+            for r, (h, f) in enumerate(zip(host_in, wl.flat)):
+                with torch.cuda.stream(h2d_streams[r % n_h2d]):
                     f[lo:hi].copy_(h[lo:hi], non_blocking=True)
-                ev_in[b].record(h2d_stream)
+            for i, hs in enumerate(h2d_streams):
+                ev_in[b][i].record(hs)
         red.begin_iteration()
         for b, (lo, hi, olo, ohi, vars_c, n) in enumerate(buckets):
-            stream.wait_event(ev_in[b])
+            for ev in ev_in[b]:
+                stream.wait_event(ev)
             red.mark_ready_many(vars_c, stream)
             ev_red[b].record(stream)
-            d2h_stream.wait_event(ev_red[b])
-            with torch.cuda.stream(d2h_stream):
+            ds = d2h_streams[b % n_d2h]
+            ds.wait_event(ev_red[b])
+            with torch.cuda.stream(ds):
                 host_out[olo:ohi].copy_(wl.out_flat[olo:ohi], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(d2h_stream)
-        stream.wait_event(done)
+        for ds in d2h_streams:
+            done = torch.cuda.Event()
+            done.record(ds)
+            stream.wait_event(done)
 
     with torch.cuda.stream(stream):
         ms, _, _ = time_steps(torch, stream, one, steps, 1, dist)
@@ -501,7 +507,8 @@ def measure_e2e(torch, wl, stream, steps, dist):
             "h2d_gbs": round(h2d / (ms_step * 1e-3) / 1e9, 1),
             "note": ("algorithmic bytes of the step / time of a step that copies the replicas' gradients "
                      "host->device per bucket, reduces each bucket as it lands (mark_ready_many per bucket) "
-                     "and copies its averaged gradients back; pinned host buffers, copies on two streams")}
+                     f"and copies its averaged gradients back; pinned host buffers, {n_h2d} host->device and "
+                     f"{n_d2h} device->host copy streams")}
 
 
 def extra_configs(torch, device, stream, args, dist, keep):
