@@ -161,6 +161,26 @@ int ddp_reduce_all(ddp_ctx* ctx, void* stream);
 int ddp_get_progress(const ddp_ctx* ctx, int32_t* next_bucket, int32_t* parked,
                      int32_t* n_parked);
 
+/* ---------------------------------------------------------------- rebuild */
+
+/* The ready events of the last finished iteration, in order (the hooks'
+ * record of the actual gradient-ready order; "NCCL 专家课程 30", section
+ * "第一次迭代为何不同").  order: host array [P] or NULL; *n receives the count
+ * (P when every variable reported through ddp_mark_ready/_many; fewer when
+ * buckets went out through explicit launches). */
+int ddp_get_ready_trace(const ddp_ctx* ctx, int32_t* order, int32_t* n);
+
+/* Re-pack the buckets in a recorded ready order (same source): walk `order`
+ * (host array [P], every variable once; NULL = the last finished iteration's
+ * trace), append whole tensors, close a bucket once its bytes reach
+ * first_cap_bytes (bucket 0) or cap_bytes (every later bucket).  Call between
+ * iterations.  Locators, bucket count and arena layout change (the arena size
+ * does not); a bound context keeps its pointers and gets a new device segment
+ * table (synchronous).
+ * Errors: INVALID_ARG (inside an iteration, not a permutation, no complete
+ * trace, negative caps), CUDA, NO_MEMORY. */
+int ddp_rebuild_buckets(ddp_ctx* ctx, const int32_t* order, int64_t first_cap_bytes, int64_t cap_bytes);
+
 /* ---------------------------------------------------------------- no_sync */
 
 /* One local accumulation micro-step for all W replicas ("PyTorch Distributed",

@@ -26,7 +26,8 @@ def accumulate(acc, g, first_step: bool):
     """One micro-step for one replica's list of per-variable arrays."""
     if first_step:
         return [np.array(x, dtype=np.float32, copy=True) for x in g]
-    return [a + x for a, x in zip(acc, g)]
+    with np.errstate(invalid="ignore", over="ignore"):     # IEEE results, no warnings
+        return [a + x for a, x in zip(acc, g)]
 
 
 def accumulate_steps(steps):

@@ -48,8 +48,14 @@ struct ddp_ctx {
     std::vector<uint8_t> ready;
     int32_t next = 0;
 
+    int64_t first_cap = 0;
+    std::vector<int32_t> trace_cur;               // ready events of the current iteration
+    std::vector<int32_t> trace_last;              // ... of the last finished iteration
+
     // ---- binding
     bool bound = false;
+    std::vector<const void*> bind_grads;          // W*P, kept for rebuilds
+    std::vector<float*> bind_outs;                // n_out*P
     int W = 0;
     int n_out = 0;
     int device = -1;
@@ -107,6 +113,47 @@ void start_iteration(ddp_ctx* c) {
     reset_iteration(c);
     c->active = c->B > 0;
     c->iter_launches = 0;
+    c->trace_cur.clear();
+}
+
+// The iteration launched its last bucket: keep its ready order for a rebuild.
+void finish_iteration(ddp_ctx* c) {
+    c->active = false;
+    c->trace_last = c->trace_cur;
+}
+
+// Layout from a walk over `order` (every variable once): append, close the
+// bucket once its bytes reach the limit (first_cap for bucket 0, cap after).
+void assign_layout(ddp_ctx* c, const int32_t* order, int64_t first_cap, int64_t cap) {
+    c->members.clear();
+    c->loc.assign(c->P, ddp_locator{-1, -1, 0, 0});
+    std::vector<int32_t> cur;
+    int64_t size = 0;
+    for (int32_t i = 0; i < c->P; ++i) {
+        const int32_t v = order[i];
+        cur.push_back(v);
+        size += c->numel[v] * c->elem;
+        const int64_t limit = c->members.empty() ? first_cap : cap;
+        if (size >= limit) {
+            c->members.push_back(std::move(cur));
+            cur.clear();
+            size = 0;
+        }
+    }
+    if (!cur.empty()) c->members.push_back(std::move(cur));
+    c->B = static_cast<int32_t>(c->members.size());
+    c->bucket_off.assign(c->B + 1, 0);
+    for (int32_t b = 0; b < c->B; ++b) {
+        int64_t off = 0;
+        for (size_t i = 0; i < c->members[b].size(); ++i) {
+            const int32_t v = c->members[b][i];
+            c->loc[v] = ddp_locator{b, static_cast<int32_t>(i), off, c->numel[v]};
+            off += c->numel[v];
+        }
+        c->bucket_off[b + 1] = c->bucket_off[b] + off;
+    }
+    c->cap = cap;
+    c->first_cap = first_cap;
 }
 
 // Starts an iteration implicitly when the previous one has finished.
@@ -197,7 +244,7 @@ int release(ddp_ctx* c, int32_t* launched, int32_t* n_launched, void* stream) {
     if (launched)
         for (int32_t b = first; b < c->next; ++b) launched[b - first] = b;
     if (n_launched) *n_launched = c->next - first;
-    if (c->next == c->B) c->active = false;
+    if (c->next == c->B) finish_iteration(c);
     return launch_range(c, first, c->next, stream);
 }
 
@@ -246,34 +293,11 @@ int ddp_build_buckets(const int64_t* numel, int32_t P, ddp_dtype grad_dtype, int
         c->elem = grad_dtype == DDP_F32 ? 4 : 2;
         c->cap = cap_bytes;
         c->numel.assign(numel, numel + P);
-        c->loc.assign(P, ddp_locator{-1, -1, 0, 0});
-
         // Walk the parameters in reverse registration order; close a bucket
         // as soon as its byte size reaches the cap (tensors never split).
-        std::vector<int32_t> cur;
-        int64_t size = 0;
-        for (int32_t v = P - 1; v >= 0; --v) {
-            cur.push_back(v);
-            size += c->numel[v] * c->elem;
-            if (size >= cap_bytes) {
-                c->members.push_back(std::move(cur));
-                cur.clear();
-                size = 0;
-            }
-        }
-        if (!cur.empty()) c->members.push_back(std::move(cur));
-        c->B = static_cast<int32_t>(c->members.size());
-
-        c->bucket_off.assign(c->B + 1, 0);
-        for (int32_t b = 0; b < c->B; ++b) {
-            int64_t off = 0;
-            for (size_t i = 0; i < c->members[b].size(); ++i) {
-                const int32_t v = c->members[b][i];
-                c->loc[v] = ddp_locator{b, static_cast<int32_t>(i), off, c->numel[v]};
-                off += c->numel[v];
-            }
-            c->bucket_off[b + 1] = c->bucket_off[b] + off;
-        }
+        std::vector<int32_t> order(P);
+        for (int32_t i = 0; i < P; ++i) order[i] = P - 1 - i;
+        assign_layout(c, order.data(), cap_bytes, cap_bytes);
         reset_iteration(c);
     } catch (const std::bad_alloc&) {
         delete c;
@@ -297,17 +321,15 @@ int ddp_get_bucket_info(const ddp_ctx* ctx, int32_t* B, int64_t* bucket_offsets)
     return DDP_OK;
 }
 
-int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_arena, float* const* grad_out,
-             int32_t n_out) {
-    if (!c) return DDP_ERR_INVALID_ARG;
-    if (W < 1) return fail(c, DDP_ERR_INVALID_ARG, "W must be >= 1");
-    if (n_out != 0 && n_out != 1 && n_out != W) return fail(c, DDP_ERR_INVALID_ARG, "n_out must be 0, 1 or W");
-    if (c->P > 0 && !grads) return fail(c, DDP_ERR_INVALID_ARG, "grads is NULL");
-    if (n_out > 0 && c->P > 0 && !grad_out) return fail(c, DDP_ERR_INVALID_ARG, "grad_out is NULL with n_out > 0");
+}  // extern "C"
+
+namespace {
+
+// Build the segment table of the current layout for the given pointers and
+// upload it (replacing any previous table).
+int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_arena, float* const* grad_out,
+                int32_t n_out) {
     const int64_t total = c->bucket_off[c->B];
-    if (total > 0 && !bucket_arena) return fail(c, DDP_ERR_INVALID_ARG, "bucket_arena is NULL");
-    if (!is_aligned16(reinterpret_cast<uintptr_t>(bucket_arena)))
-        return fail(c, DDP_ERR_INVALID_ARG, "bucket_arena must be 16-byte aligned");
 
     // Host segment table: merge consecutive members of a bucket whose
     // gradients (every replica) and outputs (every copy) are contiguous.
@@ -416,6 +438,73 @@ int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_aren
     return refresh_launch_cfg(c);
 }
 
+}  // namespace
+
+extern "C" {
+
+int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_arena, float* const* grad_out,
+             int32_t n_out) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (W < 1) return fail(c, DDP_ERR_INVALID_ARG, "W must be >= 1");
+    if (n_out != 0 && n_out != 1 && n_out != W) return fail(c, DDP_ERR_INVALID_ARG, "n_out must be 0, 1 or W");
+    if (c->P > 0 && !grads) return fail(c, DDP_ERR_INVALID_ARG, "grads is NULL");
+    if (n_out > 0 && c->P > 0 && !grad_out) return fail(c, DDP_ERR_INVALID_ARG, "grad_out is NULL with n_out > 0");
+    const int64_t total = c->bucket_off[c->B];
+    if (total > 0 && !bucket_arena) return fail(c, DDP_ERR_INVALID_ARG, "bucket_arena is NULL");
+    if (!is_aligned16(reinterpret_cast<uintptr_t>(bucket_arena)))
+        return fail(c, DDP_ERR_INVALID_ARG, "bucket_arena must be 16-byte aligned");
+    std::vector<const void*> g_copy;
+    std::vector<float*> o_copy;
+    try {
+        g_copy.assign(grads, grads + static_cast<int64_t>(W) * c->P);
+        if (n_out > 0) o_copy.assign(grad_out, grad_out + static_cast<int64_t>(n_out) * c->P);
+    } catch (const std::bad_alloc&) {
+        return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+    const int st = build_table(c, W, g_copy.data(), bucket_arena, o_copy.empty() ? nullptr : o_copy.data(), n_out);
+    if (st != DDP_OK) return st;
+    c->bind_grads = std::move(g_copy);
+    c->bind_outs = std::move(o_copy);
+    return DDP_OK;
+}
+
+int ddp_get_ready_trace(const ddp_ctx* c, int32_t* order, int32_t* n) {
+    if (!c || !n) return DDP_ERR_INVALID_ARG;
+    *n = static_cast<int32_t>(c->trace_last.size());
+    if (order) std::copy(c->trace_last.begin(), c->trace_last.end(), order);
+    return DDP_OK;
+}
+
+int ddp_rebuild_buckets(ddp_ctx* c, const int32_t* order, int64_t first_cap_bytes, int64_t cap_bytes) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (c->active) return fail(c, DDP_ERR_INVALID_ARG, "rebuild inside an unfinished iteration");
+    if (first_cap_bytes < 0 || cap_bytes < 0) return fail(c, DDP_ERR_INVALID_ARG, "negative cap");
+    std::vector<int32_t> ord;
+    try {
+        if (order) ord.assign(order, order + c->P);
+        else ord = c->trace_last;
+    } catch (const std::bad_alloc&) {
+        return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+    if (static_cast<int32_t>(ord.size()) != c->P)
+        return fail(c, DDP_ERR_INVALID_ARG, "the order must list every variable once (no complete recorded iteration)");
+    std::vector<uint8_t> seen(c->P, 0);
+    for (int32_t v : ord) {
+        if (v < 0 || v >= c->P || seen[v]) return fail(c, DDP_ERR_INVALID_ARG, "the order is not a permutation");
+        seen[v] = 1;
+    }
+    try {
+        assign_layout(c, ord.data(), first_cap_bytes, cap_bytes);
+    } catch (const std::bad_alloc&) {
+        return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+    reset_iteration(c);
+    c->active = false;
+    if (!c->bound) return DDP_OK;
+    return build_table(c, c->W, c->bind_grads.data(), c->arena, c->bind_outs.empty() ? nullptr : c->bind_outs.data(),
+                       c->n_out);
+}
+
 int ddp_begin_iteration(ddp_ctx* c) {
     if (!c) return DDP_ERR_INVALID_ARG;
     if (c->active)
@@ -442,6 +531,7 @@ int ddp_mark_ready(ddp_ctx* c, int32_t var, int32_t* launched, int32_t* n_launch
     ensure_started(c);
     if (c->ready[var]) return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready");
     c->ready[var] = 1;
+    c->trace_cur.push_back(var);
     const int32_t b = c->loc[var].bucket;
     if (--c->pending[b] == 0 && b == c->next) return release(c, launched, n_launched, stream);
     return DDP_OK;
@@ -460,6 +550,7 @@ int ddp_mark_ready_many(ddp_ctx* c, const int32_t* vars, int32_t n, int32_t* n_d
         if (c->ready[var])
             return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready at event " + std::to_string(i));
         c->ready[var] = 1;
+        c->trace_cur.push_back(var);
         const int32_t b = c->loc[var].bucket;
         if (--c->pending[b] == 0 && b == c->next) {
             const int st = release(c, nullptr, nullptr, stream);
@@ -495,7 +586,7 @@ int ddp_reduce_all(ddp_ctx* c, void* stream) {
         c->pending[b] = 0;
     }
     c->next = c->B;
-    c->active = false;
+    finish_iteration(c);
     return launch_range(c, first, c->B, stream);
 }
 

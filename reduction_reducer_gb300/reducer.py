@@ -180,6 +180,23 @@ class Reducer:
         self._check(self.lib.ddp_get_progress(self._h, C.byref(nxt), parked, C.byref(n)))
         return nxt.value, [parked[i] for i in range(n.value)]
 
+    # ---------------------------------------------------------------- rebuild
+    def get_ready_trace(self):
+        n = C.c_int32()
+        buf = (C.c_int32 * max(self.P, 1))()
+        self._check(self.lib.ddp_get_ready_trace(self._h, buf, C.byref(n)))
+        return [buf[i] for i in range(n.value)]
+
+    def rebuild_buckets(self, order=None, first_cap_bytes=None, cap_bytes=25 << 20):
+        """Re-pack in ``order`` (default: the last finished iteration's trace)."""
+        arr = None if order is None else (C.c_int32 * max(self.P, 1))(*order)
+        fc = cap_bytes if first_cap_bytes is None else first_cap_bytes
+        self._check(self.lib.ddp_rebuild_buckets(self._h, arr, int(fc), int(cap_bytes)))
+        B = C.c_int32()
+        self.lib.ddp_get_bucket_info(self._h, C.byref(B), None)
+        self.B = B.value
+        self._launched = (C.c_int32 * max(self.B, 1))()
+
     # ---------------------------------------------------------------- no allocation
     def reduce_all_noalloc(self, grads, bucket_arena, grad_out=None, stream=None):
         """Every bucket in one pass without any device allocation: for callers

@@ -216,3 +216,76 @@ def test_mark_ready_many_error_stops_at_event(lib):
         red.mark_ready_many([3, 2, 3, 1])
     # events before the failing one stay applied: buckets 0 and 1 are out
     assert red.get_progress() == (2, [])
+
+
+# ---------------------------------------------------------------- rebuild
+
+def test_trace_and_rebuild_match_oracle(lib):
+    from oracle.rebuild import rebuild_buckets
+    numel = [3, 0, 2, 5, 1, 4, 7]
+    for order in itertools.permutations(range(len(numel))):
+        if hash(order) % 7:                      # a seeded subset of the 5040 orders
+            continue
+        red = _make(numel, "f32", 12)
+        red.set_dry_run(True)
+        red.begin_iteration()
+        red.mark_ready_many(list(order))
+        assert red.get_ready_trace() == list(order)
+        for fc, cap in ((4, 12), (0, 8), (40, 4)):
+            red.rebuild_buckets(None, fc, cap)
+            members, locs = rebuild_buckets(numel, 4, list(order), fc, cap)
+            assert red.get_locators() == [(l.bucket, l.intra, l.offset, l.length) for l in locs]
+            assert red.B == len(members)
+            # the state machine now runs on the new layout
+            red.begin_iteration()
+            sm = ReadinessOracle(members)
+            sm.begin_iteration()
+            for v in order:
+                assert red.mark_ready(v) == sm.mark_ready(v)
+            assert red.get_ready_trace() == list(order)
+        red.destroy()
+
+
+def test_rebuild_bert_trace_and_page_layouts(lib):
+    from oracle.rebuild import rebuild_buckets
+    numel = shapes.numels(shapes.bert_large())
+    with open(os.path.join(GOLDEN, "bert_large_ready_order.txt")) as f:
+        order = [int(l) for l in f if l.strip() and not l.startswith("#")]
+    red = _make(numel, "f32", 25 << 20)
+    red.set_dry_run(True)
+    red.begin_iteration()
+    red.mark_ready_many(order)
+    red.rebuild_buckets(None, 1 << 20, 25 << 20)
+    _, locs = rebuild_buckets(numel, 4, order, 1 << 20, 25 << 20)
+    assert red.get_locators() == [(l.bucket, l.intra, l.offset, l.length) for l in locs]
+    # course page: 12 x 4 MiB, one 48 MiB bucket first, then 1 / 3 / 12 after the rebuild
+    n12 = [1 << 20] * 12
+    red = _make(n12, "f32", (1 << 63) - 1)
+    assert red.get_bucket_info() == (1, [0, 12 << 20])
+    red.set_dry_run(True)
+    red.begin_iteration()
+    red.mark_ready_many(list(range(11, -1, -1)))
+    for cap_mib, nb in ((64, 1), (16, 3), (4, 12)):
+        red.rebuild_buckets(None, cap_mib << 20, cap_mib << 20)
+        assert red.B == nb
+
+
+def test_rebuild_errors(lib):
+    from reduction_reducer_gb300 import InvalidArg
+    red = _make([1, 1, 1, 1], "f32", 4)
+    red.set_dry_run(True)
+    with pytest.raises(InvalidArg):
+        red.rebuild_buckets(None, 4, 4)           # no finished iteration yet
+    red.begin_iteration()
+    red.mark_ready(3)
+    with pytest.raises(InvalidArg):
+        red.rebuild_buckets([0, 1, 2, 3], 4, 4)   # inside an iteration
+    red.abort_iteration()
+    with pytest.raises(InvalidArg):
+        red.rebuild_buckets([0, 1, 1, 3], 4, 4)   # not a permutation
+    red.reduce_all()                              # explicit launch: no complete trace
+    assert red.get_ready_trace() == []
+    with pytest.raises(InvalidArg):
+        red.rebuild_buckets(None, 4, 4)
+    red.rebuild_buckets([0, 1, 2, 3], 8, 8)
+    assert red.get_members() == [[0, 1], [2, 3]]
