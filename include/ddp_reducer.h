@@ -161,6 +161,36 @@ int ddp_reduce_all(ddp_ctx* ctx, void* stream);
 int ddp_get_progress(const ddp_ctx* ctx, int32_t* next_bucket, int32_t* parked,
                      int32_t* n_parked);
 
+/* ---------------------------------------------------------------- unused parameters */
+
+/* Local-use bits of the replicas (find_unused_parameters; "Distributed Data
+ * Parallel" notes, "Forward pass"; "PyTorch Distributed" summary, the
+ * globally-unused bitmap).  used: host array [W*P], used[r*P+v] != 0 when
+ * replica r's backward produces a gradient for v (NULL = all used).  The bits
+ * are OR-ed into the bitmap that the next reduction uses (the bitmap also
+ * collects the no_sync micro-steps' bits, see ddp_accumulate_nosync_used) and
+ * that reduction then:
+ *   - counts a replica without the gradient as a zero-filled slice (+0.0 in
+ *     the rank-order sum; the mean is still over all W replicas);
+ *   - marks every variable used on no replica ready at its first event
+ *     (first mark_ready / explicit launch), before that event, so its bucket
+ *     can launch; reporting such a variable is DDP_ERR_ALREADY_READY;
+ *   - leaves the copy-back of such a variable untouched (its bucket slice
+ *     receives the reduced zeros).
+ * Needs DDP_OPT_FIND_UNUSED and a bound context.  Errors: INVALID_ARG,
+ * NOT_BOUND, NO_MEMORY. */
+int ddp_set_local_used(ddp_ctx* ctx, const uint8_t* used);
+
+/* ddp_accumulate_nosync with the micro-step's local-use bits (host array
+ * [W*P] or NULL = all used).  An unused (r, v) leaves acc untouched; a used
+ * one takes g when its field is still empty in this no_sync block
+ * (first_step != 0 starts a block: every field empty) and adds g otherwise.
+ * With DDP_OPT_FIND_UNUSED the bits are OR-ed into the bitmap of the next
+ * reduction ("PyTorch Distributed" summary, the conflict between no_sync and
+ * unused-parameter marking).  Non-NULL bits need DDP_OPT_FIND_UNUSED. */
+int ddp_accumulate_nosync_used(ddp_ctx* ctx, void* const* acc, const void* const* g, const uint8_t* used,
+                               int32_t first_step, void* stream);
+
 /* ---------------------------------------------------------------- rebuild */
 
 /* The ready events of the last finished iteration, in order (the hooks'
@@ -227,7 +257,8 @@ int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, fl
 /* ---------------------------------------------------------------- options, info */
 
 enum ddp_option {
-    DDP_OPT_DRY_RUN = 0,          /* 1: run the state machine, launch nothing (host tests) */
+    DDP_OPT_DRY_RUN = 0,          /* 1: run the state machine, launch nothing; ddp_bind records the
+                                     pointers without a device table (host tests) */
     DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 = occupancy maximum */
     DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
     DDP_OPT_BLOCK_THREADS = 3,    /* register-streaming kernel: 128 or 256 (default) */
@@ -247,8 +278,11 @@ enum ddp_option {
                                      the iteration's previous launch on the same stream starts at once and
                                      waits for it only before exiting; stream order still holds for any
                                      work after the iteration. */
-    DDP_OPT_QUERY_KERNEL = 10     /* read only (ddp_get_option): kernel the bound context launches,
+    DDP_OPT_QUERY_KERNEL = 10,    /* read only (ddp_get_option): kernel the bound context launches,
                                      0 or 1; -1 before ddp_bind */
+    DDP_OPT_FIND_UNUSED = 11      /* 1: track unused parameters (find_unused_parameters; default 0):
+                                     enables ddp_set_local_used and the local-use bits of
+                                     ddp_accumulate_nosync_used; segments are never merged; W <= 64 */
 };
 int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
 int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);

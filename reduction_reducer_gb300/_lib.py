@@ -27,7 +27,7 @@ STATUS = {
 
 OPT_DRY_RUN, OPT_CTAS_PER_SM, OPT_PDL, OPT_BLOCK_THREADS = 0, 1, 2, 3
 OPT_KERNEL, OPT_STAGES, OPT_STAGE_BYTES, OPT_TMA_CTAS_PER_SM = 4, 5, 6, 7
-OPT_AUTO_MIN_ELEMS, OPT_CHAINED, OPT_QUERY_KERNEL = 8, 9, 10
+OPT_AUTO_MIN_ELEMS, OPT_CHAINED, OPT_QUERY_KERNEL, OPT_FIND_UNUSED = 8, 9, 10, 11
 KERNEL_LDG, KERNEL_TMA, KERNEL_AUTO = 0, 1, 2
 
 
@@ -48,6 +48,9 @@ SIGNATURES = {
     "ddp_reduce_bucket": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p]),
     "ddp_reduce_all": (C.c_int, [C.c_void_p, C.c_void_p]),
     "ddp_get_progress": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+    "ddp_set_local_used": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint8)]),
+    "ddp_accumulate_nosync_used": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                                             C.POINTER(C.c_uint8), C.c_int32, C.c_void_p]),
     "ddp_get_ready_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "ddp_rebuild_buckets": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.c_int64, C.c_int64]),
     "ddp_accumulate_nosync": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ddp_kernels.h"
+
 namespace ddpk {
 namespace dev {
 
@@ -134,28 +136,49 @@ __device__ __forceinline__ void pdl_exit(int chain) {
     if (chain) pdl_wait();
 }
 
+// ------------------------------------------------------------------ replica masks
+
+// Local-use masks of a launch with unused parameters: bit r of bits[s - s0]
+// is set when replica r has a gradient for segment s (one parameter per
+// segment in this mode).  A clear bit makes the replica contribute +0.0 (its
+// zero-filled bucket slice) without loading anything; a segment with no bit
+// set is unused on every replica and its copy-back is not written.
+__device__ __forceinline__ unsigned long long seg_mask(const NoMask&, int) { return ~0ull; }
+__device__ __forceinline__ unsigned long long seg_mask(const SegMask& m, int rel) { return m.bits[rel]; }
+
+__device__ __forceinline__ bool has_replica(unsigned long long mk, int r) { return (mk >> r) & 1ull; }
+
+// Any replica uses the segment (W <= 64 in masked launches; ~0 otherwise).
+__device__ __forceinline__ bool any_replica(unsigned long long mk, int W) {
+    return W >= 64 ? mk != 0ull : (mk & ((1ull << W) - 1ull)) != 0ull;
+}
+
 // Rank-order fp32 mean of one element, scalar path (heads, tails, segments
 // whose pointers do not share the arena's 16-byte phase).
 template <typename Tin>
 __device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* const* src,
                                               float* const* dst, long long a0, long long x,
-                                              long long e, int W, int tid, int nthr) {
+                                              long long e, int W, int tid, int nthr,
+                                              unsigned long long mk = ~0ull) {
+    const bool write_dst = any_replica(mk, W);
     for (long long a = x + tid; a < e; a += nthr) {
         const long long j = a - a0;
-        float acc = widen1(src[0][j]);
-        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, widen1(src[r][j]));
+        float acc = has_replica(mk, 0) ? widen1(src[0][j]) : 0.0f;
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, has_replica(mk, r) ? widen1(src[r][j]) : 0.0f);
         const float m = __fmul_rn(acc, p.inv_w);
         p.arena[a] = m;
-        for (int o = 0; o < p.n_out; ++o) dst[o][j] = m;
+        if (write_dst)
+            for (int o = 0; o < p.n_out; ++o) dst[o][j] = m;
     }
 }
 
 template <int N>
 __device__ __forceinline__ void store_vec(const ReduceParams& p, float* const* dst, long long a,
-                                          long long j, const float (&m)[N]) {
+                                          long long j, const float (&m)[N], bool write_dst = true) {
 #pragma unroll
     for (int q = 0; q < N; q += 4)
         st_stream(p.arena + a + q, make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]));
+    if (!write_dst) return;
     for (int o = 0; o < p.n_out; ++o) {
         float* d = dst[o] + j;
 #pragma unroll
@@ -167,21 +190,22 @@ __device__ __forceinline__ void store_vec(const ReduceParams& p, float* const* d
 // ------------------------------------------------------------------ accumulate parameters
 
 // The (acc, g) pairs of one accumulate launch travel in the kernel's
-// parameter block (32 B each; the block stays under 32 KiB).
-constexpr int kMaxAccPairs = 1000;
+// parameter block (40 B each; the block stays under 32 KiB).
+constexpr int kMaxAccPairs = 800;
 
 struct AccPairDev {
     const float* g;
     float* acc;
     long long off;   // start in the launch's flat space (multiple of 4)
     long long len;
+    int assign;      // 1: acc = g (the gradient field was empty); 0: acc = fl32(acc + g)
+    int pad;
 };
 
 struct AccParams {
     long long total;   // flat extent (last pair's padded end)
     long long piece;   // elements per CTA, multiple of 4
     int npairs;
-    int first;         // 1: acc = g; 0: acc = fl32(acc + g)
     int chain;         // 1: follows this call's previous accumulate launch
     int stages;        // bulk-copy variant: ring depth
     int tile;          // bulk-copy variant: elements per operand per stage (multiple of 4)

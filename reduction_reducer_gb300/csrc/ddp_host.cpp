@@ -52,6 +52,16 @@ struct ddp_ctx {
     std::vector<int32_t> trace_cur;               // ready events of the current iteration
     std::vector<int32_t> trace_last;              // ... of the last finished iteration
 
+    // ---- unused parameters (DDP_OPT_FIND_UNUSED)
+    bool opt_find_unused = false;
+    std::vector<uint8_t> pending_used;            // W*P: OR of local-use bits since the last reduction
+    bool pending_set = false;
+    std::vector<uint8_t> iter_used;               // W*P: bits of the current iteration
+    std::vector<uint8_t> gused;                   // P: used on some replica
+    bool iter_masked = false;                     // some replica lacks some gradient
+    bool unused_marked = false;                   // globally unused variables marked ready
+    std::vector<uint8_t> has_grad;                // W*P: accumulator holds a gradient (no_sync block)
+
     // ---- binding
     bool bound = false;
     std::vector<const void*> bind_grads;          // W*P, kept for rebuilds
@@ -64,6 +74,8 @@ struct ddp_ctx {
     void* dev_table = nullptr;
     ddpk::SegTable tab{};
     std::vector<int32_t> bucket_seg;              // B+1 segment ranges
+    std::vector<int64_t> seg_off_h;               // host copy of the segment offsets (S+1)
+    std::vector<int32_t> seg_var;                 // first variable of each segment
 
     // ---- options and counters
     bool dry = false;
@@ -114,6 +126,32 @@ void start_iteration(ddp_ctx* c) {
     c->active = c->B > 0;
     c->iter_launches = 0;
     c->trace_cur.clear();
+    c->iter_masked = false;
+    c->unused_marked = false;
+    if (c->pending_set) {
+        // the local-use bits gathered since the last reduction serve this one
+        c->iter_used.swap(c->pending_used);
+        c->pending_used.assign(c->iter_used.size(), 0);
+        c->pending_set = false;
+        c->gused.assign(c->P, 0);
+        for (int r = 0; r < c->W; ++r)
+            for (int32_t v = 0; v < c->P; ++v) {
+                const uint8_t u = c->iter_used[static_cast<size_t>(r) * c->P + v];
+                c->gused[v] |= u;
+                if (!u) c->iter_masked = true;
+            }
+    }
+}
+
+// Globally unused variables count as ready from the iteration's first event.
+void mark_unused(ddp_ctx* c) {
+    if (!c->iter_masked || c->unused_marked) return;
+    c->unused_marked = true;
+    for (int32_t v = 0; v < c->P; ++v)
+        if (!c->gused[v] && !c->ready[v]) {
+            c->ready[v] = 1;
+            --c->pending[c->loc[v].bucket];
+        }
 }
 
 // The iteration launched its last bucket: keep its ready order for a rebuild.
@@ -169,7 +207,7 @@ void free_binding(ddp_ctx* c) {
 }
 
 int refresh_launch_cfg(ddp_ctx* c) {
-    if (!c->bound) return DDP_OK;
+    if (!c->bound || c->dry) return DDP_OK;
     int sms = 0;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e != cudaSuccess) return cuda_fail(c, e, "cudaDeviceGetAttribute");
@@ -225,14 +263,41 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
     // opted in (DDP_OPT_CHAINED).
     const bool follows_own = c->iter_launches > 0 && stream == c->iter_stream;
     cfg.chain = c->pdl && follows_own && (c->call_launches > 0 || c->opt_chain) ? 1 : 0;
-    long long n = 0;
-    cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, lo, hi, s0, s1, c->inv_w,
-                                        cfg, static_cast<cudaStream_t>(stream), &n);
-    c->launches += n;
-    c->iter_launches += n;
-    c->call_launches += n;
-    c->iter_stream = stream;
-    if (e != cudaSuccess) return cuda_fail(c, e, "bucket reduce launch");
+    if (!c->iter_masked) {
+        long long n = 0;
+        cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, lo, hi, s0, s1, c->inv_w,
+                                            cfg, static_cast<cudaStream_t>(stream), &n);
+        c->launches += n;
+        c->iter_launches += n;
+        c->call_launches += n;
+        c->iter_stream = stream;
+        if (e != cudaSuccess) return cuda_fail(c, e, "bucket reduce launch");
+        return DDP_OK;
+    }
+    // Unused parameters: the replicas' local-use masks travel in the launch's
+    // parameter block, at most kMaxMaskSegs segments per launch.
+    thread_local ddpk::SegMask mask;
+    for (int sa = s0; sa < s1; sa += ddpk::kMaxMaskSegs) {
+        const int sb = std::min(s1, sa + ddpk::kMaxMaskSegs);
+        mask.n = sb - sa;
+        for (int sg = sa; sg < sb; ++sg) {
+            const int32_t v = c->seg_var[sg];
+            unsigned long long bits = 0;
+            for (int r = 0; r < c->W; ++r)
+                if (c->iter_used[static_cast<size_t>(r) * c->P + v]) bits |= 1ull << r;
+            mask.bits[sg - sa] = bits;
+        }
+        if (sa > s0) cfg.chain = c->pdl ? 1 : 0;   // follows this call's previous launch
+        long long n = 0;
+        cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, c->seg_off_h[sa],
+                                            c->seg_off_h[sb], sa, sb, c->inv_w, cfg,
+                                            static_cast<cudaStream_t>(stream), &n, &mask);
+        c->launches += n;
+        c->iter_launches += n;
+        c->call_launches += n;
+        c->iter_stream = stream;
+        if (e != cudaSuccess) return cuda_fail(c, e, "bucket reduce launch (unused parameters)");
+    }
     return DDP_OK;
 }
 
@@ -339,6 +404,7 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
     std::vector<int32_t> seg_vec;
     std::vector<int32_t> bucket_seg(c->B + 1, 0);
     std::vector<int64_t> seg_len;
+    std::vector<int32_t> seg_var;
     try {
         for (int32_t b = 0; b < c->B; ++b) {
             bucket_seg[b] = static_cast<int32_t>(seg_off.size());
@@ -355,7 +421,8 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
                         return fail(c, DDP_ERR_INVALID_ARG, "NULL output for copy " + std::to_string(o) +
                                                                 " variable " + std::to_string(v));
                 const size_t S = seg_off.size();
-                bool merge = static_cast<int32_t>(S) > bucket_seg[b];
+                // with unused parameters every segment is one variable (one mask each)
+                bool merge = !c->opt_find_unused && static_cast<int32_t>(S) > bucket_seg[b];
                 if (merge) {
                     const int64_t plen = seg_len[S - 1];
                     for (int r = 0; r < W && merge; ++r) {
@@ -382,6 +449,7 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
                 }
                 seg_off.push_back(a0);
                 seg_len.push_back(n);
+                seg_var.push_back(v);
                 for (int r = 0; r < W; ++r) seg_src.push_back(grads[static_cast<int64_t>(r) * c->P + v]);
                 for (int o = 0; o < n_out; ++o) seg_dst.push_back(grad_out[static_cast<int64_t>(o) * c->P + v]);
                 seg_vec.push_back(vec ? 1 : 0);
@@ -391,6 +459,19 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
         seg_off.push_back(total);
     } catch (const std::bad_alloc&) {
         return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+
+    if (c->dry) {   // dry run: the host-side state only, no device table
+        free_binding(c);
+        c->bucket_seg = std::move(bucket_seg);
+        c->seg_off_h = seg_off;
+        c->seg_var = std::move(seg_var);
+        c->W = W;
+        c->n_out = n_out;
+        c->arena = bucket_arena;
+        c->inv_w = 1.0f / static_cast<float>(W);
+        c->bound = true;
+        return DDP_OK;
     }
 
     int dev = -1;
@@ -429,6 +510,8 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
     c->tab.seg_vec = reinterpret_cast<const int*>(base + b_off + b_src + b_dst);
     c->tab.status = reinterpret_cast<int*>(base + b_off + b_src + b_dst + b_vec);
     c->bucket_seg = std::move(bucket_seg);
+    c->seg_off_h = seg_off;
+    c->seg_var = std::move(seg_var);
     c->W = W;
     c->n_out = n_out;
     c->arena = bucket_arena;
@@ -461,10 +544,15 @@ int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_aren
     } catch (const std::bad_alloc&) {
         return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
     }
+    if (c->opt_find_unused && W > 64)
+        return fail(c, DDP_ERR_INVALID_ARG, "unused-parameter tracking supports W <= 64");
     const int st = build_table(c, W, g_copy.data(), bucket_arena, o_copy.empty() ? nullptr : o_copy.data(), n_out);
     if (st != DDP_OK) return st;
     c->bind_grads = std::move(g_copy);
     c->bind_outs = std::move(o_copy);
+    c->pending_used.clear();
+    c->pending_set = false;
+    c->has_grad.clear();
     return DDP_OK;
 }
 
@@ -529,11 +617,13 @@ int ddp_mark_ready(ddp_ctx* c, int32_t var, int32_t* launched, int32_t* n_launch
     if (var < 0 || var >= c->P) return fail(c, DDP_ERR_INVALID_ARG, "variable index out of range");
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "mark_ready before bind");
     ensure_started(c);
-    if (c->ready[var]) return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready");
+    if (c->ready[var] || (c->iter_masked && !c->gused[var]))
+        return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready");
+    mark_unused(c);
     c->ready[var] = 1;
     c->trace_cur.push_back(var);
-    const int32_t b = c->loc[var].bucket;
-    if (--c->pending[b] == 0 && b == c->next) return release(c, launched, n_launched, stream);
+    --c->pending[c->loc[var].bucket];
+    if (c->next < c->B && c->pending[c->next] == 0) return release(c, launched, n_launched, stream);
     return DDP_OK;
 }
 
@@ -547,12 +637,13 @@ int ddp_mark_ready_many(ddp_ctx* c, const int32_t* vars, int32_t n, int32_t* n_d
         const int32_t var = vars[i];
         if (var < 0 || var >= c->P) return fail(c, DDP_ERR_INVALID_ARG, "variable index out of range at event " + std::to_string(i));
         ensure_started(c);
-        if (c->ready[var])
+        if (c->ready[var] || (c->iter_masked && !c->gused[var]))
             return fail(c, DDP_ERR_ALREADY_READY, "variable " + std::to_string(var) + " already ready at event " + std::to_string(i));
+        mark_unused(c);
         c->ready[var] = 1;
         c->trace_cur.push_back(var);
-        const int32_t b = c->loc[var].bucket;
-        if (--c->pending[b] == 0 && b == c->next) {
+        --c->pending[c->loc[var].bucket];
+        if (c->next < c->B && c->pending[c->next] == 0) {
             const int st = release(c, nullptr, nullptr, stream);
             if (st != DDP_OK) return st;
         }
@@ -570,6 +661,7 @@ int ddp_reduce_bucket(ddp_ctx* c, int32_t bucket, void* stream) {
     if (bucket != c->next)
         return fail(c, DDP_ERR_OUT_OF_ORDER, "bucket " + std::to_string(bucket) + " is not next (next is " +
                                                  std::to_string(c->next) + ")");
+    mark_unused(c);
     for (int32_t v : c->members[bucket]) c->ready[v] = 1;
     c->pending[bucket] = 0;
     return release(c, nullptr, nullptr, stream);
@@ -603,23 +695,42 @@ int ddp_get_progress(const ddp_ctx* c, int32_t* next_bucket, int32_t* parked, in
     return DDP_OK;
 }
 
-int ddp_accumulate_nosync(ddp_ctx* c, void* const* acc, const void* const* g, int32_t first_step, void* stream) {
+int ddp_accumulate_nosync_used(ddp_ctx* c, void* const* acc, const void* const* g, const uint8_t* used,
+                               int32_t first_step, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
     if (c->dtype != DDP_F32) return fail(c, DDP_ERR_INVALID_ARG, "no_sync accumulation supports fp32 gradients only");
     if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "accumulate_nosync before bind (W unknown)");
     if (c->P > 0 && (!acc || !g)) return fail(c, DDP_ERR_INVALID_ARG, "acc or g is NULL");
+    if (used && !c->opt_find_unused)
+        return fail(c, DDP_ERR_INVALID_ARG, "local-use bits need DDP_OPT_FIND_UNUSED");
+    const size_t WP = static_cast<size_t>(c->W) * c->P;
     std::vector<ddpk::AccPair> pairs;
     try {
-        pairs.reserve(static_cast<size_t>(c->W) * c->P);
+        // A gradient field that is empty in this block takes the gradient;
+        // a filled one adds it.  Without a block record every field counts
+        // as filled after the first step.
+        if (first_step || c->has_grad.size() != WP) c->has_grad.assign(WP, first_step ? 0 : 1);
+        pairs.reserve(WP);
         for (int r = 0; r < c->W; ++r)
             for (int32_t v = 0; v < c->P; ++v) {
-                const int64_t i = static_cast<int64_t>(r) * c->P + v;
-                if (c->numel[v] == 0) continue;
+                const size_t i = static_cast<size_t>(r) * c->P + v;
+                if (used && !used[i]) continue;
+                if (c->numel[v] == 0) {
+                    c->has_grad[i] = 1;
+                    continue;
+                }
                 if (!acc[i] || !g[i])
                     return fail(c, DDP_ERR_INVALID_ARG, "NULL accumulator or gradient at replica " +
                                                             std::to_string(r) + " variable " + std::to_string(v));
-                pairs.push_back(ddpk::AccPair{static_cast<const float*>(g[i]), static_cast<float*>(acc[i]), c->numel[v]});
+                pairs.push_back(ddpk::AccPair{static_cast<const float*>(g[i]), static_cast<float*>(acc[i]),
+                                              c->numel[v], c->has_grad[i] ? 0 : 1});
+                c->has_grad[i] = 1;
             }
+        if (c->opt_find_unused) {   // the local-use bitmap accumulates until the next reduction
+            if (c->pending_used.size() != WP) c->pending_used.assign(WP, 0);
+            for (size_t i = 0; i < WP; ++i) c->pending_used[i] |= used ? (used[i] ? 1 : 0) : 1;
+            c->pending_set = true;
+        }
     } catch (const std::bad_alloc&) {
         return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
     }
@@ -629,10 +740,30 @@ int ddp_accumulate_nosync(ddp_ctx* c, void* const* acc, const void* const* g, in
     ddpk::LaunchCfg cfg = c->cfg;
     cfg.ctas_per_sm = c->acc_ctas;
     long long n = 0;
-    cudaError_t e = ddpk::launch_accumulate(pairs.data(), static_cast<int>(pairs.size()), first_step ? 1 : 0, cfg,
+    cudaError_t e = ddpk::launch_accumulate(pairs.data(), static_cast<int>(pairs.size()), cfg,
                                             static_cast<cudaStream_t>(stream), &n);
     c->launches += n;
     if (e != cudaSuccess) return cuda_fail(c, e, "accumulate launch");
+    return DDP_OK;
+}
+
+int ddp_accumulate_nosync(ddp_ctx* c, void* const* acc, const void* const* g, int32_t first_step, void* stream) {
+    return ddp_accumulate_nosync_used(c, acc, g, nullptr, first_step, stream);
+}
+
+int ddp_set_local_used(ddp_ctx* c, const uint8_t* used) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (!c->opt_find_unused) return fail(c, DDP_ERR_INVALID_ARG, "local-use bits need DDP_OPT_FIND_UNUSED");
+    if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "set_local_used before bind (W unknown)");
+    if (c->W > 64) return fail(c, DDP_ERR_INVALID_ARG, "unused-parameter tracking supports W <= 64");
+    const size_t WP = static_cast<size_t>(c->W) * c->P;
+    try {
+        if (c->pending_used.size() != WP) c->pending_used.assign(WP, 0);
+    } catch (const std::bad_alloc&) {
+        return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+    }
+    for (size_t i = 0; i < WP; ++i) c->pending_used[i] |= used ? (used[i] ? 1 : 0) : 1;
+    c->pending_set = true;
     return DDP_OK;
 }
 
@@ -657,6 +788,20 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             return DDP_OK;
         case DDP_OPT_QUERY_KERNEL:
             return fail(c, DDP_ERR_INVALID_ARG, "DDP_OPT_QUERY_KERNEL is read with ddp_get_option");
+        case DDP_OPT_FIND_UNUSED: {
+            if (c->active) return fail(c, DDP_ERR_INVALID_ARG, "find_unused changes between iterations only");
+            const bool on = value != 0;
+            if (on && c->bound && c->W > 64)
+                return fail(c, DDP_ERR_INVALID_ARG, "unused-parameter tracking supports W <= 64");
+            if (on == c->opt_find_unused) return DDP_OK;
+            c->opt_find_unused = on;
+            c->pending_used.clear();
+            c->pending_set = false;
+            c->has_grad.clear();
+            if (!c->bound) return DDP_OK;   // a bound context gets an unmerged (or merged) table now
+            return build_table(c, c->W, c->bind_grads.data(), c->arena,
+                               c->bind_outs.empty() ? nullptr : c->bind_outs.data(), c->n_out);
+        }
         case DDP_OPT_KERNEL:
             if (value != ddpk::KERNEL_LDG && value != ddpk::KERNEL_TMA && value != ddpk::KERNEL_AUTO)
                 return fail(c, DDP_ERR_INVALID_ARG, "kernel must be 0 (register streaming), 1 (bulk copy) or 2 (by size)");
@@ -714,6 +859,7 @@ int ddp_get_option(const ddp_ctx* c, int32_t option, int64_t* value) {
         case DDP_OPT_AUTO_MIN_ELEMS: *value = c->opt_auto_min; return DDP_OK;
         case DDP_OPT_CHAINED: *value = c->opt_chain; return DDP_OK;
         case DDP_OPT_QUERY_KERNEL: *value = c->bound ? c->cfg.kernel : -1; return DDP_OK;
+        case DDP_OPT_FIND_UNUSED: *value = c->opt_find_unused; return DDP_OK;
         default: return DDP_ERR_INVALID_ARG;
     }
 }

@@ -53,13 +53,19 @@ constexpr int kMaxBlock = 256;
 template <int WC>
 __host__ __device__ constexpr int unroll_for() { return WC <= 2 ? 4 : (WC <= 8 ? 2 : 1); }
 
+// A replica's 16-byte vector, or zeros when the replica has no gradient for
+// the segment (its zero-filled bucket slice).
+template <typename Raw>
+__device__ __forceinline__ Raw zero_raw() { return Raw{}; }
+
 // Vector body, W known at compile time: all WC x U loads in flight at once.
 template <typename Tin, int WC, int U>
 __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Tin* const* src,
                                                  float* const* dst, long long a0, long long kb,
-                                                 long long ke) {
+                                                 long long ke, unsigned long long mk) {
     using V = Vec<Tin>;
     constexpr int N = V::N;
+    const bool write_dst = any_replica(mk, WC);
     const Tin* s[WC];
 #pragma unroll
     for (int r = 0; r < WC; ++r) s[r] = src[r];
@@ -73,7 +79,9 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
                 const long long j = kk * N - a0;
 #pragma unroll
                 for (int r = 0; r < WC; ++r)
-                    raw[u][r] = ld_stream(reinterpret_cast<const typename V::Raw*>(s[r] + j));
+                    raw[u][r] = has_replica(mk, r)
+                                    ? ld_stream(reinterpret_cast<const typename V::Raw*>(s[r] + j))
+                                    : zero_raw<typename V::Raw>();
             }
         }
 #pragma unroll
@@ -90,7 +98,7 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
                 }
 #pragma unroll
                 for (int q = 0; q < N; ++q) acc[q] = __fmul_rn(acc[q], p.inv_w);
-                store_vec<N>(p, dst, kk * N, kk * N - a0, acc);
+                store_vec<N>(p, dst, kk * N, kk * N - a0, acc, write_dst);
             }
         }
     }
@@ -100,18 +108,24 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
 template <typename Tin>
 __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin* const* src,
                                                float* const* dst, long long a0, long long kb,
-                                               long long ke, int W) {
+                                               long long ke, int W, unsigned long long mk) {
     using V = Vec<Tin>;
     constexpr int N = V::N;
+    const bool write_dst = any_replica(mk, W);
     for (long long k = kb + threadIdx.x; k < ke; k += blockDim.x) {
         const long long j = k * N - a0;
         float acc[N], f[N];
-        V::unpack(ld_stream(reinterpret_cast<const typename V::Raw*>(src[0] + j)), acc);
+        V::unpack(has_replica(mk, 0) ? ld_stream(reinterpret_cast<const typename V::Raw*>(src[0] + j))
+                                     : zero_raw<typename V::Raw>(),
+                  acc);
         for (int r = 1; r < W; r += 4) {
             typename V::Raw raw[4];
 #pragma unroll
             for (int g = 0; g < 4; ++g)
-                if (r + g < W) raw[g] = ld_stream(reinterpret_cast<const typename V::Raw*>(src[r + g] + j));
+                if (r + g < W)
+                    raw[g] = has_replica(mk, r + g)
+                                 ? ld_stream(reinterpret_cast<const typename V::Raw*>(src[r + g] + j))
+                                 : zero_raw<typename V::Raw>();
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 if (r + g < W) {
@@ -123,13 +137,14 @@ __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin*
         }
 #pragma unroll
         for (int q = 0; q < N; ++q) acc[q] = __fmul_rn(acc[q], p.inv_w);
-        store_vec<N>(p, dst, k * N, j, acc);
+        store_vec<N>(p, dst, k * N, j, acc, write_dst);
     }
 }
 
-template <typename Tin, int WC>
+// M = NoMask (every replica has every gradient) or SegMask (unused parameters).
+template <typename Tin, int WC, typename M>
 __global__ void __launch_bounds__(kMaxBlock)
-bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
+bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_constant__ M mask) {
     pdl_enter(p.chain);
     using V = Vec<Tin>;
     constexpr int N = V::N;
@@ -152,17 +167,18 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p) {
         const long long e = a1 < y ? a1 : y;
         const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(s) * W;
         float* const* dst = p.seg_dst + static_cast<long long>(s) * p.n_out;
+        const unsigned long long mk = seg_mask(mask, s - p.s0);
         const long long kb = (x + N - 1) / N;   // first whole vector
         const long long ke = e / N;             // one past the last whole vector
         if (__ldg(p.seg_vec + s) && kb < ke) {
-            reduce_scalar<Tin>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x);
+            reduce_scalar<Tin>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x, mk);
             if constexpr (WC > 0)
-                reduce_vec_fixed<Tin, WC, U>(p, src, dst, a0, kb, ke);
+                reduce_vec_fixed<Tin, WC, U>(p, src, dst, a0, kb, ke, mk);
             else
-                reduce_vec_any<Tin>(p, src, dst, a0, kb, ke, W);
-            reduce_scalar<Tin>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x);
+                reduce_vec_any<Tin>(p, src, dst, a0, kb, ke, W, mk);
+            reduce_scalar<Tin>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x, mk);
         } else {
-            reduce_scalar<Tin>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x);
+            reduce_scalar<Tin>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x, mk);
         }
         x = e;
         ++s;
@@ -189,6 +205,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
         const long long end = q.off + q.len;
         const long long e = end < y ? end : y;
         if (x < e) {
+            const bool assign = q.assign != 0;
             const float* g = q.g - q.off;      // indexed by flat position
             float* acc = q.acc - q.off;
             const bool vec = ((reinterpret_cast<uintptr_t>(q.g) | reinterpret_cast<uintptr_t>(q.acc)) & 15u) == 0;
@@ -196,7 +213,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
             if (!vec || kb >= ke) { kb = ke = 0; }
             const long long sc_end = vec && kb < ke ? kb * 4 : e;
             for (long long a = x + threadIdx.x; a < sc_end; a += step)
-                acc[a] = p.first ? g[a] : __fadd_rn(acc[a], g[a]);
+                acc[a] = assign ? g[a] : __fadd_rn(acc[a], g[a]);
             constexpr int UA = 4;   // vectors per thread per iteration: 2 x 4 loads in flight
             for (long long k = kb + threadIdx.x; k < ke; k += UA * step) {
                 float4 gv[UA], cv[UA];
@@ -205,14 +222,14 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
                     const long long kk = k + u * step;
                     if (kk < ke) {
                         gv[u] = ld_stream(reinterpret_cast<const float4*>(g + 4 * kk));
-                        if (!p.first) cv[u] = __ldcs(reinterpret_cast<const float4*>(acc + 4 * kk));
+                        if (!assign) cv[u] = __ldcs(reinterpret_cast<const float4*>(acc + 4 * kk));
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < UA; ++u) {
                     const long long kk = k + u * step;
                     if (kk < ke) {
-                        if (p.first) {
+                        if (assign) {
                             st_stream(acc + 4 * kk, gv[u]);
                         } else {
                             st_stream(acc + 4 * kk, make_float4(__fadd_rn(cv[u].x, gv[u].x), __fadd_rn(cv[u].y, gv[u].y),
@@ -223,7 +240,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
             }
             if (vec && kb < ke)
                 for (long long a = ke * 4 + threadIdx.x; a < e; a += step)
-                    acc[a] = p.first ? g[a] : __fadd_rn(acc[a], g[a]);
+                    acc[a] = assign ? g[a] : __fadd_rn(acc[a], g[a]);
         }
         x = end > x ? end : x;
         // skip the padding up to the next pair's start
@@ -235,8 +252,8 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
 
 // ------------------------------------------------------------------ launch helpers
 
-template <typename Kernel, typename Params>
-cudaError_t launch(Kernel k, int grid, int block, const Params& params, bool pdl, cudaStream_t st) {
+template <typename Kernel, typename... Params>
+cudaError_t launch(Kernel k, int grid, int block, bool pdl, cudaStream_t st, const Params&... params) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(block));
@@ -247,27 +264,29 @@ cudaError_t launch(Kernel k, int grid, int block, const Params& params, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k, params);
+    return cudaLaunchKernelEx(&cfg, k, params...);
 }
 
-using ReduceKernel = void (*)(ReduceParams);
+template <typename M>
+using ReduceKernel = void (*)(ReduceParams, M);
 
-ReduceKernel pick_reduce(InType in, int W) {
+template <typename M>
+ReduceKernel<M> pick_reduce(InType in, int W) {
     if (in == IN_F32) {
         switch (W) {
-            case 2: return bucket_reduce_kernel<float, 2>;
-            case 4: return bucket_reduce_kernel<float, 4>;
-            case 8: return bucket_reduce_kernel<float, 8>;
-            case 16: return bucket_reduce_kernel<float, 16>;
-            default: return bucket_reduce_kernel<float, 0>;
+            case 2: return bucket_reduce_kernel<float, 2, M>;
+            case 4: return bucket_reduce_kernel<float, 4, M>;
+            case 8: return bucket_reduce_kernel<float, 8, M>;
+            case 16: return bucket_reduce_kernel<float, 16, M>;
+            default: return bucket_reduce_kernel<float, 0, M>;
         }
     }
     switch (W) {
-        case 2: return bucket_reduce_kernel<uint16_t, 2>;
-        case 4: return bucket_reduce_kernel<uint16_t, 4>;
-        case 8: return bucket_reduce_kernel<uint16_t, 8>;
-        case 16: return bucket_reduce_kernel<uint16_t, 16>;
-        default: return bucket_reduce_kernel<uint16_t, 0>;
+        case 2: return bucket_reduce_kernel<uint16_t, 2, M>;
+        case 4: return bucket_reduce_kernel<uint16_t, 4, M>;
+        case 8: return bucket_reduce_kernel<uint16_t, 8, M>;
+        case 16: return bucket_reduce_kernel<uint16_t, 16, M>;
+        default: return bucket_reduce_kernel<uint16_t, 0, M>;
     }
 }
 
@@ -277,7 +296,7 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 int reduce_max_ctas_per_sm(InType in, int W, int block) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick_reduce(in, W), block, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick_reduce<NoMask>(in, W), block, 0) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
@@ -291,10 +310,11 @@ int accumulate_max_ctas_per_sm(int block) {
 
 cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float* arena,
                           long long lo, long long hi, int s0, int s1, float inv_w,
-                          const LaunchCfg& cfg, cudaStream_t stream, long long* launches) {
+                          const LaunchCfg& cfg, cudaStream_t stream, long long* launches,
+                          const SegMask* mask) {
     if (hi <= lo || s1 <= s0) return cudaSuccess;
     if (cfg.kernel == KERNEL_TMA)
-        return launch_reduce_tma(t, in, W, n_out, arena, lo, hi, s0, s1, inv_w, cfg, stream, launches);
+        return launch_reduce_tma(t, in, W, n_out, arena, lo, hi, s0, s1, inv_w, cfg, stream, launches, mask);
     const int N = in == IN_F32 ? 4 : 8;
     ReduceParams p = {};
     p.seg_off = t.seg_off;
@@ -321,20 +341,22 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
     if (grid < 1) grid = 1;
     p.piece = ceil_div(ceil_div(span, grid), N) * N;
     grid = ceil_div(span, p.piece);
-    cudaError_t err = launch(pick_reduce(in, W), static_cast<int>(grid), cfg.block, p, cfg.pdl, stream);
+    cudaError_t err = mask ? launch(pick_reduce<SegMask>(in, W), static_cast<int>(grid), cfg.block, cfg.pdl,
+                                    stream, p, *mask)
+                           : launch(pick_reduce<NoMask>(in, W), static_cast<int>(grid), cfg.block, cfg.pdl,
+                                    stream, p, NoMask{});
     if (err == cudaSuccess && launches) ++*launches;
     return err;
 }
 
-cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,
                               cudaStream_t stream, long long* launches) {
-    if (cfg.kernel == KERNEL_TMA) return launch_accumulate_tma(pairs, n, first, cfg, stream, launches);
+    if (cfg.kernel == KERNEL_TMA) return launch_accumulate_tma(pairs, n, cfg, stream, launches);
     thread_local AccParams p;   // ~32 KiB: kept off the stack, one per host thread
     int i = 0;
     int issued = 0;
     while (i < n) {
         p.npairs = 0;
-        p.first = first;
         // launches after the first of this call directly follow it on the
         // stream and touch other pairs: no need to wait for it on entry
         p.chain = cfg.pdl && issued > 0 ? 1 : 0;
@@ -346,6 +368,8 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const Laun
                 d.acc = pairs[i].acc;
                 d.off = off;
                 d.len = pairs[i].len;
+                d.assign = pairs[i].assign;
+                d.pad = 0;
                 off += (pairs[i].len + 3) / 4 * 4;
             }
             ++i;
@@ -358,7 +382,7 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const Laun
         if (grid < 1) grid = 1;
         p.piece = ceil_div(ceil_div(off, grid), 4) * 4;
         grid = ceil_div(off, p.piece);
-        cudaError_t err = launch(accumulate_kernel, static_cast<int>(grid), cfg.block, p, cfg.pdl, stream);
+        cudaError_t err = launch(accumulate_kernel, static_cast<int>(grid), cfg.block, cfg.pdl, stream, p);
         if (err != cudaSuccess) return err;
         ++issued;
         if (launches) ++*launches;

@@ -42,36 +42,54 @@ struct LaunchCfg {
 
 enum InType { IN_F32 = 0, IN_BF16 = 1 };
 
+// Local-use masks of one launch with unused parameters (one parameter per
+// segment): bit r of bits[s - s0] set = replica r has a gradient for segment
+// s.  Passed by value in the kernel's parameter block.
+constexpr int kMaxMaskSegs = 3840;   // 8 B each: the block stays < 32 KiB
+
+struct SegMask {
+    int n;
+    unsigned long long bits[kMaxMaskSegs];
+};
+
+struct NoMask {
+    int unused;
+};
+
 // Fused bucket pass over arena range [lo, hi) = segments [s0, s1):
 // gather W replicas, fp32 sum in rank order, x inv_w, write arena and copies.
+// mask: nullptr for launches without unused parameters; otherwise the masks of
+// segments [s0, s1) (s1 - s0 <= kMaxMaskSegs).
 cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float* arena,
                           long long lo, long long hi, int s0, int s1, float inv_w,
-                          const LaunchCfg& cfg, cudaStream_t stream, long long* launches);
+                          const LaunchCfg& cfg, cudaStream_t stream, long long* launches,
+                          const SegMask* mask = nullptr);
 
 // Largest number of resident CTAs per SM of the register-streaming kernel.
 int reduce_max_ctas_per_sm(InType in, int W, int block);
 
-// One accumulation pair: acc[0..len) (+)= g[0..len).
+// One accumulation pair: acc = g (assign) or acc = fl32(acc + g) over len elements.
 struct AccPair {
     const float* g;
     float* acc;
     long long len;
+    int assign;
 };
 
-// acc = g (first != 0) or acc = fl32(acc + g) for every pair; the bulk-copy
-// variant when cfg.kernel is KERNEL_TMA.
-cudaError_t launch_accumulate(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+// Every pair; the bulk-copy variant when cfg.kernel is KERNEL_TMA.
+cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,
                               cudaStream_t stream, long long* launches);
 
 int accumulate_max_ctas_per_sm(int block);
 
 // Bulk-copy (TMA) pipelined variant of launch_accumulate, in ddp_kernels_tma.cu.
-cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, const LaunchCfg& cfg,
                                   cudaStream_t stream, long long* launches);
 
 // Bulk-copy (TMA) pipelined variant of launch_reduce, in ddp_kernels_tma.cu.
 cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
                               long long lo, long long hi, int s0, int s1, float inv_w,
-                              const LaunchCfg& cfg, cudaStream_t stream, long long* launches);
+                              const LaunchCfg& cfg, cudaStream_t stream, long long* launches,
+                              const SegMask* mask = nullptr);
 
 }  // namespace ddpk

@@ -133,9 +133,9 @@ __device__ __forceinline__ void walk(const ReduceParams& p, int s, long long x, 
     }
 }
 
-template <typename Tin, int WC>
+template <typename Tin, int WC, typename M>
 __global__ void __launch_bounds__(kThreads, 1)
-bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
+bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_constant__ M mask) {
     extern __shared__ __align__(128) unsigned char smem[];
     using V = Vec<Tin>;
     constexpr int N = V::N;
@@ -181,11 +181,16 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
                 if (use > 0) mbar_wait(smem_u32(empty + st), (use - 1) & 1u, p.status, kStatusEmptyTimeout, failed);
                 const uint32_t bytes = static_cast<uint32_t>(L * sizeof(Tin));
                 const uint32_t fb = smem_u32(full + st);
-                mbar_expect_tx(fb, bytes * static_cast<uint32_t>(W));
+                // replicas without a gradient for this segment copy nothing
+                const unsigned long long mk = seg_mask(mask, sg - p.s0);
+                uint32_t present = 0;
+                for (int r = 0; r < W; ++r) present += has_replica(mk, r) ? 1u : 0u;
+                mbar_expect_tx(fb, bytes * present);
                 const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * W;
                 Tin* dst = ring + st * stage_elems;
                 for (int r = 0; r < W; ++r)
-                    bulk_g2s(smem_u32(dst + static_cast<long long>(r) * p.tile), src[r] + (c - a0), bytes, fb);
+                    if (has_replica(mk, r))
+                        bulk_g2s(smem_u32(dst + static_cast<long long>(r) * p.tile), src[r] + (c - a0), bytes, fb);
                 ++k;
             },
             [](int, long long, long long, long long) {});
@@ -209,27 +214,34 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
             mbar_wait(smem_u32(full + st), use & 1u, p.status, kStatusFullTimeout, failed);
             const Tin* base = ring + st * stage_elems;
             float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
+            const unsigned long long mk = seg_mask(mask, sg - p.s0);
+            const bool write_dst = any_replica(mk, W);
             const int nv = static_cast<int>(L / N);
+            using Raw = typename V::Raw;
             for (int v = tc; v < nv; v += nct) {
                 float acc[N], f[N];
-                V::unpack(*reinterpret_cast<const typename V::Raw*>(base + v * N), acc);
+                V::unpack(has_replica(mk, 0) ? *reinterpret_cast<const Raw*>(base + v * N) : Raw{}, acc);
                 if constexpr (WC > 0) {
 #pragma unroll
                     for (int r = 1; r < WC; ++r) {
-                        V::unpack(*reinterpret_cast<const typename V::Raw*>(base + r * p.tile + v * N), f);
+                        V::unpack(has_replica(mk, r) ? *reinterpret_cast<const Raw*>(base + r * p.tile + v * N) : Raw{}, f);
 #pragma unroll
                         for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
                     }
                 } else {
                     for (int r = 1; r < W; ++r) {
-                        V::unpack(*reinterpret_cast<const typename V::Raw*>(base + static_cast<long long>(r) * p.tile + v * N), f);
+                        V::unpack(has_replica(mk, r)
+                                      ? *reinterpret_cast<const Raw*>(base + static_cast<long long>(r) * p.tile + v * N)
+                                      : Raw{},
+                                  f);
 #pragma unroll
                         for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
                     }
                 }
 #pragma unroll
                 for (int q = 0; q < N; ++q) acc[q] = __fmul_rn(acc[q], p.inv_w);
-                store_vec<N>(p, dst, c + static_cast<long long>(v) * N, c - a0 + static_cast<long long>(v) * N, acc);
+                store_vec<N>(p, dst, c + static_cast<long long>(v) * N, c - a0 + static_cast<long long>(v) * N, acc,
+                             write_dst);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(empty + st));
@@ -238,7 +250,7 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p) {
         [&](int sg, long long a0, long long lo, long long hi) {
             const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * W;
             float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
-            reduce_scalar<Tin>(p, src, dst, a0, lo, hi, W, tc, nct);
+            reduce_scalar<Tin>(p, src, dst, a0, lo, hi, W, tc, nct, seg_mask(mask, sg - p.s0));
         });
 }
 
@@ -318,11 +330,11 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
                 if (use > 0) mbar_wait(smem_u32(empty + st), (use - 1) & 1u, p.status, kStatusEmptyTimeout, failed);
                 const uint32_t bytes = static_cast<uint32_t>(L * sizeof(float));
                 const uint32_t fb = smem_u32(full + st);
-                mbar_expect_tx(fb, p.first ? bytes : 2u * bytes);
                 const AccPairDev& q = p.pair[i];
+                mbar_expect_tx(fb, q.assign ? bytes : 2u * bytes);
                 float* dst = ring + st * stage_elems;
                 bulk_g2s(smem_u32(dst), q.g + (c - q.off), bytes, fb);
-                if (!p.first) bulk_g2s(smem_u32(dst + p.tile), q.acc + (c - q.off), bytes, fb);
+                if (!q.assign) bulk_g2s(smem_u32(dst + p.tile), q.acc + (c - q.off), bytes, fb);
                 ++k;
             },
             [](int, long long, long long) {});
@@ -345,10 +357,11 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
             const float* gt = ring + st * stage_elems;
             const float* at = gt + p.tile;
             float* acc = p.pair[i].acc + (c - p.pair[i].off);
+            const bool assign = p.pair[i].assign != 0;
             const int nv = static_cast<int>(L / 4);
             for (int v = tc; v < nv; v += nct) {
                 const float4 g = *reinterpret_cast<const float4*>(gt + 4 * v);
-                if (p.first) {
+                if (assign) {
                     st_stream(acc + 4 * v, g);
                 } else {
                     const float4 a = *reinterpret_cast<const float4*>(at + 4 * v);
@@ -364,29 +377,31 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
             const AccPairDev& q = p.pair[i];
             for (long long a = lo + tc; a < hi; a += nct) {
                 const long long j = a - q.off;
-                q.acc[j] = p.first ? q.g[j] : __fadd_rn(q.acc[j], q.g[j]);
+                q.acc[j] = q.assign ? q.g[j] : __fadd_rn(q.acc[j], q.g[j]);
             }
         });
 }
 
-using TmaKernel = void (*)(ReduceParams);
+template <typename M>
+using TmaKernel = void (*)(ReduceParams, M);
 
-TmaKernel pick_tma(InType in, int W) {
+template <typename M>
+TmaKernel<M> pick_tma(InType in, int W) {
     if (in == IN_F32) {
         switch (W) {
-            case 2: return bucket_reduce_tma_kernel<float, 2>;
-            case 4: return bucket_reduce_tma_kernel<float, 4>;
-            case 8: return bucket_reduce_tma_kernel<float, 8>;
-            case 16: return bucket_reduce_tma_kernel<float, 16>;
-            default: return bucket_reduce_tma_kernel<float, 0>;
+            case 2: return bucket_reduce_tma_kernel<float, 2, M>;
+            case 4: return bucket_reduce_tma_kernel<float, 4, M>;
+            case 8: return bucket_reduce_tma_kernel<float, 8, M>;
+            case 16: return bucket_reduce_tma_kernel<float, 16, M>;
+            default: return bucket_reduce_tma_kernel<float, 0, M>;
         }
     }
     switch (W) {
-        case 2: return bucket_reduce_tma_kernel<uint16_t, 2>;
-        case 4: return bucket_reduce_tma_kernel<uint16_t, 4>;
-        case 8: return bucket_reduce_tma_kernel<uint16_t, 8>;
-        case 16: return bucket_reduce_tma_kernel<uint16_t, 16>;
-        default: return bucket_reduce_tma_kernel<uint16_t, 0>;
+        case 2: return bucket_reduce_tma_kernel<uint16_t, 2, M>;
+        case 4: return bucket_reduce_tma_kernel<uint16_t, 4, M>;
+        case 8: return bucket_reduce_tma_kernel<uint16_t, 8, M>;
+        case 16: return bucket_reduce_tma_kernel<uint16_t, 16, M>;
+        default: return bucket_reduce_tma_kernel<uint16_t, 0, M>;
     }
 }
 
@@ -419,7 +434,7 @@ cudaError_t ensure_smem_attr(K k) {
 
 }  // namespace
 
-cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const LaunchCfg& cfg,
+cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, const LaunchCfg& cfg,
                                   cudaStream_t stream, long long* launches) {
     thread_local AccParams p;   // ~32 KiB: kept off the stack, one per host thread
     const int stages = cfg.stages < 2 ? 2 : cfg.stages;
@@ -434,7 +449,6 @@ cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const 
     int issued = 0;
     while (i < n) {
         p.npairs = 0;
-        p.first = first;
         p.chain = cfg.pdl && issued > 0 ? 1 : 0;
         p.stages = stages;
         p.tile = static_cast<int>(tile);
@@ -447,6 +461,8 @@ cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const 
                 d.acc = pairs[i].acc;
                 d.off = off;
                 d.len = pairs[i].len;
+                d.assign = pairs[i].assign;
+                d.pad = 0;
                 off += (pairs[i].len + 3) / 4 * 4;
             }
             ++i;
@@ -478,7 +494,8 @@ cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, int first, const 
 
 cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
                               long long lo, long long hi, int s0, int s1, float inv_w,
-                              const LaunchCfg& cfg, cudaStream_t stream, long long* launches) {
+                              const LaunchCfg& cfg, cudaStream_t stream, long long* launches,
+                              const SegMask* mask) {
     if (hi <= lo || s1 <= s0) return cudaSuccess;
     const int N = in == IN_F32 ? 4 : 8;
     const int s_in = in == IN_F32 ? 4 : 2;
@@ -515,8 +532,7 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     p.piece = ceil_div(ceil_div(span, grid), N) * N;
     grid = ceil_div(span, p.piece);
 
-    TmaKernel k = pick_tma(in, W);
-    cudaError_t e = ensure_smem_attr(k);
+    cudaError_t e = mask ? ensure_smem_attr(pick_tma<SegMask>(in, W)) : ensure_smem_attr(pick_tma<NoMask>(in, W));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(grid));
@@ -528,7 +544,8 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = cfg.pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&lc, k, p);
+    e = mask ? cudaLaunchKernelEx(&lc, pick_tma<SegMask>(in, W), p, *mask)
+             : cudaLaunchKernelEx(&lc, pick_tma<NoMask>(in, W), p, NoMask{});
     if (e == cudaSuccess && launches) ++*launches;
     return e;
 }

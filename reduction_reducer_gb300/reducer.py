@@ -226,11 +226,26 @@ class Reducer:
         (marshalling done once instead of on every call)."""
         return _ptr_array([_ptr(t) for rep in replicas for t in rep])
 
-    def accumulate_nosync(self, acc, g, first_step: bool, stream=None):
-        """acc, g: W lists of P fp32 tensors, or arrays from ``pointers``."""
+    @staticmethod
+    def _bits(used):
+        flat = [1 if u else 0 for rep in used for u in rep]
+        return (C.c_uint8 * max(len(flat), 1))(*flat)
+
+    def accumulate_nosync(self, acc, g, first_step: bool, stream=None, used=None):
+        """acc, g: W lists of P fp32 tensors, or arrays from ``pointers``;
+        used: W lists of P local-use flags of this micro-step (None = all)."""
         a = acc if isinstance(acc, C.Array) else self.pointers(acc)
         b = g if isinstance(g, C.Array) else self.pointers(g)
-        self._check(self.lib.ddp_accumulate_nosync(self._h, a, b, 1 if first_step else 0, _stream(stream)))
+        if used is None:
+            self._check(self.lib.ddp_accumulate_nosync(self._h, a, b, 1 if first_step else 0, _stream(stream)))
+        else:
+            self._check(self.lib.ddp_accumulate_nosync_used(self._h, a, b, self._bits(used),
+                                                            1 if first_step else 0, _stream(stream)))
+
+    # ---------------------------------------------------------------- unused parameters
+    def set_local_used(self, used):
+        """used: W lists of P flags (None = all used)."""
+        self._check(self.lib.ddp_set_local_used(self._h, None if used is None else self._bits(used)))
 
     # ---------------------------------------------------------------- options
     def set_option(self, option: int, value: int):

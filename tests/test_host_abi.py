@@ -13,6 +13,7 @@ import itertools
 import os
 import re
 
+import numpy as np
 import pytest
 
 from oracle.buckets import assign_buckets
@@ -289,3 +290,75 @@ def test_rebuild_errors(lib):
         red.rebuild_buckets(None, 4, 4)
     red.rebuild_buckets([0, 1, 2, 3], 8, 8)
     assert red.get_members() == [[0, 1], [2, 3]]
+
+
+# ---------------------------------------------------------------- unused parameters
+
+def _dry_bound(numel, W, cap, find_unused=True):
+    from reduction_reducer_gb300 import _lib as L
+    red = _make(numel, "f32", cap)
+    red.set_dry_run(True)
+    if find_unused:
+        red.set_option(L.OPT_FIND_UNUSED, 1)
+    fake = [[0x100000 + 0x1000 * (r * len(numel) + v) for v in range(len(numel))] for r in range(W)]
+    red.bind(fake, 0x10000000, None)
+    return red
+
+
+def test_unused_state_machine_matches_oracle(lib):
+    from oracle.unused import UnusedReadiness
+    numel = [1, 2, 1, 3, 1, 2]
+    members, _ = assign_buckets(numel, 4, 8)
+    rng = np.random.default_rng(3)
+    W = 3
+    for trial in range(60):
+        used = rng.random((W, len(numel))) < 0.6
+        g = used.any(axis=0)
+        reported = [v for v in range(len(numel)) if g[v]]
+        if not reported:
+            continue
+        order = [int(v) for v in rng.permutation(reported)]
+        red = _dry_bound(numel, W, 8)
+        assert red.get_members() == members
+        red.set_local_used(used.tolist())
+        red.begin_iteration()
+        sm = UnusedReadiness(members, used.tolist())
+        sm.begin_iteration()
+        for v in order:
+            assert red.mark_ready(v) == sm.mark_ready(v), (used, order)
+        assert red.get_progress() == (len(members), [])
+        # a new iteration without new bits: every variable reports again
+        red.begin_iteration()
+        for v in range(len(numel)):
+            red.mark_ready(v)
+        red.destroy()
+
+
+def test_unused_errors_and_bitmap_or(lib):
+    from reduction_reducer_gb300 import AlreadyReady, InvalidArg
+    numel = [1, 1, 1]
+    red = _dry_bound(numel, 2, 4)
+    red.set_local_used([[True, False, False], [False, False, False]])
+    red.set_local_used([[False, False, False], [False, True, False]])     # OR: 0 and 1 used
+    red.begin_iteration()
+    with pytest.raises(AlreadyReady):
+        red.mark_ready(2)                     # unused on every replica: already ready
+    assert red.mark_ready(1) == [0, 1]        # buckets: v2 -> 0 (unused, marked), v1 -> 1
+    assert red.mark_ready(0) == [2]
+    # no_sync bits accumulate into the next reduction's bitmap
+    W, P = 2, 3
+    fake = red.pointers([[0x2000 + 16 * i for i in range(P)] for _ in range(W)])
+    red.accumulate_nosync(fake, fake, True, used=[[True, False, False], [False, False, False]])
+    red.accumulate_nosync(fake, fake, False, used=[[False, False, True], [False, False, False]])
+    red.begin_iteration()
+    # v1 is unused in both micro-steps on both replicas: marked ready at the
+    # first event, so bucket 1 goes out right after bucket 0 (v2)
+    assert red.mark_ready(2) == [0, 1]
+    with pytest.raises(AlreadyReady):
+        red.mark_ready(1)
+    assert red.mark_ready(0) == [2]
+    plain = _make(numel, "f32", 4)
+    plain.set_dry_run(True)
+    plain.bind([[0x3000] * 3], 0x10000000, None)
+    with pytest.raises(InvalidArg):
+        plain.set_local_used([[True] * 3])    # needs DDP_OPT_FIND_UNUSED
