@@ -533,6 +533,20 @@ def extra_configs(torch, device, stream, args, dist, keep):
     keep.driver = "events"
     timed(keep, "bert_large_event_calls", "one mark_ready call per event (launches wait for their predecessor)")
     keep.driver = "hooks"
+    # BERT-large after a rebuild from the recorded (straggler) ready order,
+    # first bucket capped at 1 MiB
+    import time as _time
+    t0 = _time.perf_counter()
+    keep.red.rebuild_buckets(None, 1 << 20, 25 << 20)
+    rebuild_ms = (_time.perf_counter() - t0) * 1e3
+    keep._order_c = (__import__("ctypes").c_int32 * len(keep.order))(*keep.order)
+    timed(keep, "bert_large_rebuilt", "after ddp_rebuild_buckets from the recorded order (first cap 1 MiB)")
+    out["bert_large_rebuilt"]["rebuild_host_ms"] = round(rebuild_ms, 3)
+    out["bert_large_rebuilt"]["buckets"] = keep.red.B
+    keep.red.rebuild_buckets(list(range(keep.P - 1, -1, -1)), 25 << 20, 25 << 20)   # back to the construction layout
+    # BERT-large with unused parameters: pooler unused everywhere, the FFN of
+    # every fourth layer unused on replica 1
+    unused_config(keep, timed, out)
     # BERT-large as-view: replicas laid out as buckets, no copy-back
     wl = Workload("bert_large", torch, device, 25, n_out=0, driver="hooks", layout="buckets")
     timed(wl, "bert_large_as_view", "gradient_as_bucket_view: W*N*4 + N*4 bytes")
@@ -549,6 +563,41 @@ def extra_configs(torch, device, stream, args, dist, keep):
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
     return out
+
+
+def unused_config(wl, timed, out):
+    """find_unused_parameters on BERT-large: the masked launches of one
+    iteration, bytes = the replica reads that happen + bucket writes +
+    copy-backs actually written."""
+    import ctypes
+    from reduction_reducer_gb300 import _lib
+    names = [n for n, _ in shapes.bert_large()]
+    used = [[True] * wl.P for _ in range(wl.W)]
+    for v, n in enumerate(names):
+        if n.startswith("pooler"):
+            for r in range(wl.W):
+                used[r][v] = False
+        if (".intermediate." in n or ".output.dense" in n) and int(n.split(".")[2]) % 4 == 0:
+            used[1][v] = False
+    gused = [any(used[r][v] for r in range(wl.W)) for v in range(wl.P)]
+    wl.red.set_option(_lib.OPT_FIND_UNUSED, 1)
+    order = [v for v in wl.order if gused[v]]
+    order_c = (ctypes.c_int32 * len(order))(*order)
+    saved_step, saved_bytes = wl.step, wl.bytes
+
+    used_c = wl.red.bits(used)                     # marshalled once
+
+    def step(stream):
+        wl.red.set_local_used(used_c)
+        wl.red.begin_iteration()
+        wl.red.mark_ready_many(order_c, stream)
+    wl.step = step
+    wl.bytes = (sum(wl.numel[v] * wl.s_in for r in range(wl.W) for v in range(wl.P) if used[r][v])
+                + wl.N * 4 + sum(wl.numel[v] * 4 for v in range(wl.P) if gused[v]))
+    timed(wl, "bert_large_find_unused", "find_unused: pooler unused on every replica, every 4th FFN unused "
+          "on replica 1; bytes count only the reads and copy-backs that happen")
+    wl.step, wl.bytes = saved_step, saved_bytes
+    wl.red.set_option(_lib.OPT_FIND_UNUSED, 0)
 
 
 def nosync_config(torch, device, stream, steps, warm, dist, K=8):

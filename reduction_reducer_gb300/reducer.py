@@ -227,7 +227,10 @@ class Reducer:
         return _ptr_array([_ptr(t) for rep in replicas for t in rep])
 
     @staticmethod
-    def _bits(used):
+    def bits(used):
+        """W lists of P flags -> a reusable array of W*P local-use bytes."""
+        if isinstance(used, C.Array):
+            return used
         flat = [1 if u else 0 for rep in used for u in rep]
         return (C.c_uint8 * max(len(flat), 1))(*flat)
 
@@ -239,13 +242,13 @@ class Reducer:
         if used is None:
             self._check(self.lib.ddp_accumulate_nosync(self._h, a, b, 1 if first_step else 0, _stream(stream)))
         else:
-            self._check(self.lib.ddp_accumulate_nosync_used(self._h, a, b, self._bits(used),
+            self._check(self.lib.ddp_accumulate_nosync_used(self._h, a, b, self.bits(used),
                                                             1 if first_step else 0, _stream(stream)))
 
     # ---------------------------------------------------------------- unused parameters
     def set_local_used(self, used):
-        """used: W lists of P flags (None = all used)."""
-        self._check(self.lib.ddp_set_local_used(self._h, None if used is None else self._bits(used)))
+        """used: W lists of P flags, or an array from ``bits`` (None = all used)."""
+        self._check(self.lib.ddp_set_local_used(self._h, None if used is None else self.bits(used)))
 
     # ---------------------------------------------------------------- options
     def set_option(self, option: int, value: int):
