@@ -547,6 +547,8 @@ def extra_configs(torch, device, stream, args, dist, keep):
     # BERT-large with unused parameters: pooler unused everywhere, the FFN of
     # every fourth layer unused on replica 1
     unused_config(keep, timed, out)
+    # BERT-large through the built-in mean hook: gather + hook + copy-back
+    hook_config(torch, device, keep, timed, out)
     # BERT-large as-view: replicas laid out as buckets, no copy-back
     wl = Workload("bert_large", torch, device, 25, n_out=0, driver="hooks", layout="buckets")
     timed(wl, "bert_large_as_view", "gradient_as_bucket_view: W*N*4 + N*4 bytes")
@@ -563,6 +565,24 @@ def extra_configs(torch, device, stream, args, dist, keep):
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
     return out
+
+
+def hook_config(torch, device, keep, timed, out):
+    """The communication-hook path (unfused): every bucket is gathered into
+    W replica bucket buffers, reduced by the built-in mean hook and copied
+    back.  Reported against the fused pass's algorithmic bytes (what the
+    iteration must move) and against the bytes the three passes move."""
+    wl = Workload("bert_large", torch, device, 25, n_out=1, driver="hooks")
+    rb = [torch.empty(wl.red.arena_numel(), dtype=torch.float32, device=device) for _ in range(wl.W)]
+    wl.red.register_comm_hook("mean", rb)
+    timed(wl, "bert_large_hook_mean", "register_comm_hook('mean'): gather + hook + copy-back per bucket; "
+          "gbs uses the fused pass's algorithmic bytes")
+    moved = 2 * wl.W * wl.N * 4 + wl.W * wl.N * 4 + wl.N * 4 + 2 * wl.N * 4
+    out["bert_large_hook_mean"]["bytes_moved_per_step"] = moved
+    out["bert_large_hook_mean"]["moved_gbs"] = round(moved / (out["bert_large_hook_mean"]["ms_per_step"] * 1e-3) / 1e9, 1)
+    wl.free()
+    del rb
+    torch.cuda.empty_cache()
 
 
 def unused_config(wl, timed, out):

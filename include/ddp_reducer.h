@@ -59,7 +59,8 @@ enum ddp_status {
     DDP_ERR_PRIOR_REDUCTION_UNFINISHED = -4,  /* previous iteration left buckets unlaunched */
     DDP_ERR_NOT_BOUND = -5,                   /* launch requested before ddp_bind */
     DDP_ERR_CUDA = -6,                        /* a CUDA runtime call failed */
-    DDP_ERR_NO_MEMORY = -7                    /* host or library-owned device allocation failed */
+    DDP_ERR_NO_MEMORY = -7,                   /* host or library-owned device allocation failed */
+    DDP_ERR_HOOK = -8                         /* a communication hook returned nonzero */
 };
 
 /* ---------------------------------------------------------------- construction */
@@ -190,6 +191,51 @@ int ddp_set_local_used(ddp_ctx* ctx, const uint8_t* used);
  * unused-parameter marking).  Non-NULL bits need DDP_OPT_FIND_UNUSED. */
 int ddp_accumulate_nosync_used(ddp_ctx* ctx, void* const* acc, const void* const* g, const uint8_t* used,
                                int32_t first_step, void* stream);
+
+/* ---------------------------------------------------------------- communication hooks */
+
+/* One ready bucket as a hook sees it ("Distributed Data Parallel" notes,
+ * "Custom gradient aggregation"; "NCCL 专家课程 30", section "从 Bucket 到
+ * AllReduce Future": index, bucket count, flat buffer, per-parameter views).
+ * Host arrays are valid during the hook call only. */
+typedef struct ddp_grad_bucket {
+    int32_t index;                 /* bucket index */
+    int32_t num_buckets;
+    int32_t is_last;               /* index == num_buckets - 1 */
+    int32_t W;                     /* replicas */
+    int32_t dtype;                 /* ddp_dtype of the replica buffers */
+    int32_t n_vars;
+    int64_t numel;                 /* elements in the bucket */
+    const void* const* replicas;   /* host [W] of device pointers: replica r's gradients of this bucket, gathered
+                                      into the bucket layout (numel elements of dtype) */
+    float* result;                 /* device fp32 [numel]: the hook writes the reduced bucket here (the arena slice) */
+    const int32_t* variables;      /* host [n_vars]: the bucket's variables in push order */
+    const int64_t* offsets;        /* host [n_vars]: element offset of each variable in the bucket */
+    const int64_t* lengths;        /* host [n_vars]: element count of each variable */
+} ddp_grad_bucket;
+
+/* A hook enqueues its reduction on `stream` and returns 0 (nonzero aborts the
+ * launch with DDP_ERR_HOOK).  It owns the averaging: the result is what the
+ * parameters' gradients receive. */
+typedef int (*ddp_comm_hook_fn)(void* state, const ddp_grad_bucket* bucket, void* stream);
+
+/* Replace the fused bucket pass by: gather (each replica's gradients copied
+ * into its bucket buffer), hook, copy-back (the result into the gradient
+ * outputs), per launched bucket in index order.  Register once, after
+ * ddp_bind and before the first launch.
+ *   replica_buffers  host array [W] of device pointers, caller-owned, each 16-byte
+ *                    aligned with room for bucket_offsets[B] elements of the
+ *                    gradient dtype (bucket b of replica r lives at
+ *                    replica_buffers[r] + bucket_offsets[b])
+ * W <= 64; not with DDP_OPT_FIND_UNUSED.  Errors: INVALID_ARG, NOT_BOUND. */
+int ddp_register_comm_hook(ddp_ctx* ctx, ddp_comm_hook_fn hook, void* state, void* const* replica_buffers);
+
+/* Built-in hooks (state unused): the default, the rank-order fp32 mean of the
+ * replicas' buffers x fl32(1/W) -- the fused pass's arithmetic -- and a
+ * compression variant that first rounds every replica value to bf16 (round to
+ * nearest even), i.e. averages what a bf16 wire would carry. */
+int ddp_hook_mean(void* state, const ddp_grad_bucket* bucket, void* stream);
+int ddp_hook_bf16_compress(void* state, const ddp_grad_bucket* bucket, void* stream);
 
 /* ---------------------------------------------------------------- rebuild */
 

@@ -5,6 +5,6 @@ C++ host core + hand-written sm_103a CUDA kernels behind the C ABI of
 ``reduction_reducer_gb300.build``); this package is the thin Python binding.
 """
 
-from .reducer import (AlreadyReady, CudaError, DDPError, InvalidArg, NoMemory, NotBound,  # noqa: F401
-                      OutOfOrder, PriorReductionUnfinished, Reducer)
+from .reducer import (AlreadyReady, CudaError, DDPError, HookError, InvalidArg, NoMemory,  # noqa: F401
+                      NotBound, OutOfOrder, PriorReductionUnfinished, Reducer)
 from ._lib import LIB_PATH, load  # noqa: F401

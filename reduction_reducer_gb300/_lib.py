@@ -23,6 +23,7 @@ STATUS = {
     -5: "DDP_ERR_NOT_BOUND",
     -6: "DDP_ERR_CUDA",
     -7: "DDP_ERR_NO_MEMORY",
+    -8: "DDP_ERR_HOOK",
 }
 
 OPT_DRY_RUN, OPT_CTAS_PER_SM, OPT_PDL, OPT_BLOCK_THREADS = 0, 1, 2, 3
@@ -34,6 +35,18 @@ KERNEL_LDG, KERNEL_TMA, KERNEL_AUTO = 0, 1, 2
 class Locator(C.Structure):
     _fields_ = [("bucket", C.c_int32), ("intra", C.c_int32), ("offset", C.c_int64), ("length", C.c_int64)]
 
+
+class GradBucket(C.Structure):
+    """struct ddp_grad_bucket."""
+    _fields_ = [("index", C.c_int32), ("num_buckets", C.c_int32), ("is_last", C.c_int32), ("W", C.c_int32),
+                ("dtype", C.c_int32), ("n_vars", C.c_int32), ("numel", C.c_int64),
+                ("replicas", C.POINTER(C.c_void_p)), ("result", C.c_void_p),
+                ("variables", C.POINTER(C.c_int32)), ("offsets", C.POINTER(C.c_int64)),
+                ("lengths", C.POINTER(C.c_int64))]
+
+
+# int (*ddp_comm_hook_fn)(void* state, const ddp_grad_bucket* bucket, void* stream)
+HOOKFN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.POINTER(GradBucket), C.c_void_p)
 
 # name -> (restype, argtypes); every symbol of include/ddp_reducer.h
 SIGNATURES = {
@@ -51,6 +64,9 @@ SIGNATURES = {
     "ddp_set_local_used": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint8)]),
     "ddp_accumulate_nosync_used": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                                              C.POINTER(C.c_uint8), C.c_int32, C.c_void_p]),
+    "ddp_register_comm_hook": (C.c_int, [C.c_void_p, HOOKFN, C.c_void_p, C.POINTER(C.c_void_p)]),
+    "ddp_hook_mean": (C.c_int, [C.c_void_p, C.POINTER(GradBucket), C.c_void_p]),
+    "ddp_hook_bf16_compress": (C.c_int, [C.c_void_p, C.POINTER(GradBucket), C.c_void_p]),
     "ddp_get_ready_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "ddp_rebuild_buckets": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.c_int64, C.c_int64]),
     "ddp_accumulate_nosync": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),

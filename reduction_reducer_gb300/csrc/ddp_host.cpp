@@ -62,6 +62,11 @@ struct ddp_ctx {
     bool unused_marked = false;                   // globally unused variables marked ready
     std::vector<uint8_t> has_grad;                // W*P: accumulator holds a gradient (no_sync block)
 
+    // ---- communication hook
+    ddp_comm_hook_fn hook = nullptr;
+    void* hook_state = nullptr;
+    std::vector<void*> hook_rb;                   // W replica bucket buffers
+
     // ---- binding
     bool bound = false;
     std::vector<const void*> bind_grads;          // W*P, kept for rebuilds
@@ -246,6 +251,55 @@ int check_device(ddp_ctx* c) {
     return DDP_OK;
 }
 
+// The hook path for buckets [b0, b1): per bucket, gather into the replica
+// buffers, the hook, copy-back.
+int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& cfg, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<const void*> reps(c->W);
+    std::vector<int64_t> offs, lens;
+    for (int32_t b = b0; b < b1; ++b) {
+        const long long lo = c->bucket_off[b], hi = c->bucket_off[b + 1];
+        const int s0 = c->bucket_seg[b], s1 = c->bucket_seg[b + 1];
+        long long n = 0;
+        cudaError_t e = ddpk::launch_seg_copy(c->tab, 0, c->elem, c->W, c->n_out, c->arena, c->hook_rb.data(), lo, hi,
+                                              s0, s1, cfg, st, &n);
+        c->launches += n;
+        if (e != cudaSuccess) return cuda_fail(c, e, "hook gather launch");
+        const auto& vs = c->members[b];
+        offs.resize(vs.size());
+        lens.resize(vs.size());
+        for (size_t i = 0; i < vs.size(); ++i) {
+            offs[i] = c->loc[vs[i]].offset;
+            lens[i] = c->loc[vs[i]].length;
+        }
+        for (int r = 0; r < c->W; ++r)
+            reps[r] = static_cast<const char*>(c->hook_rb[r]) + lo * c->elem;
+        ddp_grad_bucket gb;
+        gb.index = b;
+        gb.num_buckets = c->B;
+        gb.is_last = b == c->B - 1;
+        gb.W = c->W;
+        gb.dtype = c->dtype;
+        gb.n_vars = static_cast<int32_t>(vs.size());
+        gb.numel = hi - lo;
+        gb.replicas = reps.data();
+        gb.result = c->arena + lo;
+        gb.variables = vs.data();
+        gb.offsets = offs.data();
+        gb.lengths = lens.data();
+        const int hr = c->hook(c->hook_state, &gb, stream);
+        if (hr != 0) return fail(c, DDP_ERR_HOOK, "communication hook returned " + std::to_string(hr) + " for bucket " +
+                                                      std::to_string(b));
+        n = 0;
+        e = ddpk::launch_seg_copy(c->tab, 1, 4, c->W, c->n_out, c->arena, nullptr, lo, hi, s0, s1, cfg, st, &n);
+        c->launches += n;
+        if (e != cudaSuccess) return cuda_fail(c, e, "hook copy-back launch");
+    }
+    c->iter_launches += 1;
+    c->iter_stream = stream;
+    return DDP_OK;
+}
+
 // One kernel launch over buckets [b0, b1).
 int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
     if (c->dry || b1 <= b0) return DDP_OK;
@@ -263,6 +317,7 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
     // opted in (DDP_OPT_CHAINED).
     const bool follows_own = c->iter_launches > 0 && stream == c->iter_stream;
     cfg.chain = c->pdl && follows_own && (c->call_launches > 0 || c->opt_chain) ? 1 : 0;
+    if (c->hook) return hook_range(c, b0, b1, cfg, stream);
     if (!c->iter_masked) {
         long long n = 0;
         cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, lo, hi, s0, s1, c->inv_w,
@@ -331,6 +386,7 @@ const char* ddp_status_string(int status) {
         case DDP_ERR_NOT_BOUND: return "DDP_ERR_NOT_BOUND";
         case DDP_ERR_CUDA: return "DDP_ERR_CUDA";
         case DDP_ERR_NO_MEMORY: return "DDP_ERR_NO_MEMORY";
+        case DDP_ERR_HOOK: return "DDP_ERR_HOOK";
         default: return "unknown ddp status";
     }
 }
@@ -554,6 +610,51 @@ int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_aren
     c->pending_set = false;
     c->has_grad.clear();
     return DDP_OK;
+}
+
+int ddp_register_comm_hook(ddp_ctx* c, ddp_comm_hook_fn hook, void* state, void* const* replica_buffers) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (!hook) return fail(c, DDP_ERR_INVALID_ARG, "hook is NULL");
+    if (c->hook) return fail(c, DDP_ERR_INVALID_ARG, "a communication hook is registered already");
+    if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "register the hook after ddp_bind");
+    if (c->launches > 0 || c->active) return fail(c, DDP_ERR_INVALID_ARG, "register the hook before the first launch");
+    if (c->W > ddpk::kMaxHookReplicas) return fail(c, DDP_ERR_INVALID_ARG, "hooks support W <= 64");
+    if (c->opt_find_unused) return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with DDP_OPT_FIND_UNUSED");
+    if (c->bucket_off[c->B] > 0 && !replica_buffers) return fail(c, DDP_ERR_INVALID_ARG, "replica_buffers is NULL");
+    std::vector<void*> rb(c->W, nullptr);
+    for (int r = 0; r < c->W && c->bucket_off[c->B] > 0; ++r) {
+        if (!replica_buffers[r] || !is_aligned16(reinterpret_cast<uintptr_t>(replica_buffers[r])))
+            return fail(c, DDP_ERR_INVALID_ARG, "replica buffer " + std::to_string(r) + " is NULL or not 16-byte aligned");
+        rb[r] = replica_buffers[r];
+    }
+    c->hook = hook;
+    c->hook_state = state;
+    c->hook_rb = std::move(rb);
+    return DDP_OK;
+}
+
+namespace {
+int builtin_mean(const ddp_grad_bucket* b, void* stream, int compress) {
+    if (!b || b->W < 1 || b->W > ddpk::kMaxHookReplicas) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 2;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 2;
+    const ddpk::InType in = b->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
+    const cudaError_t e = ddpk::launch_flat_mean(in, b->W, b->replicas, b->result, b->numel,
+                                                 1.0f / static_cast<float>(b->W), compress, sms,
+                                                 static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? 0 : 3;
+}
+}  // namespace
+
+int ddp_hook_mean(void* state, const ddp_grad_bucket* bucket, void* stream) {
+    (void)state;
+    return builtin_mean(bucket, stream, 0);
+}
+
+int ddp_hook_bf16_compress(void* state, const ddp_grad_bucket* bucket, void* stream) {
+    (void)state;
+    return builtin_mean(bucket, stream, 1);
 }
 
 int ddp_get_ready_trace(const ddp_ctx* c, int32_t* order, int32_t* n) {
@@ -790,6 +891,8 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             return fail(c, DDP_ERR_INVALID_ARG, "DDP_OPT_QUERY_KERNEL is read with ddp_get_option");
         case DDP_OPT_FIND_UNUSED: {
             if (c->active) return fail(c, DDP_ERR_INVALID_ARG, "find_unused changes between iterations only");
+            if (value != 0 && c->hook)
+                return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with DDP_OPT_FIND_UNUSED");
             const bool on = value != 0;
             if (on && c->bound && c->W > 64)
                 return fail(c, DDP_ERR_INVALID_ARG, "unused-parameter tracking supports W <= 64");

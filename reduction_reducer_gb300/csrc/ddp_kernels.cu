@@ -250,6 +250,109 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
     if (threadIdx.x == 0) pdl_exit(p.chain);
 }
 
+// ------------------------------------------------------------------ hook path kernels
+
+struct CopyParams {
+    const long long* seg_off;
+    const void* const* seg_src;
+    float* const* seg_dst;
+    const int* seg_vec;
+    const float* arena;
+    long long base, lo, hi, piece;
+    int s0, s1;
+    int W, n_out;
+    int mode;   // 0 gather, 1 copy-back
+    int elem;   // bytes per element (gather: gradient dtype; copy-back: 4)
+    void* rb[kMaxHookReplicas];
+};
+
+__device__ __forceinline__ void copy_elem(char* d, const char* s, int elem) {
+    if (elem == 4) *reinterpret_cast<float*>(d) = *reinterpret_cast<const float*>(s);
+    else *reinterpret_cast<uint16_t*>(d) = *reinterpret_cast<const uint16_t*>(s);
+}
+
+// One run: `from` holds the segment's elements starting at its first one,
+// `to` is indexed like `from` (both already offset); elements [x, e) of the
+// segment, 16-byte vectors where the run is aligned.
+__device__ __forceinline__ void copy_run(const char* from, char* to, long long a0, long long x, long long e,
+                                         int elem, bool vec) {
+    const int n = 16 / elem;
+    long long kb = (x + n - 1) / n, ke = e / n;
+    if (!vec || kb >= ke) kb = ke = 0;
+    const long long sc_end = vec && kb < ke ? kb * n : e;
+    for (long long a = x + threadIdx.x; a < sc_end; a += blockDim.x)
+        copy_elem(to + (a - a0) * elem, from + (a - a0) * elem, elem);
+    for (long long k = kb + threadIdx.x; k < ke; k += blockDim.x) {
+        const long long j = (k * n - a0) * elem;
+        st_stream(reinterpret_cast<float*>(to + j), __ldcs(reinterpret_cast<const float4*>(from + j)));
+    }
+    if (vec && kb < ke)
+        for (long long a = ke * n + threadIdx.x; a < e; a += blockDim.x)
+            copy_elem(to + (a - a0) * elem, from + (a - a0) * elem, elem);
+}
+
+__global__ void __launch_bounds__(kMaxBlock) seg_copy_kernel(const __grid_constant__ CopyParams p) {
+    pdl_enter(0);
+    long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
+    long long y = x + p.piece;
+    x = x < p.lo ? p.lo : x;
+    y = y > p.hi ? p.hi : y;
+    if (x >= y) return;
+    int s = find_segment(p.seg_off, p.s0, p.s1, x);
+    while (x < y) {
+        const long long a0 = __ldg(p.seg_off + s);
+        const long long a1 = __ldg(p.seg_off + s + 1);
+        const long long e = a1 < y ? a1 : y;
+        const bool vec = __ldg(p.seg_vec + s) != 0;
+        if (p.mode == 0) {
+            for (int r = 0; r < p.W; ++r) {
+                const char* from = static_cast<const char*>(p.seg_src[static_cast<long long>(s) * p.W + r]);
+                char* to = static_cast<char*>(p.rb[r]) + a0 * p.elem;
+                copy_run(from, to, a0, x, e, p.elem, vec);
+            }
+        } else {
+            const char* from = reinterpret_cast<const char*>(p.arena + a0);
+            for (int o = 0; o < p.n_out; ++o)
+                copy_run(from, reinterpret_cast<char*>(p.seg_dst[static_cast<long long>(s) * p.n_out + o]), a0, x,
+                         e, 4, vec);
+        }
+        x = e;
+        ++s;
+    }
+}
+
+// bf16 round to nearest even, widened back to fp32 (NaN stays a quiet NaN).
+__device__ __forceinline__ float round_bf16(float x) {
+    const uint32_t u = __float_as_uint(x);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return __uint_as_float((u | 0x00400000u) & 0xffff0000u);
+    const uint32_t r = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
+    return __uint_as_float(r);
+}
+
+struct FlatMeanParams {
+    float* out;
+    long long n;
+    float inv_w;
+    int W;
+    int compress;
+    const void* src[kMaxHookReplicas];
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(kMaxBlock) flat_mean_kernel(const __grid_constant__ FlatMeanParams p) {
+    pdl_enter(0);
+    const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += step) {
+        float x = widen1(static_cast<const Tin*>(p.src[0])[i]);
+        float acc = p.compress ? round_bf16(x) : x;
+        for (int r = 1; r < p.W; ++r) {
+            x = widen1(static_cast<const Tin*>(p.src[r])[i]);
+            acc = __fadd_rn(acc, p.compress ? round_bf16(x) : x);
+        }
+        p.out[i] = __fmul_rn(acc, p.inv_w);
+    }
+}
+
 // ------------------------------------------------------------------ launch helpers
 
 template <typename Kernel, typename... Params>
@@ -347,6 +450,58 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
                                     stream, p, NoMask{});
     if (err == cudaSuccess && launches) ++*launches;
     return err;
+}
+
+cudaError_t launch_seg_copy(const SegTable& t, int mode, int elem, int W, int n_out, const float* arena,
+                            void* const* rb, long long lo, long long hi, int s0, int s1,
+                            const LaunchCfg& cfg, cudaStream_t stream, long long* launches) {
+    if (hi <= lo || s1 <= s0 || (mode == 1 && n_out == 0)) return cudaSuccess;
+    if (W > kMaxHookReplicas) return cudaErrorInvalidValue;
+    CopyParams p = {};
+    p.seg_off = t.seg_off;
+    p.seg_src = t.seg_src;
+    p.seg_dst = t.seg_dst;
+    p.seg_vec = t.seg_vec;
+    p.arena = arena;
+    p.lo = lo;
+    p.hi = hi;
+    const int n = 16 / (mode == 0 ? elem : 4);
+    p.base = lo - lo % n;
+    p.s0 = s0;
+    p.s1 = s1;
+    p.W = W;
+    p.n_out = n_out;
+    p.mode = mode;
+    p.elem = mode == 0 ? elem : 4;
+    for (int r = 0; r < W && mode == 0; ++r) p.rb[r] = rb[r];
+    const long long span = hi - p.base;
+    const long long min_piece = static_cast<long long>(cfg.block) * n * 2;
+    long long grid = static_cast<long long>(cfg.sms) * 4;
+    grid = grid < ceil_div(span, min_piece) ? grid : ceil_div(span, min_piece);
+    if (grid < 1) grid = 1;
+    p.piece = ceil_div(ceil_div(span, grid), n) * n;
+    grid = ceil_div(span, p.piece);
+    cudaError_t err = launch(seg_copy_kernel, static_cast<int>(grid), cfg.block, cfg.pdl, stream, p);
+    if (err == cudaSuccess && launches) ++*launches;
+    return err;
+}
+
+cudaError_t launch_flat_mean(InType in, int W, const void* const* src, float* out, long long n, float inv_w,
+                             int compress, int sms, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    if (W < 1 || W > kMaxHookReplicas) return cudaErrorInvalidValue;
+    FlatMeanParams p = {};
+    p.out = out;
+    p.n = n;
+    p.inv_w = inv_w;
+    p.W = W;
+    p.compress = compress;
+    for (int r = 0; r < W; ++r) p.src[r] = src[r];
+    long long grid = ceil_div(n, 256);
+    const long long cap = static_cast<long long>(sms > 0 ? sms : 152) * 8;
+    grid = grid < cap ? grid : cap;
+    return in == IN_F32 ? launch(flat_mean_kernel<float>, static_cast<int>(grid), 256, true, stream, p)
+                        : launch(flat_mean_kernel<uint16_t>, static_cast<int>(grid), 256, true, stream, p);
 }
 
 cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,

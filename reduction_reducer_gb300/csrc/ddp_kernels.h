@@ -82,6 +82,21 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,
 
 int accumulate_max_ctas_per_sm(int block);
 
+// ------------------------------------------------------------------ hook path
+
+// Gather (mode 0): for segments [s0, s1) copy every replica's gradients into
+// its bucket buffer at the arena offsets (rb[r] + a, grad element size).
+// Copy-back (mode 1): copy the arena into every output copy's views.
+constexpr int kMaxHookReplicas = 64;
+cudaError_t launch_seg_copy(const SegTable& t, int mode, int elem, int W, int n_out, const float* arena,
+                            void* const* rb, long long lo, long long hi, int s0, int s1,
+                            const LaunchCfg& cfg, cudaStream_t stream, long long* launches);
+
+// out[i] = fp32 rank-order mean of widen(in_r[i]) x inv_w (compress = 1: each
+// fp32 value first rounded to bf16, round to nearest even).
+cudaError_t launch_flat_mean(InType in, int W, const void* const* src, float* out, long long n, float inv_w,
+                             int compress, int sms, cudaStream_t stream);
+
 // Bulk-copy (TMA) pipelined variant of launch_accumulate, in ddp_kernels_tma.cu.
 cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, const LaunchCfg& cfg,
                                   cudaStream_t stream, long long* launches);

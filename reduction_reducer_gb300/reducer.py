@@ -30,10 +30,11 @@ class PriorReductionUnfinished(DDPError): pass
 class NotBound(DDPError): pass
 class CudaError(DDPError): pass
 class NoMemory(DDPError): pass
+class HookError(DDPError): pass
 
 
 _ERRORS = {-1: InvalidArg, -2: AlreadyReady, -3: OutOfOrder, -4: PriorReductionUnfinished,
-           -5: NotBound, -6: CudaError, -7: NoMemory}
+           -5: NotBound, -6: CudaError, -7: NoMemory, -8: HookError}
 
 
 def _ptr(x) -> int:
@@ -179,6 +180,31 @@ class Reducer:
         parked = (C.c_int32 * max(self.B, 1))()
         self._check(self.lib.ddp_get_progress(self._h, C.byref(nxt), parked, C.byref(n)))
         return nxt.value, [parked[i] for i in range(n.value)]
+
+    # ---------------------------------------------------------------- communication hooks
+    def register_comm_hook(self, hook, replica_buffers, state=None):
+        """hook: "mean" | "bf16_compress" (built-in) or a callable
+        ``hook(bucket: _lib.GradBucket, stream: int) -> int|None`` that enqueues
+        its reduction into ``bucket.result`` on ``stream``; replica_buffers: W
+        device buffers (tensors or addresses) of ``arena_numel()`` elements of
+        the gradient dtype."""
+        if hook == "mean":
+            fn = C.cast(self.lib.ddp_hook_mean, _lib.HOOKFN)
+        elif hook == "bf16_compress":
+            fn = C.cast(self.lib.ddp_hook_bf16_compress, _lib.HOOKFN)
+        else:
+            user = hook
+
+            def trampoline(_state, bucket, stream):
+                try:
+                    rc = user(bucket.contents, stream)
+                    return int(rc or 0)
+                except Exception:       # noqa: BLE001 -- a Python error must not cross the C ABI
+                    return 1
+            fn = _lib.HOOKFN(trampoline)
+        rb = _ptr_array([_ptr(t) for t in replica_buffers])
+        self._check(self.lib.ddp_register_comm_hook(self._h, fn, state, rb))
+        self._hook_keep = (fn, rb, replica_buffers, hook)
 
     # ---------------------------------------------------------------- rebuild
     def get_ready_trace(self):

@@ -362,3 +362,20 @@ def test_unused_errors_and_bitmap_or(lib):
     plain.bind([[0x3000] * 3], 0x10000000, None)
     with pytest.raises(InvalidArg):
         plain.set_local_used([[True] * 3])    # needs DDP_OPT_FIND_UNUSED
+
+
+def test_hook_registration_rules(lib):
+    from reduction_reducer_gb300 import InvalidArg, NotBound, _lib as L
+    red = _make([4, 4], "f32", 16)
+    with pytest.raises(NotBound):
+        red.register_comm_hook("mean", [0x1000, 0x2000])
+    red.set_dry_run(True)
+    red.bind([[0x1000, 0x1100], [0x2000, 0x2100]], 0x10000000, None)
+    with pytest.raises(InvalidArg):
+        red.register_comm_hook("mean", [0x1000, 0x2008])      # misaligned replica buffer
+    red.register_comm_hook("mean", [0x1000, 0x2000])
+    with pytest.raises(InvalidArg):
+        red.register_comm_hook("mean", [0x1000, 0x2000])      # once only
+    with pytest.raises(InvalidArg):
+        red.set_option(L.OPT_FIND_UNUSED, 1)
+    assert lib.ddp_status_string(-8) == b"DDP_ERR_HOOK"
