@@ -564,7 +564,33 @@ def extra_configs(torch, device, stream, args, dist, keep):
         wl.free()
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
+    # whole iterations captured in a CUDA graph (launch-bound layouts)
+    for name, cap in (("gpt2_medium", 0), ("bert_large", 25)):
+        wl = Workload(name, torch, device, cap, n_out=1, driver="hooks")
+        graph_config(torch, wl, stream, steps, warm, dist, out, f"{name}_cap{cap}_graph")
+        wl.free()
+        torch.cuda.empty_cache()
     return out
+
+
+def graph_config(torch, wl, stream, steps, warm, dist, out, key):
+    """One iteration (begin_iteration + mark_ready_many) captured into a CUDA
+    graph after a warm-up iteration, replayed as the step."""
+    with torch.cuda.stream(stream):
+        wl.step(stream)                          # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            wl.step(stream)
+    launches = wl.red.launch_count()
+    with torch.cuda.stream(stream):
+        ms, _, _ = time_steps(torch, stream, g.replay, steps, warm, dist)
+    t = ms / steps
+    out[key] = {"gbs": round(wl.bytes / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4), "bytes_per_step": wl.bytes,
+                "buckets": wl.B, "W": wl.W, "kernel": kernel_name(wl),
+                "note": "iteration captured in a CUDA graph (PDL-chained launches), replayed per step"}
+    del g
 
 
 def hook_config(torch, device, keep, timed, out):

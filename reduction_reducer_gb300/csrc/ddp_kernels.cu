@@ -339,16 +339,39 @@ struct FlatMeanParams {
 };
 
 template <typename Tin>
-__global__ void __launch_bounds__(kMaxBlock) flat_mean_kernel(const __grid_constant__ FlatMeanParams p) {
+__device__ __forceinline__ float flat_term(const FlatMeanParams& p, int r, long long i) {
+    const float x = widen1(static_cast<const Tin*>(p.src[r])[i]);
+    return p.compress ? round_bf16(x) : x;
+}
+
+// vec != 0: every pointer 16-byte aligned; 16-byte loads over whole vectors,
+// the tail element by element.
+template <typename Tin>
+__global__ void __launch_bounds__(kMaxBlock) flat_mean_kernel(const __grid_constant__ FlatMeanParams p, int vec) {
     pdl_enter(0);
+    using V = Vec<Tin>;
+    constexpr int N = V::N;
     const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += step) {
-        float x = widen1(static_cast<const Tin*>(p.src[0])[i]);
-        float acc = p.compress ? round_bf16(x) : x;
+    const long long t0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nv = vec ? p.n / N : 0;
+    for (long long k = t0; k < nv; k += step) {
+        float acc[N], f[N];
+        V::unpack(ld_stream(reinterpret_cast<const typename V::Raw*>(static_cast<const Tin*>(p.src[0]) + k * N)), acc);
+        if (p.compress)
+            for (int q = 0; q < N; ++q) acc[q] = round_bf16(acc[q]);
         for (int r = 1; r < p.W; ++r) {
-            x = widen1(static_cast<const Tin*>(p.src[r])[i]);
-            acc = __fadd_rn(acc, p.compress ? round_bf16(x) : x);
+            V::unpack(ld_stream(reinterpret_cast<const typename V::Raw*>(static_cast<const Tin*>(p.src[r]) + k * N)), f);
+#pragma unroll
+            for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], p.compress ? round_bf16(f[q]) : f[q]);
         }
+#pragma unroll
+        for (int q = 0; q < N; q += 4)
+            st_stream(p.out + k * N + q, make_float4(__fmul_rn(acc[q], p.inv_w), __fmul_rn(acc[q + 1], p.inv_w),
+                                                     __fmul_rn(acc[q + 2], p.inv_w), __fmul_rn(acc[q + 3], p.inv_w)));
+    }
+    for (long long i = nv * N + t0; i < p.n; i += step) {
+        float acc = flat_term<Tin>(p, 0, i);
+        for (int r = 1; r < p.W; ++r) acc = __fadd_rn(acc, flat_term<Tin>(p, r, i));
         p.out[i] = __fmul_rn(acc, p.inv_w);
     }
 }
@@ -496,12 +519,18 @@ cudaError_t launch_flat_mean(InType in, int W, const void* const* src, float* ou
     p.inv_w = inv_w;
     p.W = W;
     p.compress = compress;
-    for (int r = 0; r < W; ++r) p.src[r] = src[r];
-    long long grid = ceil_div(n, 256);
+    int vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    for (int r = 0; r < W; ++r) {
+        p.src[r] = src[r];
+        vec = vec && (reinterpret_cast<uintptr_t>(src[r]) & 15u) == 0;
+    }
+    const int N = in == IN_F32 ? 4 : 8;
+    long long grid = ceil_div(vec ? ceil_div(n, N) : n, 256);
     const long long cap = static_cast<long long>(sms > 0 ? sms : 152) * 8;
     grid = grid < cap ? grid : cap;
-    return in == IN_F32 ? launch(flat_mean_kernel<float>, static_cast<int>(grid), 256, true, stream, p)
-                        : launch(flat_mean_kernel<uint16_t>, static_cast<int>(grid), 256, true, stream, p);
+    if (grid < 1) grid = 1;
+    return in == IN_F32 ? launch(flat_mean_kernel<float>, static_cast<int>(grid), 256, true, stream, p, vec)
+                        : launch(flat_mean_kernel<uint16_t>, static_cast<int>(grid), 256, true, stream, p, vec);
 }
 
 cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,

@@ -24,6 +24,7 @@
 // CTA exits.
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "ddp_device.cuh"
@@ -407,16 +408,19 @@ TmaKernel<M> pick_tma(InType in, int W) {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-// The dynamic shared-memory limit is raised once per kernel and device.
+// The dynamic shared-memory limit is raised once per kernel and device
+// (the cache is shared by every context and host thread).
 template <typename K>
 cudaError_t ensure_smem_attr(K k) {
     constexpr int kSlots = 64;
     static K done_k[kSlots];
     static int done_dev[kSlots];
     static int n_done = 0;
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n_done; ++i)
         if (done_k[i] == k && done_dev[i] == dev) return cudaSuccess;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);

@@ -46,7 +46,7 @@ def _setup(numel, W, dtype, cap, n_out, odd=False):
 
 @pytest.mark.parametrize("hook", ["mean", "bf16_compress"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("W,n_out", [(1, 1), (3, 1), (4, 4), (8, 0)])
+@pytest.mark.parametrize("W,n_out", [(1, 1), (3, 1), (4, 4), (8, 0), (33, 1)])
 def test_builtin_hooks(hook, dtype, W, n_out):
     numel = RAGGED
     cap = 16 * 1024

@@ -181,6 +181,15 @@ def test_ragged_every_W(W, dtype, kernel):
     full_compare(RAGGED, W, dtype, cap=64 * 1024, order="straggler", n_out=1, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [32, 64])
+def test_many_replicas(W, dtype, kernel):
+    """W beyond the compiled-in widths: the generic replica loop."""
+    numel = [3, 4097, 0, 70001, 16, 1000]
+    full_compare(numel, W, dtype, cap=32 * 1024, order="random", n_out=1, kernel=kernel)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n_out", [0, 1, "W"])
@@ -533,3 +542,40 @@ def test_rebuild_then_reduce(kernel):
     for v in range(len(numel)):
         assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])
     assert red.device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+def test_iteration_captured_in_cuda_graph(kernel):
+    """An iteration's launches (PDL-chained) captured into a CUDA graph and
+    replayed on new gradient values in the same buffers: each replay matches
+    the oracle on those values.  A warm-up iteration comes first, so the
+    one-time kernel attribute calls happen outside the capture."""
+    numel = RAGGED
+    W, cap = 4, 8 * 1024
+    flats, views, offs = host_grads(numel, W, "f32")
+    flat_dev, grads_dev = host_to_device_views(flats, numel, offs, "f32", DEV)
+    members, locs = assign_buckets(numel, 4, cap)
+    order = gen.straggler_order(members, p=0.5, seed=2)
+    red = Reducer(numel, "f32", cap)
+    set_kernel(red, kernel)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+    run_path(red, grads_dev, arena, outs, order=order, mode="mark_ready_many")   # warm-up
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            red.begin_iteration()
+            red.mark_ready_many(order, side)
+    torch.cuda.synchronize()
+    for step in (1, 2):
+        new_flats, new_views, _ = host_grads(numel, W, "f32", step=step)
+        for r in range(W):
+            flat_dev[r].copy_(torch.from_numpy(new_flats[r]).to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        want_arena, want_outs = reduce_buckets(new_views, members, locs, numel)
+        assert bits_equal(arena.cpu().numpy(), want_arena), first_mismatch(arena.cpu().numpy(), want_arena)
+        for v in range(len(numel)):
+            assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])

@@ -77,7 +77,7 @@ def _check_outputs(bufs, out_offs, numel, want_outs, used):
 
 @pytest.mark.parametrize("kernel", ["ldg", "tma"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("W", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 8, 64])
 def test_unused_reduce(W, dtype, kernel):
     numel = RAGGED
     P = len(numel)
