@@ -14,12 +14,18 @@ you can turn off"):
 
 Readings: the first micro-step *assigns* its gradient (the gradient field
 is empty before it, so ``acc = g_1`` exactly, keeping -0.0), every later one
-does ``acc = fl32(acc + g_k)`` in step order; fp32 gradients only.
+does ``acc = fl32(acc + g_k)`` in step order; fp32 gradients only.  The
+synchronizing backward that ends the block is one more micro-step whose
+gradient accumulates into the same fields before its hooks hand them to the
+bucket pass: each replica's reduced input is ``fl32(acc_r + g_r)``, formed
+per replica and only then summed in rank order.
 """
 
 from __future__ import annotations
 
 import numpy as np
+
+from .reduce import reduce_buckets
 
 
 def accumulate(acc, g, first_step: bool):
@@ -36,3 +42,11 @@ def accumulate_steps(steps):
     for k, g in enumerate(steps):
         acc = accumulate(acc, g, k == 0)
     return acc
+
+
+def reduce_last_step(acc, g_last, members, locators, numel, n_out: int = 1):
+    """The synchronizing micro-step: ``g_last`` accumulates into every
+    replica's fields (``acc`` is not changed), then the ordinary bucket pass
+    averages the sums.  Returns ``(arena, outs)`` as ``reduce_buckets``."""
+    summed = [accumulate(a, g, first_step=False) for a, g in zip(acc, g_last)]
+    return reduce_buckets(summed, members, locators, numel, n_out=n_out)
