@@ -270,6 +270,24 @@ int ddp_rebuild_buckets(ddp_ctx* ctx, const int32_t* order, int64_t first_cap_by
 int ddp_accumulate_nosync(ddp_ctx* ctx, void* const* acc, const void* const* g,
                           int32_t first_step, void* stream);
 
+/* The synchronizing micro-step that ends a no_sync block, fused into the bucket
+ * pass ("PyTorch Distributed", Section 3.2.4: the first backward after the
+ * block accumulates its gradient into the same fields and then reduces them).
+ * With g_last bound, every reduction of this context (ddp_mark_ready,
+ * ddp_mark_ready_many, ddp_reduce_bucket, ddp_reduce_all) takes replica r's
+ * input for variable v as fl32(grads[r*P+v] + g_last[r*P+v]), formed per
+ * replica before the rank-order sum: the result equals ddp_accumulate_nosync
+ * (first_step = 0) followed by the reduction, bit for bit, while each operand
+ * is read once and the accumulated fields are not written.
+ *   g_last  host array [W*P] of device fp32 addresses (numel[v] elements each;
+ *           W = the bound W), copied; NULL unbinds it (reductions read the bound
+ *           gradients alone again).  The caller owns the memory.
+ * ddp_bind drops a bound last step.  Between iterations only.
+ * Errors: INVALID_ARG (bf16 context, a NULL entry for a non-empty variable, a
+ *         communication hook registered, DDP_OPT_FIND_UNUSED on, inside an
+ *         unfinished iteration), NOT_BOUND, NO_MEMORY, CUDA. */
+int ddp_bind_last_step(ddp_ctx* ctx, const void* const* g_last);
+
 /* ---------------------------------------------------------------- no allocation */
 
 /* The fused pass of ddp_reduce_all over every bucket, for callers that may not
@@ -311,8 +329,11 @@ enum ddp_option {
     DDP_OPT_KERNEL = 4,           /* 0: register-streaming kernel, 1: bulk-copy (TMA) pipeline,
                                      2 (default): per context, bulk copy when the median bucket has at
                                      least DDP_OPT_AUTO_MIN_ELEMS elements, register streaming below */
-    DDP_OPT_STAGES = 5,           /* bulk-copy kernel: ring depth, 2..8 (default 3) */
-    DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB) */
+    DDP_OPT_STAGES = 5,           /* bulk-copy kernel: ring depth, 2..8 (default 3); fewer when the
+                                     stages would not fit in shared memory */
+    DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB);
+                                     raised to 4 KiB per tile for many streams (W > 8, or W > 4 with
+                                     a bound last step) */
     DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernel: CTAs per SM, 1 (default) or 2 */
     DDP_OPT_AUTO_MIN_ELEMS = 8,   /* kernel 2: median bucket length (elements) from which the bulk-copy
                                      kernel is used (default 2^20) */

@@ -70,6 +70,7 @@ SIGNATURES = {
     "ddp_get_ready_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "ddp_rebuild_buckets": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.c_int64, C.c_int64]),
     "ddp_accumulate_nosync": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
+    "ddp_bind_last_step": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p)]),
     "ddp_set_option": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
     "ddp_get_option": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64)]),
     "ddp_get_launch_count": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64)]),

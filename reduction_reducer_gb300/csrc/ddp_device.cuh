@@ -153,9 +153,18 @@ __device__ __forceinline__ bool any_replica(unsigned long long mk, int W) {
     return W >= 64 ? mk != 0ull : (mk & ((1ull << W) - 1ull)) != 0ull;
 }
 
+// Replica r's input at segment element j: its gradient, or with ADD (fused
+// last micro-step) fl32(accumulated + last-step gradient), whose pointers
+// are src[r] and src[W + r].
+template <bool ADD, typename Tin>
+__device__ __forceinline__ float replica_in(const Tin* const* src, int W, int r, long long j) {
+    if constexpr (ADD) return __fadd_rn(widen1(src[r][j]), widen1(src[W + r][j]));
+    else return widen1(src[r][j]);
+}
+
 // Rank-order fp32 mean of one element, scalar path (heads, tails, segments
 // whose pointers do not share the arena's 16-byte phase).
-template <typename Tin>
+template <typename Tin, bool ADD = false>
 __device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* const* src,
                                               float* const* dst, long long a0, long long x,
                                               long long e, int W, int tid, int nthr,
@@ -163,8 +172,8 @@ __device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* 
     const bool write_dst = any_replica(mk, W);
     for (long long a = x + tid; a < e; a += nthr) {
         const long long j = a - a0;
-        float acc = has_replica(mk, 0) ? widen1(src[0][j]) : 0.0f;
-        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, has_replica(mk, r) ? widen1(src[r][j]) : 0.0f);
+        float acc = has_replica(mk, 0) ? replica_in<ADD>(src, W, 0, j) : 0.0f;
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, has_replica(mk, r) ? replica_in<ADD>(src, W, r, j) : 0.0f);
         const float m = __fmul_rn(acc, p.inv_w);
         p.arena[a] = m;
         if (write_dst)

@@ -70,6 +70,7 @@ struct ddp_ctx {
     // ---- binding
     bool bound = false;
     std::vector<const void*> bind_grads;          // W*P, kept for rebuilds
+    std::vector<const void*> bind_last;           // W*P last-step gradients (fused last micro-step), or empty
     std::vector<float*> bind_outs;                // n_out*P
     int W = 0;
     int n_out = 0;
@@ -220,7 +221,8 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->cfg.sms = sms;
     c->cfg.block = c->opt_block;
     c->cfg.pdl = c->pdl;
-    c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas : ddpk::reduce_max_ctas_per_sm(in, c->W, c->opt_block);
+    c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas
+                                         : ddpk::reduce_max_ctas_per_sm(in, c->W, c->opt_block, c->tab.add != 0);
     if (c->opt_kernel == ddpk::KERNEL_AUTO) {
         std::vector<int64_t> lens;
         for (int32_t b = 0; b < c->B; ++b) lens.push_back(c->bucket_off[b + 1] - c->bucket_off[b]);
@@ -448,9 +450,15 @@ namespace {
 
 // Build the segment table of the current layout for the given pointers and
 // upload it (replacing any previous table).
-int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_arena, float* const* grad_out,
-                int32_t n_out) {
+// last: W*P last-step gradients (fused last micro-step; fp32) or nullptr.
+int build_table(ddp_ctx* c, int32_t W, const void* const* grads, const void* const* last, float* bucket_arena,
+                float* const* grad_out, int32_t n_out) {
     const int64_t total = c->bucket_off[c->B];
+    // source streams per segment: the W gradients, then the W last-step gradients
+    const int NS = last ? 2 * W : W;
+    auto source = [&](int q, int32_t v) -> const void* {
+        return q < W ? grads[static_cast<int64_t>(q) * c->P + v] : last[static_cast<int64_t>(q - W) * c->P + v];
+    };
 
     // Host segment table: merge consecutive members of a bucket whose
     // gradients (every replica) and outputs (every copy) are contiguous.
@@ -468,10 +476,11 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
                 const int64_t n = c->numel[v];
                 if (n == 0) continue;
                 const int64_t a0 = c->bucket_off[b] + c->loc[v].offset;
-                for (int r = 0; r < W; ++r)
-                    if (!grads[static_cast<int64_t>(r) * c->P + v])
-                        return fail(c, DDP_ERR_INVALID_ARG, "NULL gradient for replica " + std::to_string(r) +
-                                                                " variable " + std::to_string(v));
+                for (int q = 0; q < NS; ++q)
+                    if (!source(q, v))
+                        return fail(c, DDP_ERR_INVALID_ARG,
+                                    std::string(q < W ? "NULL gradient" : "NULL last-step gradient") + " for replica " +
+                                        std::to_string(q % W) + " variable " + std::to_string(v));
                 for (int o = 0; o < n_out; ++o)
                     if (!grad_out[static_cast<int64_t>(o) * c->P + v])
                         return fail(c, DDP_ERR_INVALID_ARG, "NULL output for copy " + std::to_string(o) +
@@ -481,9 +490,9 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
                 bool merge = !c->opt_find_unused && static_cast<int32_t>(S) > bucket_seg[b];
                 if (merge) {
                     const int64_t plen = seg_len[S - 1];
-                    for (int r = 0; r < W && merge; ++r) {
-                        const char* prev = static_cast<const char*>(seg_src[(S - 1) * W + r]);
-                        merge = static_cast<const char*>(grads[static_cast<int64_t>(r) * c->P + v]) == prev + plen * c->elem;
+                    for (int q = 0; q < NS && merge; ++q) {
+                        const char* prev = static_cast<const char*>(seg_src[(S - 1) * NS + q]);
+                        merge = static_cast<const char*>(source(q, v)) == prev + plen * c->elem;
                     }
                     for (int o = 0; o < n_out && merge; ++o)
                         merge = grad_out[static_cast<int64_t>(o) * c->P + v] == seg_dst[(S - 1) * n_out + o] + plen;
@@ -495,8 +504,8 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
                 // 128-bit path: element a of the arena is 16-byte aligned when a is
                 // a multiple of the vector width; require the same of every stream.
                 bool vec = true;
-                for (int r = 0; r < W; ++r) {
-                    const uintptr_t p = reinterpret_cast<uintptr_t>(grads[static_cast<int64_t>(r) * c->P + v]);
+                for (int q = 0; q < NS; ++q) {
+                    const uintptr_t p = reinterpret_cast<uintptr_t>(source(q, v));
                     vec = vec && is_aligned16(p - static_cast<uintptr_t>(a0 * c->elem));
                 }
                 for (int o = 0; o < n_out; ++o) {
@@ -506,7 +515,7 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
                 seg_off.push_back(a0);
                 seg_len.push_back(n);
                 seg_var.push_back(v);
-                for (int r = 0; r < W; ++r) seg_src.push_back(grads[static_cast<int64_t>(r) * c->P + v]);
+                for (int q = 0; q < NS; ++q) seg_src.push_back(source(q, v));
                 for (int o = 0; o < n_out; ++o) seg_dst.push_back(grad_out[static_cast<int64_t>(o) * c->P + v]);
                 seg_vec.push_back(vec ? 1 : 0);
             }
@@ -565,6 +574,7 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_a
     c->tab.seg_dst = reinterpret_cast<float* const*>(base + b_off + b_src);
     c->tab.seg_vec = reinterpret_cast<const int*>(base + b_off + b_src + b_dst);
     c->tab.status = reinterpret_cast<int*>(base + b_off + b_src + b_dst + b_vec);
+    c->tab.add = last ? 1 : 0;
     c->bucket_seg = std::move(bucket_seg);
     c->seg_off_h = seg_off;
     c->seg_var = std::move(seg_var);
@@ -602,13 +612,38 @@ int ddp_bind(ddp_ctx* c, int32_t W, const void* const* grads, float* bucket_aren
     }
     if (c->opt_find_unused && W > 64)
         return fail(c, DDP_ERR_INVALID_ARG, "unused-parameter tracking supports W <= 64");
-    const int st = build_table(c, W, g_copy.data(), bucket_arena, o_copy.empty() ? nullptr : o_copy.data(), n_out);
+    const int st = build_table(c, W, g_copy.data(), nullptr, bucket_arena, o_copy.empty() ? nullptr : o_copy.data(),
+                               n_out);
     if (st != DDP_OK) return st;
     c->bind_grads = std::move(g_copy);
+    c->bind_last.clear();
     c->bind_outs = std::move(o_copy);
     c->pending_used.clear();
     c->pending_set = false;
     c->has_grad.clear();
+    return DDP_OK;
+}
+
+int ddp_bind_last_step(ddp_ctx* c, const void* const* g_last) {
+    if (!c) return DDP_ERR_INVALID_ARG;
+    if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "bind the accumulated gradients first");
+    if (c->active) return fail(c, DDP_ERR_INVALID_ARG, "the last step changes between iterations only");
+    std::vector<const void*> last;
+    if (g_last) {
+        if (c->dtype != DDP_F32) return fail(c, DDP_ERR_INVALID_ARG, "the fused last step needs fp32 gradients");
+        if (c->hook) return fail(c, DDP_ERR_INVALID_ARG, "a bound last step does not combine with hooks");
+        if (c->opt_find_unused)
+            return fail(c, DDP_ERR_INVALID_ARG, "a bound last step does not combine with DDP_OPT_FIND_UNUSED");
+        try {
+            last.assign(g_last, g_last + static_cast<int64_t>(c->W) * c->P);
+        } catch (const std::bad_alloc&) {
+            return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
+        }
+    }
+    const int st = build_table(c, c->W, c->bind_grads.data(), last.empty() ? nullptr : last.data(), c->arena,
+                               c->bind_outs.empty() ? nullptr : c->bind_outs.data(), c->n_out);
+    if (st != DDP_OK) return st;
+    c->bind_last = std::move(last);
     return DDP_OK;
 }
 
@@ -620,6 +655,7 @@ int ddp_register_comm_hook(ddp_ctx* c, ddp_comm_hook_fn hook, void* state, void*
     if (c->launches > 0 || c->active) return fail(c, DDP_ERR_INVALID_ARG, "register the hook before the first launch");
     if (c->W > ddpk::kMaxHookReplicas) return fail(c, DDP_ERR_INVALID_ARG, "hooks support W <= 64");
     if (c->opt_find_unused) return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with DDP_OPT_FIND_UNUSED");
+    if (!c->bind_last.empty()) return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with a bound last step");
     if (c->bucket_off[c->B] > 0 && !replica_buffers) return fail(c, DDP_ERR_INVALID_ARG, "replica_buffers is NULL");
     std::vector<void*> rb(c->W, nullptr);
     for (int r = 0; r < c->W && c->bucket_off[c->B] > 0; ++r) {
@@ -690,8 +726,8 @@ int ddp_rebuild_buckets(ddp_ctx* c, const int32_t* order, int64_t first_cap_byte
     reset_iteration(c);
     c->active = false;
     if (!c->bound) return DDP_OK;
-    return build_table(c, c->W, c->bind_grads.data(), c->arena, c->bind_outs.empty() ? nullptr : c->bind_outs.data(),
-                       c->n_out);
+    return build_table(c, c->W, c->bind_grads.data(), c->bind_last.empty() ? nullptr : c->bind_last.data(), c->arena,
+                       c->bind_outs.empty() ? nullptr : c->bind_outs.data(), c->n_out);
 }
 
 int ddp_begin_iteration(ddp_ctx* c) {
@@ -893,6 +929,8 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             if (c->active) return fail(c, DDP_ERR_INVALID_ARG, "find_unused changes between iterations only");
             if (value != 0 && c->hook)
                 return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with DDP_OPT_FIND_UNUSED");
+            if (value != 0 && !c->bind_last.empty())
+                return fail(c, DDP_ERR_INVALID_ARG, "a bound last step does not combine with DDP_OPT_FIND_UNUSED");
             const bool on = value != 0;
             if (on && c->bound && c->W > 64)
                 return fail(c, DDP_ERR_INVALID_ARG, "unused-parameter tracking supports W <= 64");
@@ -902,7 +940,7 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             c->pending_set = false;
             c->has_grad.clear();
             if (!c->bound) return DDP_OK;   // a bound context gets an unmerged (or merged) table now
-            return build_table(c, c->W, c->bind_grads.data(), c->arena,
+            return build_table(c, c->W, c->bind_grads.data(), nullptr, c->arena,
                                c->bind_outs.empty() ? nullptr : c->bind_outs.data(), c->n_out);
         }
         case DDP_OPT_KERNEL:

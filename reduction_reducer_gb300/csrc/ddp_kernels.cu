@@ -58,28 +58,32 @@ __host__ __device__ constexpr int unroll_for() { return WC <= 2 ? 4 : (WC <= 8 ?
 template <typename Raw>
 __device__ __forceinline__ Raw zero_raw() { return Raw{}; }
 
-// Vector body, W known at compile time: all WC x U loads in flight at once.
-template <typename Tin, int WC, int U>
+// Vector body, W known at compile time: all NS x U loads in flight at once
+// (NS = WC streams, or 2 WC with ADD: the accumulated fields and the last
+// micro-step's gradients).  Replica r's input is its vector, or with ADD
+// fl32(acc_r + g_r), added into the rank-order sum.
+template <typename Tin, int WC, int U, bool ADD>
 __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Tin* const* src,
                                                  float* const* dst, long long a0, long long kb,
                                                  long long ke, unsigned long long mk) {
     using V = Vec<Tin>;
     constexpr int N = V::N;
+    constexpr int NS = ADD ? 2 * WC : WC;
     const bool write_dst = any_replica(mk, WC);
-    const Tin* s[WC];
+    const Tin* s[NS];
 #pragma unroll
-    for (int r = 0; r < WC; ++r) s[r] = src[r];
+    for (int r = 0; r < NS; ++r) s[r] = src[r];
     const long long step = static_cast<long long>(blockDim.x);
     for (long long k = kb + threadIdx.x; k < ke; k += U * step) {
-        typename V::Raw raw[U][WC];
+        typename V::Raw raw[U][NS];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const long long kk = k + u * step;
             if (kk < ke) {
                 const long long j = kk * N - a0;
 #pragma unroll
-                for (int r = 0; r < WC; ++r)
-                    raw[u][r] = has_replica(mk, r)
+                for (int r = 0; r < NS; ++r)
+                    raw[u][r] = has_replica(mk, r % WC)
                                     ? ld_stream(reinterpret_cast<const typename V::Raw*>(s[r] + j))
                                     : zero_raw<typename V::Raw>();
             }
@@ -90,9 +94,20 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
             if (kk < ke) {
                 float acc[N], f[N];
                 V::unpack(raw[u][0], acc);
+                if constexpr (ADD) {
+                    V::unpack(raw[u][WC], f);
+#pragma unroll
+                    for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+                }
 #pragma unroll
                 for (int r = 1; r < WC; ++r) {
                     V::unpack(raw[u][r], f);
+                    if constexpr (ADD) {
+                        float h[N];
+                        V::unpack(raw[u][WC + r], h);
+#pragma unroll
+                        for (int q = 0; q < N; ++q) f[q] = __fadd_rn(f[q], h[q]);
+                    }
 #pragma unroll
                     for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
                 }
@@ -104,8 +119,27 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
     }
 }
 
+// One replica's 16-byte vector of inputs (ADD: accumulated + last step).
+template <typename Tin, bool ADD>
+__device__ __forceinline__ void load_replica(const Tin* const* src, int W, int r, long long j,
+                                             unsigned long long mk, float (&f)[Vec<Tin>::N]) {
+    using V = Vec<Tin>;
+    using Raw = typename V::Raw;
+    if (!has_replica(mk, r)) {
+        V::unpack(zero_raw<Raw>(), f);
+        return;
+    }
+    V::unpack(ld_stream(reinterpret_cast<const Raw*>(src[r] + j)), f);
+    if constexpr (ADD) {
+        float h[V::N];
+        V::unpack(ld_stream(reinterpret_cast<const Raw*>(src[W + r] + j)), h);
+#pragma unroll
+        for (int q = 0; q < V::N; ++q) f[q] = __fadd_rn(f[q], h[q]);
+    }
+}
+
 // Vector body for any W: replicas in groups of 4, still summed in rank order.
-template <typename Tin>
+template <typename Tin, bool ADD>
 __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin* const* src,
                                                float* const* dst, long long a0, long long kb,
                                                long long ke, int W, unsigned long long mk) {
@@ -114,24 +148,18 @@ __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin*
     const bool write_dst = any_replica(mk, W);
     for (long long k = kb + threadIdx.x; k < ke; k += blockDim.x) {
         const long long j = k * N - a0;
-        float acc[N], f[N];
-        V::unpack(has_replica(mk, 0) ? ld_stream(reinterpret_cast<const typename V::Raw*>(src[0] + j))
-                                     : zero_raw<typename V::Raw>(),
-                  acc);
+        float acc[N];
+        load_replica<Tin, ADD>(src, W, 0, j, mk, acc);
         for (int r = 1; r < W; r += 4) {
-            typename V::Raw raw[4];
+            float f[4][N];
 #pragma unroll
             for (int g = 0; g < 4; ++g)
-                if (r + g < W)
-                    raw[g] = has_replica(mk, r + g)
-                                 ? ld_stream(reinterpret_cast<const typename V::Raw*>(src[r + g] + j))
-                                 : zero_raw<typename V::Raw>();
+                if (r + g < W) load_replica<Tin, ADD>(src, W, r + g, j, mk, f[g]);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 if (r + g < W) {
-                    V::unpack(raw[g], f);
 #pragma unroll
-                    for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+                    for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[g][q]);
                 }
             }
         }
@@ -142,14 +170,17 @@ __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin*
 }
 
 // M = NoMask (every replica has every gradient) or SegMask (unused parameters).
-template <typename Tin, int WC, typename M>
+// ADD: fused last micro-step of a no_sync block (2W source streams per
+// segment, see SegTable).
+template <typename Tin, int WC, typename M, bool ADD>
 __global__ void __launch_bounds__(kMaxBlock)
 bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_constant__ M mask) {
     pdl_enter(p.chain);
     using V = Vec<Tin>;
     constexpr int N = V::N;
-    constexpr int U = WC == 0 ? 1 : unroll_for<WC>();
+    constexpr int U = WC == 0 ? 1 : unroll_for<ADD ? 2 * WC : WC>();
     const int W = WC > 0 ? WC : p.W;
+    const int NS = ADD ? 2 * W : W;
 
     long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
     long long y = x + p.piece;
@@ -165,20 +196,20 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_consta
         const long long a0 = __ldg(p.seg_off + s);
         const long long a1 = __ldg(p.seg_off + s + 1);
         const long long e = a1 < y ? a1 : y;
-        const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(s) * W;
+        const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(s) * NS;
         float* const* dst = p.seg_dst + static_cast<long long>(s) * p.n_out;
         const unsigned long long mk = seg_mask(mask, s - p.s0);
         const long long kb = (x + N - 1) / N;   // first whole vector
         const long long ke = e / N;             // one past the last whole vector
         if (__ldg(p.seg_vec + s) && kb < ke) {
-            reduce_scalar<Tin>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x, mk);
+            reduce_scalar<Tin, ADD>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x, mk);
             if constexpr (WC > 0)
-                reduce_vec_fixed<Tin, WC, U>(p, src, dst, a0, kb, ke, mk);
+                reduce_vec_fixed<Tin, WC, U, ADD>(p, src, dst, a0, kb, ke, mk);
             else
-                reduce_vec_any<Tin>(p, src, dst, a0, kb, ke, W, mk);
-            reduce_scalar<Tin>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x, mk);
+                reduce_vec_any<Tin, ADD>(p, src, dst, a0, kb, ke, W, mk);
+            reduce_scalar<Tin, ADD>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x, mk);
         } else {
-            reduce_scalar<Tin>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x, mk);
+            reduce_scalar<Tin, ADD>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x, mk);
         }
         x = e;
         ++s;
@@ -400,19 +431,30 @@ template <typename M>
 ReduceKernel<M> pick_reduce(InType in, int W) {
     if (in == IN_F32) {
         switch (W) {
-            case 2: return bucket_reduce_kernel<float, 2, M>;
-            case 4: return bucket_reduce_kernel<float, 4, M>;
-            case 8: return bucket_reduce_kernel<float, 8, M>;
-            case 16: return bucket_reduce_kernel<float, 16, M>;
-            default: return bucket_reduce_kernel<float, 0, M>;
+            case 2: return bucket_reduce_kernel<float, 2, M, false>;
+            case 4: return bucket_reduce_kernel<float, 4, M, false>;
+            case 8: return bucket_reduce_kernel<float, 8, M, false>;
+            case 16: return bucket_reduce_kernel<float, 16, M, false>;
+            default: return bucket_reduce_kernel<float, 0, M, false>;
         }
     }
     switch (W) {
-        case 2: return bucket_reduce_kernel<uint16_t, 2, M>;
-        case 4: return bucket_reduce_kernel<uint16_t, 4, M>;
-        case 8: return bucket_reduce_kernel<uint16_t, 8, M>;
-        case 16: return bucket_reduce_kernel<uint16_t, 16, M>;
-        default: return bucket_reduce_kernel<uint16_t, 0, M>;
+        case 2: return bucket_reduce_kernel<uint16_t, 2, M, false>;
+        case 4: return bucket_reduce_kernel<uint16_t, 4, M, false>;
+        case 8: return bucket_reduce_kernel<uint16_t, 8, M, false>;
+        case 16: return bucket_reduce_kernel<uint16_t, 16, M, false>;
+        default: return bucket_reduce_kernel<uint16_t, 0, M, false>;
+    }
+}
+
+// Fused last-step variant: fp32 accumulators, every replica present.
+ReduceKernel<NoMask> pick_reduce_add(int W) {
+    switch (W) {
+        case 2: return bucket_reduce_kernel<float, 2, NoMask, true>;
+        case 4: return bucket_reduce_kernel<float, 4, NoMask, true>;
+        case 8: return bucket_reduce_kernel<float, 8, NoMask, true>;
+        case 16: return bucket_reduce_kernel<float, 16, NoMask, true>;
+        default: return bucket_reduce_kernel<float, 0, NoMask, true>;
     }
 }
 
@@ -420,9 +462,10 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-int reduce_max_ctas_per_sm(InType in, int W, int block) {
+int reduce_max_ctas_per_sm(InType in, int W, int block, bool add) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick_reduce<NoMask>(in, W), block, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, add ? pick_reduce_add(W) : pick_reduce<NoMask>(in, W),
+                                                      block, 0) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
@@ -467,10 +510,11 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
     if (grid < 1) grid = 1;
     p.piece = ceil_div(ceil_div(span, grid), N) * N;
     grid = ceil_div(span, p.piece);
+    if (t.add && (mask || in != IN_F32)) return cudaErrorInvalidValue;   // no such variant
     cudaError_t err = mask ? launch(pick_reduce<SegMask>(in, W), static_cast<int>(grid), cfg.block, cfg.pdl,
                                     stream, p, *mask)
-                           : launch(pick_reduce<NoMask>(in, W), static_cast<int>(grid), cfg.block, cfg.pdl,
-                                    stream, p, NoMask{});
+                           : launch(t.add ? pick_reduce_add(W) : pick_reduce<NoMask>(in, W), static_cast<int>(grid),
+                                    cfg.block, cfg.pdl, stream, p, NoMask{});
     if (err == cudaSuccess && launches) ++*launches;
     return err;
 }

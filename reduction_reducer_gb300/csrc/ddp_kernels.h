@@ -16,12 +16,17 @@ namespace ddpk {
 // copy o's first element; seg_vec[s] != 0 when every pointer has the same
 // 16-byte phase as the arena, so 128-bit accesses (and bulk copies) line up.
 // status is a device word the kernels set when a bounded wait gives up.
+// add != 0 (fused last micro-step of a no_sync block, fp32 only): each
+// segment has 2W source pointers, seg_src[s*2W + r] replica r's accumulated
+// gradient and seg_src[s*2W + W + r] its last-step gradient; replica r then
+// contributes fl32(acc_r + g_r).
 struct SegTable {
     const long long* seg_off;
     const void* const* seg_src;
     float* const* seg_dst;
     const int* seg_vec;
     int* status;
+    int add;
 };
 
 // KERNEL_AUTO is resolved per context by the host core (median bucket size).
@@ -65,8 +70,9 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
                           const LaunchCfg& cfg, cudaStream_t stream, long long* launches,
                           const SegMask* mask = nullptr);
 
-// Largest number of resident CTAs per SM of the register-streaming kernel.
-int reduce_max_ctas_per_sm(InType in, int W, int block);
+// Largest number of resident CTAs per SM of the register-streaming kernel
+// (add: the fused last-step variant).
+int reduce_max_ctas_per_sm(InType in, int W, int block, bool add = false);
 
 // One accumulation pair: acc = g (assign) or acc = fl32(acc + g) over len elements.
 struct AccPair {

@@ -5,23 +5,25 @@
 // x fl32(1/W), bucket write, copy-back), with the loads moved off the
 // register file:
 //
-//   * one producer thread per CTA walks the CTA's slice of the launch and,
+//   * one producer warp per CTA walks the CTA's slice of the launch and,
 //     for every aligned chunk of a segment, issues W one-dimensional bulk
 //     copies (cp.async.bulk, global -> shared) into one stage of a ring in
-//     shared memory; an mbarrier per stage counts the landed bytes;
+//     shared memory, one lane per copy; an mbarrier per stage counts the
+//     landed bytes;
 //   * eight consumer warps wait for a stage, sum the W tiles from shared
 //     memory in rank order, scale, and stream the means to the arena and
 //     the copy-back outputs with 128-bit evict-first stores, then release
 //     the stage through a second mbarrier;
-//   * with 3 stages of 64 KiB each CTA keeps up to ~190 KiB of loads in
-//     flight independently of register pressure, one CTA per SM.
+//   * with the default ring of 3 stages x 32 KiB a CTA keeps 96 KiB of loads
+//     in flight independently of register pressure; two such CTAs fit in an
+//     SM, so the next launch's CTAs can start beside a draining one.
 //
 // Ragged heads/tails and segments whose pointers do not share the arena's
 // 16-byte phase bypass the ring (consumers load them directly).  Every
 // mbarrier wait is bounded: after ~2 s it records a code in the device
 // status word and carries on, so a fault in the pipeline can never hang the
-// GPU; the producer waits (bounded) for all of its copies to land before the
-// CTA exits.
+// GPU; lane 0 of the producer warp waits (bounded) for all of the CTA's
+// copies to land before the CTA exits.
 
 #include <cstdint>
 #include <mutex>
@@ -41,6 +43,7 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 constexpr int kMaxDynSmem = 232448;                // 227 KiB opt-in per CTA
 constexpr int kHeaderBytes = 128;                  // mbarriers, ring starts after
+constexpr long long kMinCopyBytes = 4096;          // smallest per-stream copy a stage is sized for
 
 // status codes written by bounded waits
 constexpr int kStatusEmptyTimeout = 1;
@@ -134,18 +137,22 @@ __device__ __forceinline__ void walk(const ReduceParams& p, int s, long long x, 
     }
 }
 
-template <typename Tin, int WC, typename M>
+// ADD: fused last micro-step of a no_sync block -- a stage holds 2W tiles
+// (the W accumulated fields, then the W last-step gradients) and replica r
+// contributes fl32(acc_r + g_r).
+template <typename Tin, int WC, typename M, bool ADD>
 __global__ void __launch_bounds__(kThreads, 1)
 bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_constant__ M mask) {
     extern __shared__ __align__(128) unsigned char smem[];
     using V = Vec<Tin>;
     constexpr int N = V::N;
     const int W = WC > 0 ? WC : p.W;
+    const int NS = ADD ? 2 * W : W;   // source streams per segment
     const int S = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + S;
     Tin* ring = reinterpret_cast<Tin*>(smem + kHeaderBytes);
-    const long long stage_elems = static_cast<long long>(W) * p.tile;
+    const long long stage_elems = static_cast<long long>(NS) * p.tile;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -170,8 +177,11 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
     const int s = find_segment(p.seg_off, p.s0, p.s1, x);
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        if (lane != 0) return;
+        // ---------------------------------------------------------- producer warp
+        // Every lane walks the same chunk sequence and waits for the stage
+        // itself; lane 0 posts the stage's byte count, then lane q issues the
+        // copies of streams q, q + 32, ...: a stage's copies go out in
+        // parallel instead of one after another from a single thread.
         long long k = 0;
         bool failed = false;
         walk<N>(
@@ -184,17 +194,21 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
                 const uint32_t fb = smem_u32(full + st);
                 // replicas without a gradient for this segment copy nothing
                 const unsigned long long mk = seg_mask(mask, sg - p.s0);
-                uint32_t present = 0;
-                for (int r = 0; r < W; ++r) present += has_replica(mk, r) ? 1u : 0u;
-                mbar_expect_tx(fb, bytes * present);
-                const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * W;
+                if (lane == 0) {
+                    uint32_t present = 0;
+                    for (int q = 0; q < NS; ++q) present += has_replica(mk, q % W) ? 1u : 0u;
+                    mbar_expect_tx(fb, bytes * present);
+                }
+                __syncwarp();
+                const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * NS;
                 Tin* dst = ring + st * stage_elems;
-                for (int r = 0; r < W; ++r)
-                    if (has_replica(mk, r))
-                        bulk_g2s(smem_u32(dst + static_cast<long long>(r) * p.tile), src[r] + (c - a0), bytes, fb);
+                for (int q = lane; q < NS; q += 32)
+                    if (has_replica(mk, q % W))
+                        bulk_g2s(smem_u32(dst + static_cast<long long>(q) * p.tile), src[q] + (c - a0), bytes, fb);
                 ++k;
             },
             [](int, long long, long long, long long) {});
+        if (lane != 0) return;
         // every issued copy must land before the CTA may exit
         for (long long j = k > S ? k - S : 0; j < k; ++j)
             mbar_wait(smem_u32(full + j % S), static_cast<uint32_t>(j / S) & 1u, p.status, kStatusDrainTimeout, failed);
@@ -219,22 +233,32 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
             const bool write_dst = any_replica(mk, W);
             const int nv = static_cast<int>(L / N);
             using Raw = typename V::Raw;
+            // replica r's input vector v of this stage (ADD: accumulated + last step)
+            auto input = [&](int r, int v, float (&f)[N]) {
+                const long long at = static_cast<long long>(r) * p.tile + v * N;
+                V::unpack(has_replica(mk, r) ? *reinterpret_cast<const Raw*>(base + at) : Raw{}, f);
+                if constexpr (ADD) {
+                    float h[N];
+                    V::unpack(has_replica(mk, r) ? *reinterpret_cast<const Raw*>(base + at + static_cast<long long>(W) * p.tile)
+                                                 : Raw{},
+                              h);
+#pragma unroll
+                    for (int q = 0; q < N; ++q) f[q] = __fadd_rn(f[q], h[q]);
+                }
+            };
             for (int v = tc; v < nv; v += nct) {
                 float acc[N], f[N];
-                V::unpack(has_replica(mk, 0) ? *reinterpret_cast<const Raw*>(base + v * N) : Raw{}, acc);
+                input(0, v, acc);
                 if constexpr (WC > 0) {
 #pragma unroll
                     for (int r = 1; r < WC; ++r) {
-                        V::unpack(has_replica(mk, r) ? *reinterpret_cast<const Raw*>(base + r * p.tile + v * N) : Raw{}, f);
+                        input(r, v, f);
 #pragma unroll
                         for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
                     }
                 } else {
                     for (int r = 1; r < W; ++r) {
-                        V::unpack(has_replica(mk, r)
-                                      ? *reinterpret_cast<const Raw*>(base + static_cast<long long>(r) * p.tile + v * N)
-                                      : Raw{},
-                                  f);
+                        input(r, v, f);
 #pragma unroll
                         for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
                     }
@@ -249,9 +273,9 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
             ++k;
         },
         [&](int sg, long long a0, long long lo, long long hi) {
-            const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * W;
+            const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * NS;
             float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
-            reduce_scalar<Tin>(p, src, dst, a0, lo, hi, W, tc, nct, seg_mask(mask, sg - p.s0));
+            reduce_scalar<Tin, ADD>(p, src, dst, a0, lo, hi, W, tc, nct, seg_mask(mask, sg - p.s0));
         });
 }
 
@@ -390,19 +414,30 @@ template <typename M>
 TmaKernel<M> pick_tma(InType in, int W) {
     if (in == IN_F32) {
         switch (W) {
-            case 2: return bucket_reduce_tma_kernel<float, 2, M>;
-            case 4: return bucket_reduce_tma_kernel<float, 4, M>;
-            case 8: return bucket_reduce_tma_kernel<float, 8, M>;
-            case 16: return bucket_reduce_tma_kernel<float, 16, M>;
-            default: return bucket_reduce_tma_kernel<float, 0, M>;
+            case 2: return bucket_reduce_tma_kernel<float, 2, M, false>;
+            case 4: return bucket_reduce_tma_kernel<float, 4, M, false>;
+            case 8: return bucket_reduce_tma_kernel<float, 8, M, false>;
+            case 16: return bucket_reduce_tma_kernel<float, 16, M, false>;
+            default: return bucket_reduce_tma_kernel<float, 0, M, false>;
         }
     }
     switch (W) {
-        case 2: return bucket_reduce_tma_kernel<uint16_t, 2, M>;
-        case 4: return bucket_reduce_tma_kernel<uint16_t, 4, M>;
-        case 8: return bucket_reduce_tma_kernel<uint16_t, 8, M>;
-        case 16: return bucket_reduce_tma_kernel<uint16_t, 16, M>;
-        default: return bucket_reduce_tma_kernel<uint16_t, 0, M>;
+        case 2: return bucket_reduce_tma_kernel<uint16_t, 2, M, false>;
+        case 4: return bucket_reduce_tma_kernel<uint16_t, 4, M, false>;
+        case 8: return bucket_reduce_tma_kernel<uint16_t, 8, M, false>;
+        case 16: return bucket_reduce_tma_kernel<uint16_t, 16, M, false>;
+        default: return bucket_reduce_tma_kernel<uint16_t, 0, M, false>;
+    }
+}
+
+// Fused last-step variant: fp32 accumulators, every replica present.
+TmaKernel<NoMask> pick_tma_add(int W) {
+    switch (W) {
+        case 2: return bucket_reduce_tma_kernel<float, 2, NoMask, true>;
+        case 4: return bucket_reduce_tma_kernel<float, 4, NoMask, true>;
+        case 8: return bucket_reduce_tma_kernel<float, 8, NoMask, true>;
+        case 16: return bucket_reduce_tma_kernel<float, 16, NoMask, true>;
+        default: return bucket_reduce_tma_kernel<float, 0, NoMask, true>;
     }
 }
 
@@ -501,14 +536,23 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
                               const LaunchCfg& cfg, cudaStream_t stream, long long* launches,
                               const SegMask* mask) {
     if (hi <= lo || s1 <= s0) return cudaSuccess;
+    if (t.add && (mask || in != IN_F32)) return cudaErrorInvalidValue;   // no such variant
     const int N = in == IN_F32 ? 4 : 8;
     const int s_in = in == IN_F32 ? 4 : 2;
-    const int stages = cfg.stages < 2 ? 2 : cfg.stages;
-    long long tile = static_cast<long long>(cfg.stage_bytes) / (static_cast<long long>(W) * s_in) / N * N;
+    const long long NS = t.add ? 2LL * W : W;   // tiles per stage
+    // A stage holds one copy per stream.  Copies under a few KiB run into the
+    // copy engine's per-request cost (measured on GB300: 1 KiB copies reach
+    // ~4.5 TB/s, 4 KiB ones ~6.8), so many streams get larger stages, and
+    // fewer of them where the ring would not fit.
+    long long stage_bytes = cfg.stage_bytes;
+    if (stage_bytes < NS * kMinCopyBytes) stage_bytes = NS * kMinCopyBytes;
+    int stages = cfg.stages < 2 ? 2 : cfg.stages;
+    while (stages > 2 && kHeaderBytes + stages * stage_bytes > kMaxDynSmem) --stages;
+    long long tile = stage_bytes / (NS * s_in) / N * N;
     if (tile < N) tile = N;
-    while (tile > N && kHeaderBytes + static_cast<long long>(stages) * W * tile * s_in > kMaxDynSmem)
+    while (tile > N && kHeaderBytes + static_cast<long long>(stages) * NS * tile * s_in > kMaxDynSmem)
         tile -= N;
-    const long long smem = kHeaderBytes + static_cast<long long>(stages) * W * tile * s_in;
+    const long long smem = kHeaderBytes + static_cast<long long>(stages) * NS * tile * s_in;
     if (smem > kMaxDynSmem || 2 * stages * 8 > kHeaderBytes) return cudaErrorInvalidValue;
 
     ReduceParams p = {};
@@ -536,7 +580,8 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     p.piece = ceil_div(ceil_div(span, grid), N) * N;
     grid = ceil_div(span, p.piece);
 
-    cudaError_t e = mask ? ensure_smem_attr(pick_tma<SegMask>(in, W)) : ensure_smem_attr(pick_tma<NoMask>(in, W));
+    const TmaKernel<NoMask> plain = t.add ? pick_tma_add(W) : pick_tma<NoMask>(in, W);
+    cudaError_t e = mask ? ensure_smem_attr(pick_tma<SegMask>(in, W)) : ensure_smem_attr(plain);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(grid));
@@ -549,7 +594,7 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     lc.attrs = attr;
     lc.numAttrs = cfg.pdl ? 1 : 0;
     e = mask ? cudaLaunchKernelEx(&lc, pick_tma<SegMask>(in, W), p, *mask)
-             : cudaLaunchKernelEx(&lc, pick_tma<NoMask>(in, W), p, NoMask{});
+             : cudaLaunchKernelEx(&lc, plain, p, NoMask{});
     if (e == cudaSuccess && launches) ++*launches;
     return e;
 }

@@ -134,6 +134,7 @@ extern "C" int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemcpyAsync(static scratch)");
 
     ddpk::SegTable t;
+    t.add = 0;   // W source streams per segment: the call's own gradients
     t.status = reinterpret_cast<int*>(base);
     t.seg_off = reinterpret_cast<const long long*>(base + b_status);
     t.seg_src = reinterpret_cast<const void* const*>(base + b_status + b_off);

@@ -271,6 +271,27 @@ class Reducer:
             self._check(self.lib.ddp_accumulate_nosync_used(self._h, a, b, self.bits(used),
                                                             1 if first_step else 0, _stream(stream)))
 
+    def bind_last_step(self, g_last=None):
+        """Fuse the synchronizing micro-step that ends a no_sync block into the
+        reductions: g_last is W lists of P fp32 tensors (or an array from
+        ``pointers``) added per replica to the bound accumulated gradients;
+        None unbinds it."""
+        if g_last is None:
+            self._check(self.lib.ddp_bind_last_step(self._h, None))
+            self._last = None
+            return
+        if not isinstance(g_last, C.Array) and getattr(self, "W", None) is not None:
+            if len(g_last) != self.W or any(len(rep) != self.P for rep in g_last):
+                raise ValueError("g_last needs W lists of P tensors")
+            for rep in g_last:
+                for v, t in enumerate(rep):
+                    if not isinstance(t, int) and t is not None:
+                        if t.numel() != self.numel[v] or not t.is_contiguous() or str(t.dtype) != "torch.float32":
+                            raise ValueError(f"last-step gradient {v}: expected {self.numel[v]} contiguous fp32")
+        arr = g_last if isinstance(g_last, C.Array) else self.pointers(g_last)
+        self._check(self.lib.ddp_bind_last_step(self._h, arr))
+        self._last = (g_last, arr)
+
     # ---------------------------------------------------------------- unused parameters
     def set_local_used(self, used):
         """used: W lists of P flags, or an array from ``bits`` (None = all used)."""

@@ -379,3 +379,46 @@ def test_hook_registration_rules(lib):
     with pytest.raises(InvalidArg):
         red.set_option(L.OPT_FIND_UNUSED, 1)
     assert lib.ddp_status_string(-8) == b"DDP_ERR_HOOK"
+
+
+def test_last_step_binding_rules(lib):
+    """ddp_bind_last_step on the host side (dry run, no device table): needs
+    a binding, fp32, no unused-parameter tracking, no hook, a complete
+    iteration; NULL entries only for zero-length variables; ddp_bind drops it."""
+    from reduction_reducer_gb300 import InvalidArg, NotBound
+    from reduction_reducer_gb300 import _lib as L
+    numel = [3, 5, 0, 7]
+    W = 2
+    fake = [[0x100000 + 0x1000 * (r * 4 + v) for v in range(4)] for r in range(W)]
+    last = [[0x800000 + 0x1000 * (r * 4 + v) for v in range(4)] for r in range(W)]
+    red = _make(numel, "f32", 16)
+    red.set_dry_run(True)
+    with pytest.raises(NotBound):
+        red.bind_last_step(last)
+    red.bind(fake, 0x10000000, None)
+    red.bind_last_step(last)
+    with pytest.raises(InvalidArg):
+        red.set_option(L.OPT_FIND_UNUSED, 1)
+    red.begin_iteration()
+    red.mark_ready(3)
+    with pytest.raises(InvalidArg):
+        red.bind_last_step(None)
+    red.abort_iteration()
+    red.bind_last_step(None)
+    red.set_option(L.OPT_FIND_UNUSED, 1)
+    with pytest.raises(InvalidArg):
+        red.bind_last_step(last)
+    red.set_option(L.OPT_FIND_UNUSED, 0)
+    holes = [row[:] for row in last]
+    holes[1][2] = 0                       # zero-length variable: no pointer needed
+    red.bind_last_step(holes)
+    holes[0][1] = 0
+    with pytest.raises(InvalidArg):
+        red.bind_last_step(holes)
+    red.bind(fake, 0x10000000, None)      # a new binding drops the last step
+    red.set_option(L.OPT_FIND_UNUSED, 1)
+    b = _make(numel, "bf16", 16)
+    b.set_dry_run(True)
+    b.bind(fake, 0x10000000, None)
+    with pytest.raises(InvalidArg):
+        b.bind_last_step(last)
