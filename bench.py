@@ -429,7 +429,8 @@ def run_ours(args):
                                  + (", stored straggler ready order" if args.layers is None and args.driver != "all"
                                     else ", reverse order" if args.driver != "all" else ""),
                        "bytes_per_step": wl.bytes,
-                       "l2": "no flush: each step streams 8.0 GB, inputs 5.4 GB > 129 MB L2",
+                       "l2": (f"no flush: each step streams {wl.bytes / 1e9:.1f} GB, inputs "
+                              f"{wl.W * wl.N * wl.s_in / 1e9:.1f} GB > 129 MB L2"),
                        "parallelism": f"replicas only x{world}"},
             "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
             "grad_elems_per_s": round(elems * world, 1),
@@ -499,13 +500,54 @@ def measure_e2e(torch, wl, stream, steps, dist, n_h2d=2, n_d2h=1):
             done.record(ds)
             stream.wait_event(done)
 
+    # per-step events: the host link is shared with the machine's other
+    # work, so the step time is reported as the median with its spread
     with torch.cuda.stream(stream):
-        ms, _, _ = time_steps(torch, stream, one, steps, 1, dist)
-    ms_step = ms / steps
-    return {"value": round(wl.bytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
+        one()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            one()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    if dist:
+        per = [max_over_ranks(t, dist, "cuda") for t in per]
+    ms_step = statistics.median(per)
+
+    # The host link itself, measured the same minute: one whole-buffer copy
+    # each way (pinned memory, best of 3).  The step cannot beat the slower
+    # direction's bytes over its rate.
+    def link(copy, nbytes):
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                copy()
+            e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1)
+            best = t if best is None else min(best, t)
+        return nbytes / (best * 1e-3) / 1e9
+    up = link(lambda: wl.flat[0].copy_(host_in[0], non_blocking=True), host_in[0].numel() * host_in[0].element_size())
+    down = link(lambda: host_out.copy_(wl.out_flat, non_blocking=True), host_out.numel() * 4)
+    bound_s = max(h2d / (up * 1e9), d2h / (down * 1e9))
+    bound = wl.bytes / bound_s / 1e9
+    value = wl.bytes / (ms_step * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "step_ms": {"median": round(ms_step, 3), "min": round(min(per), 3), "mean": round(sum(per) / steps, 3),
+                        "max": round(max(per), 3)},
             "h2d_gbs": round(h2d / (ms_step * 1e-3) / 1e9, 1),
-            "note": ("algorithmic bytes of the step / time of a step that copies the replicas' gradients "
+            "host_link": {"h2d_gbs": round(up, 1), "d2h_gbs": round(down, 1), "bound_gbs": round(bound, 1),
+                          "frac_of_bound": round(value / bound, 3),
+                          "note": "one pinned whole-buffer copy each way, best of 3, same run; bound = step "
+                                  "bytes / max(h2d bytes / h2d rate, d2h bytes / d2h rate)"},
+            "note": ("algorithmic bytes of the step / median time of a step that copies the replicas' gradients "
                      "host->device per bucket, reduces each bucket as it lands (mark_ready_many per bucket) "
                      f"and copies its averaged gradients back; pinned host buffers, {n_h2d} host->device and "
                      f"{n_d2h} device->host copy streams")}
@@ -675,15 +717,38 @@ def nosync_config(torch, device, stream, steps, warm, dist, K=8):
     def acc_only():
         red.accumulate_nosync(acc_p, fresh_p[1 % K], first_step=False, stream=stream)
 
+    # the last micro-step fused into the reduction: K - 1 accumulate launches,
+    # then one pass over (acc_r, g_r) pairs; the last step's gradient buffers
+    # are bound once, as a training loop would
+    def cycle_fused():
+        for k in range(K - 1):
+            red.accumulate_nosync(acc_p, fresh_p[k], first_step=(k == 0), stream=stream)
+        red.begin_iteration()
+        red.mark_ready_many(order_c, stream)
+
+    def last_only():
+        red.begin_iteration()
+        red.mark_ready_many(order_c, stream)
+
     with torch.cuda.stream(stream):
         ms, _, _ = time_steps(torch, stream, cycle, steps, warm, dist)
         ms_acc, _, _ = time_steps(torch, stream, acc_only, steps, warm, dist)
-    t = ms / steps
+        red.bind_last_step(fresh_p[K - 1])
+        ms_f, _, _ = time_steps(torch, stream, cycle_fused, steps, warm, dist)
+        ms_last, _, _ = time_steps(torch, stream, last_only, steps, warm, dist)
+    t, t_f = ms / steps, ms_f / steps
     cycle_bytes = 2 * W * N * 4 + (K - 1) * 3 * W * N * 4 + view_bytes(W, N, 4)
+    last_bytes = 2 * W * N * 4 + 2 * N * 4       # read acc_r and g_r, write bucket and copy-back
+    fused_bytes = 2 * W * N * 4 + (K - 2) * 3 * W * N * 4 + last_bytes
     res = {"gbs": round(cycle_bytes / (t * 1e-3) / 1e9, 1), "ms_per_cycle": round(t, 4),
            "bytes_per_cycle": cycle_bytes, "W": W, "K": K,
            "accumulate_gbs": round(3 * W * N * 4 / (ms_acc / steps * 1e-3) / 1e9, 1),
            "accumulate_ms": round(ms_acc / steps, 4),
+           "fused_last_step": {"gbs": round(fused_bytes / (t_f * 1e-3) / 1e9, 1), "ms_per_cycle": round(t_f, 4),
+                               "bytes_per_cycle": fused_bytes,
+                               "reduce_gbs": round(last_bytes / (ms_last / steps * 1e-3) / 1e9, 1),
+                               "reduce_ms": round(ms_last / steps, 4), "reduce_bytes": last_bytes,
+                               "note": "K-1 accumulate micro-steps + the K-th fused into the reduction"},
            "kernel": ("bulk copy" if red.get_option(10) == 1 else "register streaming"),
            "note": "K accumulate micro-steps (first one a copy) + one reduce (mark_ready_many)"}
     red.destroy()
@@ -699,7 +764,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--layers", type=int, default=None, help="smaller BERT (profiling case)")
     ap.add_argument("--workload", default="bert_large", choices=["bert_large", "nosync_resnet50"],
                     help="nosync_resnet50: the no_sync workload alone (profiling case)")
