@@ -651,6 +651,14 @@ def hook_config(torch, device, keep, timed, out):
     wl.free()
     del rb
     torch.cuda.empty_cache()
+    # the same hook on gradients that are views of the bucket layout: the hook
+    # reads them in place, nothing is gathered and nothing copied back
+    wl = Workload("bert_large", torch, device, 25, n_out=0, driver="hooks", layout="buckets")
+    wl.red.register_comm_hook("mean", None)
+    timed(wl, "bert_large_hook_mean_as_view", "register_comm_hook('mean', replica_buffers=None) on bucket views: "
+          "the hook's mean per bucket, W*N*4 + N*4 bytes")
+    wl.free()
+    torch.cuda.empty_cache()
 
 
 def unused_config(wl, timed, out):

@@ -226,8 +226,17 @@ typedef int (*ddp_comm_hook_fn)(void* state, const ddp_grad_bucket* bucket, void
  *   replica_buffers  host array [W] of device pointers, caller-owned, each 16-byte
  *                    aligned with room for bucket_offsets[B] elements of the
  *                    gradient dtype (bucket b of replica r lives at
- *                    replica_buffers[r] + bucket_offsets[b])
- * W <= 64; not with DDP_OPT_FIND_UNUSED.  Errors: INVALID_ARG, NOT_BOUND. */
+ *                    replica_buffers[r] + bucket_offsets[b]);
+ *                    or NULL when the bound gradients are views of the bucket
+ *                    layout ("Distributed Data Parallel" notes,
+ *                    gradient_as_bucket_view): every member v of bucket b of
+ *                    replica r at one base address + its locator offset.  Then
+ *                    nothing is gathered, the hook's replica pointers are those
+ *                    bases (the gradients themselves; NULL for a bucket without
+ *                    elements), and a launch whose bound gradients no longer
+ *                    form such views fails with INVALID_ARG.
+ * W <= 64; not with DDP_OPT_FIND_UNUSED or a bound last step.
+ * Errors: INVALID_ARG, NOT_BOUND. */
 int ddp_register_comm_hook(ddp_ctx* ctx, ddp_comm_hook_fn hook, void* state, void* const* replica_buffers);
 
 /* Built-in hooks (state unused): the default, the rank-order fp32 mean of the

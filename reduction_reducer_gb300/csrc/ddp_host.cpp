@@ -65,7 +65,8 @@ struct ddp_ctx {
     // ---- communication hook
     ddp_comm_hook_fn hook = nullptr;
     void* hook_state = nullptr;
-    std::vector<void*> hook_rb;                   // W replica bucket buffers
+    std::vector<void*> hook_rb;                   // W replica bucket buffers (empty: gradients are bucket views)
+    bool hook_alias = false;                      // the hook reads the gradients in place
 
     // ---- binding
     bool bound = false;
@@ -255,6 +256,24 @@ int check_device(ddp_ctx* c) {
 
 // The hook path for buckets [b0, b1): per bucket, gather into the replica
 // buffers, the hook, copy-back.
+// Gradient as bucket view: replica r's gradients of bucket b lie at one base
+// address plus each member's offset.  Fills base[r] (nullptr for a bucket
+// without elements) and returns false when some member lies elsewhere.
+bool bucket_view_bases(const ddp_ctx* c, int32_t b, const void** base) {
+    for (int r = 0; r < c->W; ++r) {
+        const char* b0 = nullptr;
+        for (int32_t v : c->members[b]) {
+            if (c->numel[v] == 0) continue;
+            const char* g = static_cast<const char*>(c->bind_grads[static_cast<int64_t>(r) * c->P + v]);
+            const char* at = g - c->loc[v].offset * c->elem;
+            if (!b0) b0 = at;
+            else if (at != b0) return false;
+        }
+        base[r] = b0;
+    }
+    return true;
+}
+
 int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& cfg, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::vector<const void*> reps(c->W);
@@ -263,10 +282,19 @@ int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& cfg, v
         const long long lo = c->bucket_off[b], hi = c->bucket_off[b + 1];
         const int s0 = c->bucket_seg[b], s1 = c->bucket_seg[b + 1];
         long long n = 0;
-        cudaError_t e = ddpk::launch_seg_copy(c->tab, 0, c->elem, c->W, c->n_out, c->arena, c->hook_rb.data(), lo, hi,
-                                              s0, s1, cfg, st, &n);
-        c->launches += n;
-        if (e != cudaSuccess) return cuda_fail(c, e, "hook gather launch");
+        if (c->hook_alias) {
+            // the replicas' buckets are their gradients: nothing to gather
+            if (!bucket_view_bases(c, b, reps.data()))
+                return fail(c, DDP_ERR_INVALID_ARG, "bucket " + std::to_string(b) +
+                                                        ": the bound gradients are not views of the bucket layout");
+        } else {
+            cudaError_t e = ddpk::launch_seg_copy(c->tab, 0, c->elem, c->W, c->n_out, c->arena, c->hook_rb.data(), lo,
+                                                  hi, s0, s1, cfg, st, &n);
+            c->launches += n;
+            if (e != cudaSuccess) return cuda_fail(c, e, "hook gather launch");
+            for (int r = 0; r < c->W; ++r)
+                reps[r] = static_cast<const char*>(c->hook_rb[r]) + lo * c->elem;
+        }
         const auto& vs = c->members[b];
         offs.resize(vs.size());
         lens.resize(vs.size());
@@ -274,8 +302,6 @@ int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& cfg, v
             offs[i] = c->loc[vs[i]].offset;
             lens[i] = c->loc[vs[i]].length;
         }
-        for (int r = 0; r < c->W; ++r)
-            reps[r] = static_cast<const char*>(c->hook_rb[r]) + lo * c->elem;
         ddp_grad_bucket gb;
         gb.index = b;
         gb.num_buckets = c->B;
@@ -293,7 +319,8 @@ int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& cfg, v
         if (hr != 0) return fail(c, DDP_ERR_HOOK, "communication hook returned " + std::to_string(hr) + " for bucket " +
                                                       std::to_string(b));
         n = 0;
-        e = ddpk::launch_seg_copy(c->tab, 1, 4, c->W, c->n_out, c->arena, nullptr, lo, hi, s0, s1, cfg, st, &n);
+        const cudaError_t e =
+            ddpk::launch_seg_copy(c->tab, 1, 4, c->W, c->n_out, c->arena, nullptr, lo, hi, s0, s1, cfg, st, &n);
         c->launches += n;
         if (e != cudaSuccess) return cuda_fail(c, e, "hook copy-back launch");
     }
@@ -656,16 +683,28 @@ int ddp_register_comm_hook(ddp_ctx* c, ddp_comm_hook_fn hook, void* state, void*
     if (c->W > ddpk::kMaxHookReplicas) return fail(c, DDP_ERR_INVALID_ARG, "hooks support W <= 64");
     if (c->opt_find_unused) return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with DDP_OPT_FIND_UNUSED");
     if (!c->bind_last.empty()) return fail(c, DDP_ERR_INVALID_ARG, "hooks do not combine with a bound last step");
-    if (c->bucket_off[c->B] > 0 && !replica_buffers) return fail(c, DDP_ERR_INVALID_ARG, "replica_buffers is NULL");
-    std::vector<void*> rb(c->W, nullptr);
-    for (int r = 0; r < c->W && c->bucket_off[c->B] > 0; ++r) {
-        if (!replica_buffers[r] || !is_aligned16(reinterpret_cast<uintptr_t>(replica_buffers[r])))
-            return fail(c, DDP_ERR_INVALID_ARG, "replica buffer " + std::to_string(r) + " is NULL or not 16-byte aligned");
-        rb[r] = replica_buffers[r];
+    const bool alias = !replica_buffers;
+    std::vector<void*> rb;
+    if (alias) {
+        // the gradients must already be views of the bucket layout
+        std::vector<const void*> base(c->W);
+        for (int32_t b = 0; b < c->B; ++b)
+            if (!bucket_view_bases(c, b, base.data()))
+                return fail(c, DDP_ERR_INVALID_ARG, "replica_buffers is NULL but bucket " + std::to_string(b) +
+                                                        " is not laid out as a view of the bound gradients");
+    } else {
+        rb.assign(c->W, nullptr);
+        for (int r = 0; r < c->W && c->bucket_off[c->B] > 0; ++r) {
+            if (!replica_buffers[r] || !is_aligned16(reinterpret_cast<uintptr_t>(replica_buffers[r])))
+                return fail(c, DDP_ERR_INVALID_ARG,
+                            "replica buffer " + std::to_string(r) + " is NULL or not 16-byte aligned");
+            rb[r] = replica_buffers[r];
+        }
     }
     c->hook = hook;
     c->hook_state = state;
     c->hook_rb = std::move(rb);
+    c->hook_alias = alias;
     return DDP_OK;
 }
 

@@ -376,33 +376,72 @@ __device__ __forceinline__ float flat_term(const FlatMeanParams& p, int r, long 
 }
 
 // vec != 0: every pointer 16-byte aligned; 16-byte loads over whole vectors,
-// the tail element by element.
-template <typename Tin>
+// the tail element by element.  WC > 0: W known at compile time, W x U
+// loads in flight per thread before the first add (as in the fused pass).
+template <typename Tin, int WC>
 __global__ void __launch_bounds__(kMaxBlock) flat_mean_kernel(const __grid_constant__ FlatMeanParams p, int vec) {
     pdl_enter(0);
     using V = Vec<Tin>;
+    using Raw = typename V::Raw;
     constexpr int N = V::N;
+    constexpr int U = WC == 0 ? 1 : unroll_for<WC>();
+    const int W = WC > 0 ? WC : p.W;
     const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long t0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long nv = vec ? p.n / N : 0;
-    for (long long k = t0; k < nv; k += step) {
-        float acc[N], f[N];
-        V::unpack(ld_stream(reinterpret_cast<const typename V::Raw*>(static_cast<const Tin*>(p.src[0]) + k * N)), acc);
-        if (p.compress)
-            for (int q = 0; q < N; ++q) acc[q] = round_bf16(acc[q]);
-        for (int r = 1; r < p.W; ++r) {
-            V::unpack(ld_stream(reinterpret_cast<const typename V::Raw*>(static_cast<const Tin*>(p.src[r]) + k * N)), f);
+    auto term = [&](float x) { return p.compress ? round_bf16(x) : x; };
+    if constexpr (WC > 0) {
+        for (long long k = t0; k < nv; k += U * step) {
+            Raw raw[U][WC];
 #pragma unroll
-            for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], p.compress ? round_bf16(f[q]) : f[q]);
+            for (int u = 0; u < U; ++u)
+                if (k + u * step < nv)
+#pragma unroll
+                    for (int r = 0; r < WC; ++r)
+                        raw[u][r] = ld_stream(reinterpret_cast<const Raw*>(static_cast<const Tin*>(p.src[r]) +
+                                                                           (k + u * step) * N));
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const long long kk = k + u * step;
+                if (kk < nv) {
+                    float acc[N], f[N];
+                    V::unpack(raw[u][0], acc);
+#pragma unroll
+                    for (int q = 0; q < N; ++q) acc[q] = term(acc[q]);
+#pragma unroll
+                    for (int r = 1; r < WC; ++r) {
+                        V::unpack(raw[u][r], f);
+#pragma unroll
+                        for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], term(f[q]));
+                    }
+#pragma unroll
+                    for (int q = 0; q < N; q += 4)
+                        st_stream(p.out + kk * N + q,
+                                  make_float4(__fmul_rn(acc[q], p.inv_w), __fmul_rn(acc[q + 1], p.inv_w),
+                                              __fmul_rn(acc[q + 2], p.inv_w), __fmul_rn(acc[q + 3], p.inv_w)));
+                }
+            }
         }
+    } else {
+        for (long long k = t0; k < nv; k += step) {
+            float acc[N], f[N];
+            V::unpack(ld_stream(reinterpret_cast<const Raw*>(static_cast<const Tin*>(p.src[0]) + k * N)), acc);
 #pragma unroll
-        for (int q = 0; q < N; q += 4)
-            st_stream(p.out + k * N + q, make_float4(__fmul_rn(acc[q], p.inv_w), __fmul_rn(acc[q + 1], p.inv_w),
-                                                     __fmul_rn(acc[q + 2], p.inv_w), __fmul_rn(acc[q + 3], p.inv_w)));
+            for (int q = 0; q < N; ++q) acc[q] = term(acc[q]);
+            for (int r = 1; r < W; ++r) {
+                V::unpack(ld_stream(reinterpret_cast<const Raw*>(static_cast<const Tin*>(p.src[r]) + k * N)), f);
+#pragma unroll
+                for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], term(f[q]));
+            }
+#pragma unroll
+            for (int q = 0; q < N; q += 4)
+                st_stream(p.out + k * N + q, make_float4(__fmul_rn(acc[q], p.inv_w), __fmul_rn(acc[q + 1], p.inv_w),
+                                                         __fmul_rn(acc[q + 2], p.inv_w), __fmul_rn(acc[q + 3], p.inv_w)));
+        }
     }
     for (long long i = nv * N + t0; i < p.n; i += step) {
         float acc = flat_term<Tin>(p, 0, i);
-        for (int r = 1; r < p.W; ++r) acc = __fadd_rn(acc, flat_term<Tin>(p, r, i));
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, flat_term<Tin>(p, r, i));
         p.out[i] = __fmul_rn(acc, p.inv_w);
     }
 }
@@ -569,12 +608,26 @@ cudaError_t launch_flat_mean(InType in, int W, const void* const* src, float* ou
         vec = vec && (reinterpret_cast<uintptr_t>(src[r]) & 15u) == 0;
     }
     const int N = in == IN_F32 ? 4 : 8;
+    using K = void (*)(FlatMeanParams, int);
+    auto pick = [&](auto tag) -> K {
+        using T = decltype(tag);
+        switch (W) {
+            case 2: return flat_mean_kernel<T, 2>;
+            case 4: return flat_mean_kernel<T, 4>;
+            case 8: return flat_mean_kernel<T, 8>;
+            case 16: return flat_mean_kernel<T, 16>;
+            default: return flat_mean_kernel<T, 0>;
+        }
+    };
+    const K k = in == IN_F32 ? pick(float{}) : pick(uint16_t{});
+    // one resident wave: the grid-stride loop covers the rest
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
     long long grid = ceil_div(vec ? ceil_div(n, N) : n, 256);
-    const long long cap = static_cast<long long>(sms > 0 ? sms : 152) * 8;
+    const long long cap = static_cast<long long>(sms > 0 ? sms : 152) * per_sm;
     grid = grid < cap ? grid : cap;
     if (grid < 1) grid = 1;
-    return in == IN_F32 ? launch(flat_mean_kernel<float>, static_cast<int>(grid), 256, true, stream, p, vec)
-                        : launch(flat_mean_kernel<uint16_t>, static_cast<int>(grid), 256, true, stream, p, vec);
+    return launch(k, static_cast<int>(grid), 256, true, stream, p, vec);
 }
 
 cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,

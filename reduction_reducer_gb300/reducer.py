@@ -182,12 +182,13 @@ class Reducer:
         return nxt.value, [parked[i] for i in range(n.value)]
 
     # ---------------------------------------------------------------- communication hooks
-    def register_comm_hook(self, hook, replica_buffers, state=None):
+    def register_comm_hook(self, hook, replica_buffers=None, state=None):
         """hook: "mean" | "bf16_compress" (built-in) or a callable
         ``hook(bucket: _lib.GradBucket, stream: int) -> int|None`` that enqueues
         its reduction into ``bucket.result`` on ``stream``; replica_buffers: W
         device buffers (tensors or addresses) of ``arena_numel()`` elements of
-        the gradient dtype."""
+        the gradient dtype, or None when the bound gradients are views of the
+        bucket layout (the hook then reads them in place)."""
         if hook == "mean":
             fn = C.cast(self.lib.ddp_hook_mean, _lib.HOOKFN)
         elif hook == "bf16_compress":
@@ -202,7 +203,7 @@ class Reducer:
                 except Exception:       # noqa: BLE001 -- a Python error must not cross the C ABI
                     return 1
             fn = _lib.HOOKFN(trampoline)
-        rb = _ptr_array([_ptr(t) for t in replica_buffers])
+        rb = None if replica_buffers is None else _ptr_array([_ptr(t) for t in replica_buffers])
         self._check(self.lib.ddp_register_comm_hook(self._h, fn, state, rb))
         self._hook_keep = (fn, rb, replica_buffers, hook)
 

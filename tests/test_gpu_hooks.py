@@ -137,3 +137,78 @@ def test_hook_failure_and_registration_rules():
     torch.cuda.synchronize()
     with pytest.raises(InvalidArg):
         red2.register_comm_hook("mean", rb2)            # after the first launch
+
+
+@pytest.mark.parametrize("hook", ["mean", "bf16_compress"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W,n_out", [(1, 0), (4, 0), (4, 1), (3, 3)])
+def test_hooks_on_bucket_views(hook, dtype, W, n_out):
+    """Gradients laid out as views of the bucket layout, no replica buffers:
+    nothing is gathered, the hook reads the gradients in place, and the
+    result matches the oracle bit for bit."""
+    numel = RAGGED
+    cap = 16 * 1024
+    red = Reducer(numel, dtype, cap)
+    _, boff = red.get_bucket_info()
+    locs = red.get_locators()
+    offs = [boff[b] + off for (b, _, off, _) in locs]
+    total = boff[-1]
+    flats, views, _ = host_grads(numel, W, dtype)
+    # re-pack every replica's gradients in bucket order
+    packed = []
+    for r in range(W):
+        f = np.zeros(total, dtype=flats[r].dtype)
+        for v, n in enumerate(numel):
+            f[offs[v]:offs[v] + n] = views[r][v].view(flats[r].dtype)
+        packed.append(f)
+    flat_dev, grads_dev = host_to_device_views(packed, numel, offs, dtype, DEV)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    outs = [[torch.full((n,), float("nan"), device=DEV) for n in numel] for _ in range(max(n_out, 1))]
+    red.bind(grads_dev, arena, None if n_out == 0 else (outs[0] if n_out == 1 else outs))
+    seen = []
+    lib = _lib.load()
+    builtin = lib.ddp_hook_mean if hook == "mean" else lib.ddp_hook_bf16_compress
+
+    def spy(bucket, stream):
+        seen.append([bucket.replicas[r] for r in range(bucket.W)])
+        return builtin(None, bucket, stream)
+
+    red.register_comm_hook(spy, None)
+    members, olocs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+    fn = hook_mean if hook == "mean" else hook_bf16_compress
+    want_arena, want_outs, _ = reduce_with_hook(views, members, olocs, numel, fn, n_out=max(n_out, 1))
+    launches0 = red.launch_count()
+    red.begin_iteration()
+    red.mark_ready_many(gen.straggler_order(members, p=0.5, seed=2))
+    torch.cuda.synchronize()
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    for o in range(n_out):
+        for v in range(len(numel)):
+            assert bits_equal(outs[o][v].cpu().numpy(), want_outs[0][v]), (o, v)
+    esz = 4 if dtype == "f32" else 2
+    for b, ptrs in enumerate(seen):            # the hook saw the gradients themselves
+        for r in range(W):
+            assert ptrs[r] == flat_dev[r].data_ptr() + boff[b] * esz or boff[b + 1] == boff[b]
+    # copy-back launches only (one per bucket with outputs), no gather
+    assert red.launch_count() - launches0 == (len(members) if n_out else 0)
+
+
+def test_hook_on_bucket_views_detects_a_broken_layout():
+    numel = [100, 200, 300]
+    W = 2
+    red = Reducer(numel, "f32", 1 << 20)          # one bucket: push order 2, 1, 0
+    _, boff = red.get_bucket_info()
+    locs = red.get_locators()
+    flat = [torch.zeros(boff[-1], device=DEV) for _ in range(W)]
+    views = [[f[boff[b] + off:boff[b] + off + n] for (b, _, off, n) in locs] for f in flat]
+    arena = torch.empty(red.arena_numel(), device=DEV)
+    red.bind(views, arena, None)
+    red.register_comm_hook("mean", None)
+    # rebinding in registration order breaks the view layout: the launch fails
+    other = [torch.zeros(sum(numel), device=DEV) for _ in range(W)]
+    offs = [0, 100, 300]
+    red.bind([[f[o:o + n] for o, n in zip(offs, numel)] for f in other], arena, None)
+    red.begin_iteration()
+    with pytest.raises(InvalidArg):
+        red.mark_ready_many([2, 1, 0])

@@ -422,3 +422,21 @@ def test_last_step_binding_rules(lib):
     b.bind(fake, 0x10000000, None)
     with pytest.raises(InvalidArg):
         b.bind_last_step(last)
+
+
+def test_hook_on_bucket_views_rules(lib):
+    """replica_buffers = NULL needs the bound gradients to be views of the
+    bucket layout (dry run: addresses only)."""
+    from reduction_reducer_gb300 import InvalidArg
+    red = _make([4, 4, 4], "f32", 48)           # one bucket, push order v2, v1, v0
+    red.set_dry_run(True)
+    assert red.get_members() == [[2, 1, 0]]
+    red.bind([[0x1000, 0x1010, 0x1020], [0x2000, 0x2010, 0x2020]], 0x10000000, None)   # registration order
+    with pytest.raises(InvalidArg):
+        red.register_comm_hook("mean", None)
+    red.bind([[0x1020, 0x1010, 0x1000], [0x2020, 0x2010, 0x2000]], 0x10000000, None)   # bucket order
+    red.register_comm_hook("mean", None)
+    z = _make([0, 4, 0], "f32", 48)               # zero-length members need no address
+    z.set_dry_run(True)
+    z.bind([[0, 0x1000, 0]], 0x10000000, None)
+    z.register_comm_hook("mean", None)
