@@ -313,9 +313,17 @@ __device__ __forceinline__ void copy_run(const char* from, char* to, long long a
     const long long sc_end = vec && kb < ke ? kb * n : e;
     for (long long a = x + threadIdx.x; a < sc_end; a += blockDim.x)
         copy_elem(to + (a - a0) * elem, from + (a - a0) * elem, elem);
-    for (long long k = kb + threadIdx.x; k < ke; k += blockDim.x) {
-        const long long j = (k * n - a0) * elem;
-        st_stream(reinterpret_cast<float*>(to + j), __ldcs(reinterpret_cast<const float4*>(from + j)));
+    // four independent 16-byte vectors per thread in flight
+    constexpr int UC = 4;
+    const long long step = blockDim.x;
+    for (long long k = kb + threadIdx.x; k < ke; k += UC * step) {
+        float4 v[UC];
+#pragma unroll
+        for (int u = 0; u < UC; ++u)
+            if (k + u * step < ke) v[u] = __ldcs(reinterpret_cast<const float4*>(from + ((k + u * step) * n - a0) * elem));
+#pragma unroll
+        for (int u = 0; u < UC; ++u)
+            if (k + u * step < ke) st_stream(reinterpret_cast<float*>(to + ((k + u * step) * n - a0) * elem), v[u]);
     }
     if (vec && kb < ke)
         for (long long a = ke * n + threadIdx.x; a < e; a += blockDim.x)
