@@ -62,7 +62,7 @@ def _fields(numel, W, odd=False):
 
 @pytest.mark.parametrize("mode", ["mark_ready", "mark_ready_many", "reduce_all", "reduce_bucket"])
 @pytest.mark.parametrize("kernel", ["ldg", "tma"])
-@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 16, 32])
 def test_last_step_every_element(W, kernel, mode):
     numel = RAGGED
     K, cap = 3, 16 * 1024
