@@ -337,7 +337,7 @@ def run_nosync_only(args):
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
     stream = torch.cuda.Stream(device=device)
-    res = nosync_config(torch, device, stream, args.steps, args.warmup, None, K=args.nosync_k)
+    res = nosync_config(torch, device, stream, args.steps, args.warmup, None, K=args.nosync_k, kernel=args.kernel)
     print(json.dumps({"workload": f"nosync_resnet50_w16_k{args.nosync_k}", **res}), flush=True)
     return 0
 
@@ -365,6 +365,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=device)
 
     wl = Workload("bert_large", torch, device, 25, n_out=1, driver=args.driver, layers=args.layers)
+    hook_bufs = profiling_setup(torch, device, wl.red, args, wl.W)
     with torch.cuda.stream(stream):
         l0 = wl.red.launch_count()
         ms, t0, t1 = time_steps(torch, stream, lambda: wl.step(stream), args.steps, args.warmup, dist)
@@ -431,7 +432,9 @@ def run_ours(args):
                        "bytes_per_step": wl.bytes,
                        "l2": (f"no flush: each step streams {wl.bytes / 1e9:.1f} GB, inputs "
                               f"{wl.W * wl.N * wl.s_in / 1e9:.1f} GB > 129 MB L2"),
-                       "parallelism": f"replicas only x{world}"},
+                       "parallelism": f"replicas only x{world}",
+                       **({"profiling": {"kernel": args.kernel, "hook": args.hook}}
+                          if args.kernel != "auto" or args.hook != "none" else {})},
             "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
             "grad_elems_per_s": round(elems * world, 1),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": timed_launches * world,
@@ -696,8 +699,26 @@ def unused_config(wl, timed, out):
     wl.red.set_option(_lib.OPT_FIND_UNUSED, 0)
 
 
-def nosync_config(torch, device, stream, steps, warm, dist, K=8):
-    from reduction_reducer_gb300 import Reducer
+KERNEL_FLAG = {"auto": 2, "ldg": 0, "tma": 1}
+
+
+def profiling_setup(torch, device, red, args, W):
+    """Profiling cases only: force a kernel (--kernel) and route the buckets
+    through a built-in hook (--hook).  Returns the replica buffers it
+    allocated (kept alive by the caller)."""
+    from reduction_reducer_gb300 import _lib
+    if getattr(args, "kernel", "auto") != "auto":
+        red.set_option(_lib.OPT_KERNEL, KERNEL_FLAG[args.kernel])
+    if getattr(args, "hook", "none") == "none":
+        return None
+    tdt = torch.float32 if red.dtype == "f32" else torch.bfloat16
+    bufs = [torch.empty(max(red.arena_numel(), 1), dtype=tdt, device=device) for _ in range(W)]
+    red.register_comm_hook(args.hook, bufs)
+    return bufs
+
+
+def nosync_config(torch, device, stream, steps, warm, dist, K=8, kernel="auto"):
+    from reduction_reducer_gb300 import Reducer, _lib
     numel = shapes.numels(shapes.resnet50())
     W = 16
     N = sum(numel)
@@ -707,6 +728,8 @@ def nosync_config(torch, device, stream, steps, warm, dist, K=8):
     acc_flat = [torch.empty(total, device=device) for _ in range(W)]
     acc = [[f[o:o + n] for o, n in zip(offs, numel)] for f in acc_flat]
     red = Reducer(numel, "f32", 25 * MIB)
+    if kernel != "auto":
+        red.set_option(_lib.OPT_KERNEL, KERNEL_FLAG[kernel])
     arena = torch.empty(red.arena_numel(), device=device)
     out_flat = torch.empty(total, device=device)
     red.bind(acc, arena, [out_flat[o:o + n] for o, n in zip(offs, numel)])
@@ -778,6 +801,10 @@ def main():
                     help="nosync_resnet50: the no_sync workload alone (profiling case)")
     ap.add_argument("--nosync-k", type=int, default=8, help="micro-steps of --workload nosync_resnet50")
     ap.add_argument("--driver", default="hooks", choices=["hooks", "events", "all"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "tma"],
+                    help="profiling cases: force the bucket-reduce/accumulate kernel")
+    ap.add_argument("--hook", default="none", choices=["none", "mean", "bf16_compress"],
+                    help="profiling cases: reduce the main workload through a built-in hook")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     args = ap.parse_args()

@@ -590,7 +590,12 @@ cudaError_t launch_seg_copy(const SegTable& t, int mode, int elem, int W, int n_
     for (int r = 0; r < W && mode == 0; ++r) p.rb[r] = rb[r];
     const long long span = hi - p.base;
     const long long min_piece = static_cast<long long>(cfg.block) * n * 2;
-    long long grid = static_cast<long long>(cfg.sms) * 4;
+    // one resident wave of CTAs (a second, partial wave would only add a tail)
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, seg_copy_kernel, cfg.block, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    long long grid = static_cast<long long>(cfg.sms) * per_sm;
     grid = grid < ceil_div(span, min_piece) ? grid : ceil_div(span, min_piece);
     if (grid < 1) grid = 1;
     p.piece = ceil_div(ceil_div(span, grid), n) * n;
