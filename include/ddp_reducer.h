@@ -369,6 +369,25 @@ int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);
  * (the results of that launch are not to be trusted). */
 int ddp_get_device_status(ddp_ctx* ctx, int32_t* status);
 
+/* Read and clear the bounds-check record of a bound context (synchronous).
+ * Only a library built with -DDDP_DEBUG (libddpreducer_debug.so) checks, in
+ * every kernel, that each range it walks lies inside its segment, launch and
+ * stage and that every bulk copy is 16-byte aligned and sized; the first
+ * failed check stores its code (101 segment range, 102 staged chunk range,
+ * 103 bulk-copy alignment, 104 accumulate pair range) and the element index
+ * there and the access is skipped.  A release build never writes the record:
+ * *code = 0.  The pages have no counterpart (a stand-in for a sanitizer run).
+ * Errors: INVALID_ARG, NOT_BOUND, CUDA. */
+int ddp_get_debug_record(ddp_ctx* ctx, int32_t* code, int64_t* index);
+
+/* Self-test of the kernels' bounded waits on the current device: one CTA
+ * waits on an mbarrier that nothing completes, for at most limit_cycles SM
+ * clock cycles (1 .. 4e9); the wait gives up, writes its timeout code into a
+ * status word, and the kernel returns.  *code receives that word (3 when the
+ * wait ended as designed).  Synchronous; allocates and frees 4 bytes.  The
+ * pages have no counterpart.  Errors: INVALID_ARG (limit out of range), CUDA. */
+int ddp_selftest_bounded_wait(int64_t limit_cycles, int32_t* code);
+
 /* Kernel launches issued by this context since creation. */
 int ddp_get_launch_count(const ddp_ctx* ctx, int64_t* launches);
 

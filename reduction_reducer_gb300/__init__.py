@@ -6,5 +6,5 @@ C++ host core + hand-written sm_103a CUDA kernels behind the C ABI of
 """
 
 from .reducer import (AlreadyReady, CudaError, DDPError, HookError, InvalidArg, NoMemory,  # noqa: F401
-                      NotBound, OutOfOrder, PriorReductionUnfinished, Reducer)
+                      NotBound, OutOfOrder, PriorReductionUnfinished, Reducer, selftest_bounded_wait)
 from ._lib import LIB_PATH, load  # noqa: F401

@@ -75,6 +75,8 @@ SIGNATURES = {
     "ddp_get_option": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64)]),
     "ddp_get_launch_count": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64)]),
     "ddp_get_device_status": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32)]),
+    "ddp_get_debug_record": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int64)]),
+    "ddp_selftest_bounded_wait": (C.c_int, [C.c_int64, C.POINTER(C.c_int32)]),
     "ddp_reduce_all_noalloc": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.c_void_p,
                                          C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
     "ddp_status_string": (C.c_char_p, [C.c_int]),
@@ -85,11 +87,24 @@ SIGNATURES = {
 _lib = None
 
 
+DEBUG_LIB_PATH = os.path.join(PKG, "libddpreducer_debug.so")
+_variants = {}
+
+
 def load(path: str = LIB_PATH):
-    """Load (once) and declare the library; raises if it is missing."""
+    """Load (once per path) and declare the library; raises if it is missing.
+    ``DEBUG_LIB_PATH`` is the bounds-checking build of the same sources."""
     global _lib
-    if _lib is not None:
-        return _lib
+    if path != LIB_PATH:
+        if path not in _variants:
+            _variants[path] = _open(path)
+        return _variants[path]
+    if _lib is None:
+        _lib = _open(path)
+    return _lib
+
+
+def _open(path: str):
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build it first with "
@@ -100,5 +115,4 @@ def load(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
     return lib

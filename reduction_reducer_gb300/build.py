@@ -1,6 +1,6 @@
 """Build the C-ABI library ``libddpreducer.so`` in-tree with nvcc for sm_103a.
 
-    python -m reduction_reducer_gb300.build [-v]
+    python -m reduction_reducer_gb300.build [-v] [--all]
 
 Translation units are compiled in parallel into ``_build/`` next to this
 file and linked (static CUDA runtime) into ``libddpreducer.so`` beside the
@@ -21,6 +21,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libddpreducer.so")
+# Bounds-checking variant of the same sources (-DDDP_DEBUG): every kernel
+# checks the ranges it walks and the bulk copies it issues, and records the
+# first failure instead of touching memory out of range.
+DEBUG_BUILD = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libddpreducer_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Size of the static device scratch of ddp_reduce_all_noalloc (256 KiB).
@@ -68,5 +73,18 @@ def build(verbose: bool = False, extra_flags=(), lib_path: str = LIB, build_dir:
     return lib_path
 
 
+def build_debug(verbose: bool = False) -> str:
+    """The bounds-checking variant at ``DEBUG_LIB``."""
+    return build(verbose, extra_flags=("-DDDP_DEBUG=1",), lib_path=DEBUG_LIB, build_dir=DEBUG_BUILD)
+
+
+def build_all(verbose: bool = False):
+    """Release and bounds-checking builds, compiled side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        rel = ex.submit(build, verbose)
+        dbg = ex.submit(build_debug, verbose)
+        return rel.result(), dbg.result()
+
+
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build_all(verbose="-v" in sys.argv) if "--all" in sys.argv else build(verbose="-v" in sys.argv))

@@ -45,6 +45,41 @@ __device__ __forceinline__ void st_stream(float* p, float4 v) {
     __stcs(reinterpret_cast<float4*>(p), v);
 }
 
+// ------------------------------------------------------------------ debug checks
+
+// Debug builds (-DDDP_DEBUG) check every range a kernel walks and every bulk
+// copy it issues.  The first failed check records its code in word 1 of the
+// binding's 16-byte status block and the offending element index in words
+// 2..3, and the access is skipped (no trap: the context stays usable).
+// Release builds compile the checks away.
+enum DebugCode {
+    kDbgSegRange = 101,    // a segment range outside its segment or the launch
+    kDbgChunkRange = 102,  // a staged chunk outside its segment, slice or stage
+    kDbgCopyAlign = 103,   // a bulk copy not 16-byte aligned or sized
+    kDbgPairRange = 104,   // an accumulate range outside its pair
+};
+
+#ifdef DDP_DEBUG
+constexpr bool kDebug = true;
+static __device__ __noinline__ void debug_record(int* status, int code, long long index) {
+    if (status && atomicCAS(status + 1, 0, code) == 0)
+        atomicExch(reinterpret_cast<unsigned long long*>(status + 2), static_cast<unsigned long long>(index));
+}
+#else
+constexpr bool kDebug = false;
+__device__ __forceinline__ void debug_record(int*, int, long long) {}
+#endif
+
+// `ok`, recording a failure in debug builds; always true in release builds.
+__device__ __forceinline__ bool debug_ok(int* status, bool ok, int code, long long index) {
+    if constexpr (kDebug) {
+        if (!ok) debug_record(status, code, index);
+        return ok;
+    } else {
+        return true;
+    }
+}
+
 // ------------------------------------------------------------------ element types
 
 // bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
@@ -218,7 +253,7 @@ struct AccParams {
     int chain;         // 1: follows this call's previous accumulate launch
     int stages;        // bulk-copy variant: ring depth
     int tile;          // bulk-copy variant: elements per operand per stage (multiple of 4)
-    int* status;       // bulk-copy variant: device status word
+    int* status;       // device status block (bulk-copy waits, debug checks)
     AccPairDev pair[kMaxAccPairs];
 };
 

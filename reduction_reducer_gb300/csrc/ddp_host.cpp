@@ -1025,6 +1025,45 @@ int ddp_get_device_status(ddp_ctx* c, int32_t* status) {
     return DDP_OK;
 }
 
+int ddp_get_debug_record(ddp_ctx* c, int32_t* code, int64_t* index) {
+    if (!c || !code || !index) return DDP_ERR_INVALID_ARG;
+    *code = 0;
+    *index = 0;
+    if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "debug record before bind");
+    if (c->dry) return DDP_OK;
+    int32_t words[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaMemcpy(words, c->tab.status, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "read debug record");
+    if (words[1] != 0) {
+        const int32_t zero[3] = {0, 0, 0};
+        e = cudaMemcpy(c->tab.status + 1, zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(c, e, "clear debug record");
+    }
+    *code = words[1];
+    int64_t idx = 0;
+    std::memcpy(&idx, &words[2], sizeof(idx));
+    *index = idx;
+    return DDP_OK;
+}
+
+int ddp_selftest_bounded_wait(int64_t limit_cycles, int32_t* code) {
+    if (!code) return DDP_ERR_INVALID_ARG;
+    *code = 0;
+    if (limit_cycles <= 0 || limit_cycles > 4000000000LL) return DDP_ERR_INVALID_ARG;
+    int* d = nullptr;
+    cudaError_t e = cudaMalloc(&d, sizeof(int));
+    if (e != cudaSuccess) return DDP_ERR_CUDA;
+    e = cudaMemset(d, 0, sizeof(int));
+    if (e == cudaSuccess) e = ddpk::launch_wait_selftest(limit_cycles, d, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int32_t v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, d, sizeof(v), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    if (e != cudaSuccess) return DDP_ERR_CUDA;
+    *code = v;
+    return DDP_OK;
+}
+
 int ddp_get_option(const ddp_ctx* c, int32_t option, int64_t* value) {
     if (!c || !value) return DDP_ERR_INVALID_ARG;
     switch (option) {

@@ -196,6 +196,8 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_consta
         const long long a0 = __ldg(p.seg_off + s);
         const long long a1 = __ldg(p.seg_off + s + 1);
         const long long e = a1 < y ? a1 : y;
+        if (!debug_ok(p.status, s < p.s1 && a0 <= x && x < e && e <= a1 && p.lo <= x && e <= p.hi, kDbgSegRange, x))
+            break;
         const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(s) * NS;
         float* const* dst = p.seg_dst + static_cast<long long>(s) * p.n_out;
         const unsigned long long mk = seg_mask(mask, s - p.s0);
@@ -236,6 +238,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
         const long long end = q.off + q.len;
         const long long e = end < y ? end : y;
         if (x < e) {
+            if (!debug_ok(p.status, q.off <= x && e <= p.total, kDbgPairRange, x)) break;
             const bool assign = q.assign != 0;
             const float* g = q.g - q.off;      // indexed by flat position
             float* acc = q.acc - q.off;
@@ -289,6 +292,7 @@ struct CopyParams {
     float* const* seg_dst;
     const int* seg_vec;
     const float* arena;
+    int* status;
     long long base, lo, hi, piece;
     int s0, s1;
     int W, n_out;
@@ -342,6 +346,8 @@ __global__ void __launch_bounds__(kMaxBlock) seg_copy_kernel(const __grid_consta
         const long long a0 = __ldg(p.seg_off + s);
         const long long a1 = __ldg(p.seg_off + s + 1);
         const long long e = a1 < y ? a1 : y;
+        if (!debug_ok(p.status, s < p.s1 && a0 <= x && x < e && e <= a1 && p.lo <= x && e <= p.hi, kDbgSegRange, x))
+            break;
         const bool vec = __ldg(p.seg_vec + s) != 0;
         if (p.mode == 0) {
             for (int r = 0; r < p.W; ++r) {
@@ -577,6 +583,7 @@ cudaError_t launch_seg_copy(const SegTable& t, int mode, int elem, int W, int n_
     p.seg_dst = t.seg_dst;
     p.seg_vec = t.seg_vec;
     p.arena = arena;
+    p.status = t.status;
     p.lo = lo;
     p.hi = hi;
     const int n = 16 / (mode == 0 ? elem : 4);
@@ -654,6 +661,7 @@ cudaError_t launch_accumulate(const AccPair* pairs, int n, const LaunchCfg& cfg,
         // launches after the first of this call directly follow it on the
         // stream and touch other pairs: no need to wait for it on entry
         p.chain = cfg.pdl && issued > 0 ? 1 : 0;
+        p.status = cfg.status;
         long long off = 0;
         while (i < n && p.npairs < kMaxAccPairs) {
             if (pairs[i].len > 0) {

@@ -107,6 +107,10 @@ cudaError_t launch_flat_mean(InType in, int W, const void* const* src, float* ou
 cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, const LaunchCfg& cfg,
                                   cudaStream_t stream, long long* launches);
 
+// One CTA that waits on an mbarrier nothing completes, for limit_cycles; the
+// bounded wait writes its timeout code into *status (ddp_kernels_tma.cu).
+cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t stream);
+
 // Bulk-copy (TMA) pipelined variant of launch_reduce, in ddp_kernels_tma.cu.
 cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
                               long long lo, long long hi, int s0, int s1, float inv_w,

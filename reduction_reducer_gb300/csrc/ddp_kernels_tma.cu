@@ -86,12 +86,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // after kWaitCycles, record `code` and mark the thread failed, after which
 // it never waits again (so a broken pipeline costs one time limit per
 // thread, not one per chunk).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, int code, bool& failed) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, int code, bool& failed,
+                                          long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     if (failed) return false;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             atomicExch(status, code);
             failed = true;
             return false;
@@ -122,10 +123,14 @@ __device__ __forceinline__ void walk(const ReduceParams& p, int s, long long x, 
         const long long e = a1 < y ? a1 : y;
         const long long xb = (x + N - 1) / N * N;
         const long long xe = e / N * N;
+        if (!debug_ok(p.status, s < p.s1 && a0 <= x && x < e && e <= a1 && p.lo <= x && e <= p.hi, kDbgSegRange, x))
+            return;
         if (__ldg(p.seg_vec + s) && xb < xe) {
             if (x < xb) scalar(s, a0, x, xb);
             for (long long c = xb; c < xe; c += p.tile) {
                 const long long L = xe - c < p.tile ? xe - c : p.tile;
+                if (!debug_ok(p.status, x <= c && 0 < L && L <= p.tile && c + L <= e && L % N == 0, kDbgChunkRange, c))
+                    return;
                 body(s, a0, c, L);
             }
             if (xe < e) scalar(s, a0, xe, e);
@@ -194,17 +199,29 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
                 const uint32_t fb = smem_u32(full + st);
                 // replicas without a gradient for this segment copy nothing
                 const unsigned long long mk = seg_mask(mask, sg - p.s0);
+                const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * NS;
+                Tin* dst = ring + st * stage_elems;
+                // debug builds: a stage whose copies would break the bulk-copy
+                // alignment rules is posted empty and not copied
+                bool issue = true;
+                if constexpr (kDebug) {
+                    bool ok = (bytes & 15u) == 0;
+                    for (int q = lane; q < NS; q += 32)
+                        ok = ok && ((reinterpret_cast<uintptr_t>(src[q] + (c - a0)) |
+                                     smem_u32(dst + static_cast<long long>(q) * p.tile)) & 15u) == 0;
+                    issue = __all_sync(0xffffffffu, ok);
+                    if (!issue && lane == 0) debug_record(p.status, kDbgCopyAlign, c);
+                }
                 if (lane == 0) {
                     uint32_t present = 0;
                     for (int q = 0; q < NS; ++q) present += has_replica(mk, q % W) ? 1u : 0u;
-                    mbar_expect_tx(fb, bytes * present);
+                    mbar_expect_tx(fb, issue ? bytes * present : 0u);
                 }
                 __syncwarp();
-                const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * NS;
-                Tin* dst = ring + st * stage_elems;
-                for (int q = lane; q < NS; q += 32)
-                    if (has_replica(mk, q % W))
-                        bulk_g2s(smem_u32(dst + static_cast<long long>(q) * p.tile), src[q] + (c - a0), bytes, fb);
+                if (issue)
+                    for (int q = lane; q < NS; q += 32)
+                        if (has_replica(mk, q % W))
+                            bulk_g2s(smem_u32(dst + static_cast<long long>(q) * p.tile), src[q] + (c - a0), bytes, fb);
                 ++k;
             },
             [](int, long long, long long, long long) {});
@@ -296,9 +313,14 @@ __device__ __forceinline__ void walk_pairs(const AccParams& p, int i, long long 
             const bool vec = ((reinterpret_cast<uintptr_t>(q.g) | reinterpret_cast<uintptr_t>(q.acc)) & 15u) == 0;
             const long long xb = (x + 3) / 4 * 4;
             const long long xe = e / 4 * 4;
+            if (!debug_ok(p.status, q.off <= x && e <= p.total, kDbgPairRange, x)) return;
             if (vec && xb < xe) {
                 if (x < xb) scalar(i, x, xb);
-                for (long long c = xb; c < xe; c += p.tile) body(i, c, xe - c < p.tile ? xe - c : p.tile);
+                for (long long c = xb; c < xe; c += p.tile) {
+                    const long long L = xe - c < p.tile ? xe - c : p.tile;
+                    if (!debug_ok(p.status, x <= c && 0 < L && c + L <= e && L % 4 == 0, kDbgChunkRange, c)) return;
+                    body(i, c, L);
+                }
                 if (xe < e) scalar(i, xe, e);
             } else {
                 scalar(i, x, e);
@@ -356,10 +378,19 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
                 const uint32_t bytes = static_cast<uint32_t>(L * sizeof(float));
                 const uint32_t fb = smem_u32(full + st);
                 const AccPairDev& q = p.pair[i];
-                mbar_expect_tx(fb, q.assign ? bytes : 2u * bytes);
                 float* dst = ring + st * stage_elems;
-                bulk_g2s(smem_u32(dst), q.g + (c - q.off), bytes, fb);
-                if (!q.assign) bulk_g2s(smem_u32(dst + p.tile), q.acc + (c - q.off), bytes, fb);
+                bool issue = true;
+                if constexpr (kDebug) {
+                    issue = ((bytes | reinterpret_cast<uintptr_t>(q.g + (c - q.off)) |
+                              reinterpret_cast<uintptr_t>(q.acc + (c - q.off)) | smem_u32(dst) |
+                              smem_u32(dst + p.tile)) & 15u) == 0;
+                    if (!issue) debug_record(p.status, kDbgCopyAlign, c);
+                }
+                mbar_expect_tx(fb, !issue ? 0u : q.assign ? bytes : 2u * bytes);
+                if (issue) {
+                    bulk_g2s(smem_u32(dst), q.g + (c - q.off), bytes, fb);
+                    if (!q.assign) bulk_g2s(smem_u32(dst + p.tile), q.acc + (c - q.off), bytes, fb);
+                }
                 ++k;
             },
             [](int, long long, long long) {});
@@ -405,6 +436,18 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
                 q.acc[j] = q.assign ? q.g[j] : __fadd_rn(q.acc[j], q.g[j]);
             }
         });
+}
+
+// Bounded-wait self-test: one thread waits on an mbarrier that nothing
+// arrives at, with the given cycle budget; the wait must give up, record
+// its code in *status and return.
+__global__ void wait_selftest_kernel(long long limit, int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    bool failed = false;
+    mbar_wait(smem_u32(&bar), 0u, status, kStatusFullTimeout, failed, limit);
 }
 
 template <typename M>
@@ -472,6 +515,11 @@ cudaError_t ensure_smem_attr(K k) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_cycles, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, const LaunchCfg& cfg,
                                   cudaStream_t stream, long long* launches) {

@@ -64,8 +64,10 @@ def _ptr_array(ptrs):
 class Reducer:
     """One bucketed reducer context (``ddp_ctx``)."""
 
-    def __init__(self, numel, dtype: str = "f32", cap_bytes: int = 25 << 20):
-        self.lib = _lib.load()
+    def __init__(self, numel, dtype: str = "f32", cap_bytes: int = 25 << 20, lib_path: str = _lib.LIB_PATH):
+        """lib_path: the library build to use (``_lib.DEBUG_LIB_PATH``: the
+        bounds-checking build)."""
+        self.lib = _lib.load(lib_path)
         self.numel = [int(n) for n in numel]
         self.dtype = dtype
         arr = (C.c_int64 * max(len(self.numel), 1))(*self.numel)
@@ -310,6 +312,13 @@ class Reducer:
     def set_dry_run(self, on: bool = True):
         self.set_option(_lib.OPT_DRY_RUN, 1 if on else 0)
 
+    def debug_record(self):
+        """Read and clear the bounds-check record: (code, element index);
+        (0, 0) when no check failed (always, in a release build)."""
+        code, index = C.c_int32(), C.c_int64()
+        self._check(self.lib.ddp_get_debug_record(self._h, C.byref(code), C.byref(index)))
+        return code.value, index.value
+
     def device_status(self) -> int:
         """Read and clear the kernels' device status word (synchronous)."""
         st = C.c_int32()
@@ -331,3 +340,14 @@ class Reducer:
             self.destroy()
         except Exception:
             pass
+
+
+def selftest_bounded_wait(limit_cycles: int, lib_path: str = _lib.LIB_PATH) -> int:
+    """Run the bounded-wait self-test on the current device; returns the
+    status code the abandoned wait wrote (3 when it ended as designed)."""
+    lib = _lib.load(lib_path)
+    code = C.c_int32()
+    st = lib.ddp_selftest_bounded_wait(int(limit_cycles), C.byref(code))
+    if st != 0:
+        raise _ERRORS.get(st, DDPError)(st, "ddp_selftest_bounded_wait")
+    return code.value

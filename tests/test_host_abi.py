@@ -440,3 +440,33 @@ def test_hook_on_bucket_views_rules(lib):
     z.set_dry_run(True)
     z.bind([[0, 0x1000, 0]], 0x10000000, None)
     z.register_comm_hook("mean", None)
+
+
+def test_debug_build_exports_every_declared_symbol(lib):
+    """The bounds-checking build carries the same ABI."""
+    from reduction_reducer_gb300 import _lib
+    if not os.path.exists(_lib.DEBUG_LIB_PATH):
+        from reduction_reducer_gb300 import build
+        build.build_debug()
+    dbg = _lib.load(_lib.DEBUG_LIB_PATH)
+    for name in header_functions():
+        assert hasattr(dbg, name), name
+    assert dbg is not lib
+
+
+def test_selftest_rejects_bad_limits(lib):
+    import ctypes as C
+    code = C.c_int32(7)
+    assert lib.ddp_selftest_bounded_wait(0, C.byref(code)) == -1 and code.value == 0
+    assert lib.ddp_selftest_bounded_wait(4_000_000_001, C.byref(code)) == -1
+    assert lib.ddp_selftest_bounded_wait(1000, None) == -1
+
+
+def test_debug_record_rules(lib):
+    from reduction_reducer_gb300 import NotBound
+    red = _make([4, 4], "f32", 16)
+    with pytest.raises(NotBound):
+        red.debug_record()
+    red.set_dry_run(True)
+    red.bind([[0x1000, 0x1100]], 0x10000000, None)
+    assert red.debug_record() == (0, 0)      # dry run: nothing on a device
