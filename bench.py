@@ -566,7 +566,10 @@ def extra_configs(torch, device, stream, args, dist, keep):
         with torch.cuda.stream(stream):
             ms, _, _ = time_steps(torch, stream, lambda: wl.step(stream), steps, warm, dist)
         t = ms / steps
-        out[key] = {"gbs": round(wl.bytes / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4),
+        gbs = wl.bytes / (t * 1e-3) / 1e9
+        peak, _ = peaks()
+        out[key] = {"gbs": round(gbs, 1), "ms_per_step": round(t, 4),
+                    "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
                     "bytes_per_step": wl.bytes, "buckets": wl.B, "W": wl.W, "kernel": kernel_name(wl),
                     "grad_elems_per_s": round(wl.W * wl.N / (t * 1e-3), 1), "note": note}
 

@@ -477,6 +477,40 @@ namespace {
 
 // Build the segment table of the current layout for the given pointers and
 // upload it (replacing any previous table).
+// Consistency of the layout a table is built from, checked at every bind and
+// rebuild (O(P + S)): every variable sits in exactly one bucket at the prefix
+// sum of the earlier members' lengths, the buckets tile the arena, and the
+// segments of each bucket tile exactly its non-empty range in order.
+std::string layout_problem(const ddp_ctx* c, const std::vector<int64_t>& seg_off,
+                           const std::vector<int64_t>& seg_len, const std::vector<int32_t>& bucket_seg) {
+    std::vector<uint8_t> seen(c->P, 0);
+    if (c->bucket_off.size() != static_cast<size_t>(c->B) + 1 || c->bucket_off[0] != 0) return "bucket offsets";
+    for (int32_t b = 0; b < c->B; ++b) {
+        int64_t off = 0;
+        for (size_t i = 0; i < c->members[b].size(); ++i) {
+            const int32_t v = c->members[b][i];
+            if (v < 0 || v >= c->P || seen[v]) return "variable " + std::to_string(v) + " placed twice or out of range";
+            seen[v] = 1;
+            const ddp_locator& l = c->loc[v];
+            if (l.bucket != b || l.intra != static_cast<int32_t>(i) || l.offset != off || l.length != c->numel[v])
+                return "locator of variable " + std::to_string(v);
+            off += c->numel[v];
+        }
+        if (c->bucket_off[b + 1] != c->bucket_off[b] + off) return "bucket " + std::to_string(b) + " length";
+        int64_t at = c->bucket_off[b];   // segments tile [bucket_off[b], bucket_off[b+1]) in order
+        for (int32_t sg = bucket_seg[b]; sg < bucket_seg[b + 1]; ++sg) {
+            if (seg_off[sg] != at || seg_len[sg] <= 0) return "segment " + std::to_string(sg) + " of bucket " + std::to_string(b);
+            at += seg_len[sg];
+        }
+        if (at != c->bucket_off[b + 1]) return "segments of bucket " + std::to_string(b) + " do not cover it";
+    }
+    for (int32_t v = 0; v < c->P; ++v)
+        if (!seen[v]) return "variable " + std::to_string(v) + " in no bucket";
+    if (bucket_seg[c->B] != static_cast<int32_t>(seg_len.size()) || seg_off.back() != c->bucket_off[c->B])
+        return "segment table end";
+    return "";
+}
+
 // last: W*P last-step gradients (fused last micro-step; fp32) or nullptr.
 int build_table(ddp_ctx* c, int32_t W, const void* const* grads, const void* const* last, float* bucket_arena,
                 float* const* grad_out, int32_t n_out) {
@@ -549,6 +583,8 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, const void* con
         }
         bucket_seg[c->B] = static_cast<int32_t>(seg_off.size());
         seg_off.push_back(total);
+        const std::string bad = layout_problem(c, seg_off, seg_len, bucket_seg);
+        if (!bad.empty()) return fail(c, DDP_ERR_INVALID_ARG, "internal layout check failed: " + bad);
     } catch (const std::bad_alloc&) {
         return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
     }
