@@ -573,6 +573,12 @@ def extra_configs(torch, device, stream, args, dist, keep):
                     "bytes_per_step": wl.bytes, "buckets": wl.B, "W": wl.W, "kernel": kernel_name(wl),
                     "grad_elems_per_s": round(wl.W * wl.N / (t * 1e-3), 1), "note": note}
 
+    # Linear(10,10), W=2: one bucket of 110 elements, launch latency rather
+    # than bandwidth (reported in microseconds per iteration)
+    wl = Workload("linear", torch, device, 25, n_out=1, driver="events")
+    timed(wl, "linear_w2", "Linear(10,10), W=2, one mark_ready call per event; latency-bound (one launch)")
+    out["linear_w2"]["us_per_step"] = round(out["linear_w2"]["ms_per_step"] * 1e3, 2)
+    wl.free()
     # BERT-large, one persistent launch over all buckets (kernel alone)
     keep.driver = "all"
     timed(keep, "bert_large_reduce_all", "one reduce_all launch per step")
