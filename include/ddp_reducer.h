@@ -117,7 +117,10 @@ int ddp_bind(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_ar
  * implicitly when the previous one finished. */
 int ddp_begin_iteration(ddp_ctx* ctx);
 
-/* Discard an unfinished iteration (nothing is launched). */
+/* Discard an unfinished iteration (nothing is launched); local-use bits the
+ * iteration took at its start (ddp_set_local_used) are dropped with it.
+ * Buckets already launched by it stay launched (their results are in the
+ * arena and outputs). */
 int ddp_abort_iteration(ddp_ctx* ctx);
 
 /* Variable `var`'s gradient is final ("NCCL 专家课程 30", section "Autograd Hook

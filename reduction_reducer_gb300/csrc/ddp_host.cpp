@@ -917,45 +917,49 @@ int ddp_accumulate_nosync_used(ddp_ctx* c, void* const* acc, const void* const* 
         return fail(c, DDP_ERR_INVALID_ARG, "local-use bits need DDP_OPT_FIND_UNUSED");
     const size_t WP = static_cast<size_t>(c->W) * c->P;
     std::vector<ddpk::AccPair> pairs;
+    std::vector<uint8_t> has;   // the block record after this step, committed once the step is accepted
     try {
         // A gradient field that is empty in this block takes the gradient;
         // a filled one adds it.  Without a block record every field counts
         // as filled after the first step.
-        if (first_step || c->has_grad.size() != WP) c->has_grad.assign(WP, first_step ? 0 : 1);
+        if (first_step || c->has_grad.size() != WP) has.assign(WP, first_step ? 0 : 1);
+        else has = c->has_grad;
         pairs.reserve(WP);
         for (int r = 0; r < c->W; ++r)
             for (int32_t v = 0; v < c->P; ++v) {
                 const size_t i = static_cast<size_t>(r) * c->P + v;
                 if (used && !used[i]) continue;
                 if (c->numel[v] == 0) {
-                    c->has_grad[i] = 1;
+                    has[i] = 1;
                     continue;
                 }
                 if (!acc[i] || !g[i])
                     return fail(c, DDP_ERR_INVALID_ARG, "NULL accumulator or gradient at replica " +
                                                             std::to_string(r) + " variable " + std::to_string(v));
                 pairs.push_back(ddpk::AccPair{static_cast<const float*>(g[i]), static_cast<float*>(acc[i]),
-                                              c->numel[v], c->has_grad[i] ? 0 : 1});
-                c->has_grad[i] = 1;
+                                              c->numel[v], has[i] ? 0 : 1});
+                has[i] = 1;
             }
-        if (c->opt_find_unused) {   // the local-use bitmap accumulates until the next reduction
-            if (c->pending_used.size() != WP) c->pending_used.assign(WP, 0);
-            for (size_t i = 0; i < WP; ++i) c->pending_used[i] |= used ? (used[i] ? 1 : 0) : 1;
-            c->pending_set = true;
-        }
+        if (c->opt_find_unused && c->pending_used.size() != WP) c->pending_used.assign(WP, 0);
     } catch (const std::bad_alloc&) {
         return fail(c, DDP_ERR_NO_MEMORY, "out of host memory");
     }
-    if (c->dry || pairs.empty()) return DDP_OK;
-    int st = check_device(c);
-    if (st != DDP_OK) return st;
-    ddpk::LaunchCfg cfg = c->cfg;
-    cfg.ctas_per_sm = c->acc_ctas;
-    long long n = 0;
-    cudaError_t e = ddpk::launch_accumulate(pairs.data(), static_cast<int>(pairs.size()), cfg,
-                                            static_cast<cudaStream_t>(stream), &n);
-    c->launches += n;
-    if (e != cudaSuccess) return cuda_fail(c, e, "accumulate launch");
+    if (!c->dry && !pairs.empty()) {
+        const int st = check_device(c);
+        if (st != DDP_OK) return st;
+        ddpk::LaunchCfg cfg = c->cfg;
+        cfg.ctas_per_sm = c->acc_ctas;
+        long long n = 0;
+        const cudaError_t e = ddpk::launch_accumulate(pairs.data(), static_cast<int>(pairs.size()), cfg,
+                                                      static_cast<cudaStream_t>(stream), &n);
+        c->launches += n;
+        if (e != cudaSuccess) return cuda_fail(c, e, "accumulate launch");
+    }
+    c->has_grad.swap(has);
+    if (c->opt_find_unused) {   // the local-use bitmap accumulates until the next reduction
+        for (size_t i = 0; i < WP; ++i) c->pending_used[i] |= used ? (used[i] ? 1 : 0) : 1;
+        c->pending_set = true;
+    }
     return DDP_OK;
 }
 

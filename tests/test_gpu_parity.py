@@ -579,3 +579,30 @@ def test_iteration_captured_in_cuda_graph(kernel):
         assert bits_equal(arena.cpu().numpy(), want_arena), first_mismatch(arena.cpu().numpy(), want_arena)
         for v in range(len(numel)):
             assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])
+
+
+def test_nosync_failed_step_changes_nothing():
+    """A micro-step rejected for a NULL pointer leaves the block record as it
+    was: a later adding step adds to every field (acc = g1 + g3), including
+    the fields the rejected call had walked before the NULL."""
+    from reduction_reducer_gb300 import InvalidArg
+    numel = [100, 37, 4097]
+    W = 2
+    steps = [host_grads(numel, W, "f32", step=k) for k in range(3)]
+    offs = steps[0][2]
+    dev = [host_to_device_views(steps[k][0], numel, offs, "f32", DEV)[1] for k in range(3)]
+    acc = [[torch.full((n,), float("nan"), device=DEV) for n in numel] for _ in range(W)]
+    red = Reducer(numel, "f32", 1 << 20)
+    red.bind(acc, torch.empty(red.arena_numel(), device=DEV), None)
+    red.accumulate_nosync(acc, dev[0], first_step=True)
+    bad = [[t.data_ptr() for t in rep] for rep in dev[1]]
+    bad[1][1] = 0                                            # NULL gradient, replica 1, variable 1
+    with pytest.raises(InvalidArg):
+        red.accumulate_nosync(acc, bad, first_step=True)
+    red.accumulate_nosync(acc, dev[2], first_step=False)
+    torch.cuda.synchronize()
+    for r in range(W):
+        want = accumulate_steps([steps[0][1][r], steps[2][1][r]])
+        for v in range(len(numel)):
+            assert bits_equal(acc[r][v].cpu().numpy(), want[v]), (r, v)
+    red.destroy()
