@@ -337,7 +337,9 @@ enum ddp_option {
                                      pointers without a device table (host tests) */
     DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 = occupancy maximum */
     DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
-    DDP_OPT_BLOCK_THREADS = 3,    /* register-streaming kernel: 128 or 256 (default) */
+    DDP_OPT_BLOCK_THREADS = 3,    /* threads per CTA of the register-streaming kernels: 128 or 256 for
+                                     all of them, or 0 (default): 128 for the bucket kernel, 256 for
+                                     the accumulate and hook copy kernels */
     DDP_OPT_KERNEL = 4,           /* 0: register-streaming kernel, 1: bulk-copy (TMA) pipeline,
                                      2 (default): per context, bulk copy when the median bucket has at
                                      least DDP_OPT_AUTO_MIN_ELEMS elements, register streaming below */

@@ -88,7 +88,7 @@ struct ddp_ctx {
     bool dry = false;
     bool pdl = true;
     int opt_ctas = 0;
-    int opt_block = 256;
+    int opt_block = 0;              // 0: 128 threads for the bucket kernel, 256 for accumulate and hook copies
     // Defaults from the GB300 sweeps: the kernel is chosen per context from
     // the median bucket length (bulk-copy pipeline with 3 stages of 32 KiB,
     // one CTA per SM, from 2^20 elements up; register streaming below, where
@@ -105,6 +105,7 @@ struct ddp_ctx {
     int64_t call_launches = 0;      // launches issued by the current API call
     ddpk::LaunchCfg cfg{};
     int acc_ctas = 1;
+    int aux_block = 256;            // threads per CTA of the accumulate and hook copy kernels
     int64_t launches = 0;
     std::string err;
 };
@@ -220,10 +221,14 @@ int refresh_launch_cfg(ddp_ctx* c) {
     if (e != cudaSuccess) return cuda_fail(c, e, "cudaDeviceGetAttribute");
     const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
     c->cfg.sms = sms;
-    c->cfg.block = c->opt_block;
+    // GB300 sweeps of the register-streaming kernel: 128-thread CTAs beat 256
+    // on small buckets (per-gradient and 1 MiB caps) and tie on large ones
+    const int block = c->opt_block > 0 ? c->opt_block : 128;
+    c->aux_block = c->opt_block > 0 ? c->opt_block : 256;
+    c->cfg.block = block;
     c->cfg.pdl = c->pdl;
     c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas
-                                         : ddpk::reduce_max_ctas_per_sm(in, c->W, c->opt_block, c->tab.add != 0);
+                                         : ddpk::reduce_max_ctas_per_sm(in, c->W, block, c->tab.add != 0);
     if (c->opt_kernel == ddpk::KERNEL_AUTO) {
         std::vector<int64_t> lens;
         for (int32_t b = 0; b < c->B; ++b) lens.push_back(c->bucket_off[b + 1] - c->bucket_off[b]);
@@ -241,7 +246,7 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->cfg.tma_ctas_per_sm = c->opt_tma_ctas;
     c->cfg.status = c->tab.status;
 
-    c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->opt_block);
+    c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->aux_block);
     return DDP_OK;
 }
 
@@ -274,8 +279,10 @@ bool bucket_view_bases(const ddp_ctx* c, int32_t b, const void** base) {
     return true;
 }
 
-int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& cfg, void* stream) {
+int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& launch_cfg, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ddpk::LaunchCfg cfg = launch_cfg;
+    cfg.block = c->aux_block;
     std::vector<const void*> reps(c->W);
     std::vector<int64_t> offs, lens;
     for (int32_t b = b0; b < b1; ++b) {
@@ -949,6 +956,7 @@ int ddp_accumulate_nosync_used(ddp_ctx* c, void* const* acc, const void* const* 
         if (st != DDP_OK) return st;
         ddpk::LaunchCfg cfg = c->cfg;
         cfg.ctas_per_sm = c->acc_ctas;
+        cfg.block = c->aux_block;
         long long n = 0;
         const cudaError_t e = ddpk::launch_accumulate(pairs.data(), static_cast<int>(pairs.size()), cfg,
                                                       static_cast<cudaStream_t>(stream), &n);
@@ -1041,8 +1049,8 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             c->opt_tma_ctas = static_cast<int>(value);
             return refresh_launch_cfg(c);
         case DDP_OPT_BLOCK_THREADS:
-            if (value != 128 && value != 256)
-                return fail(c, DDP_ERR_INVALID_ARG, "block threads must be 128 or 256");
+            if (value != 0 && value != 128 && value != 256)
+                return fail(c, DDP_ERR_INVALID_ARG, "block threads must be 0 (automatic), 128 or 256");
             c->opt_block = static_cast<int>(value);
             return refresh_launch_cfg(c);
         default: return fail(c, DDP_ERR_INVALID_ARG, "unknown option");
