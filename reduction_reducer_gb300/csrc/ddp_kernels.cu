@@ -187,7 +187,7 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_consta
     x = x < p.lo ? p.lo : x;
     y = y > p.hi ? p.hi : y;
     if (x >= y) {   // whole CTA leaves together
-        if (threadIdx.x == 0) pdl_exit(p.chain);
+        if (threadIdx.x == 0) pdl_exit(p.chain, p.piece >= kHoldAllPiece);
         return;
     }
 
@@ -216,7 +216,7 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_consta
         x = e;
         ++s;
     }
-    if (threadIdx.x == 0) pdl_exit(p.chain);
+    if (threadIdx.x == 0) pdl_exit(p.chain, p.piece >= kHoldAllPiece);
 }
 
 // ------------------------------------------------------------------ accumulate kernel
@@ -228,7 +228,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
     long long y = x + p.piece;
     y = y > p.total ? p.total : y;
     if (x >= y) {
-        if (threadIdx.x == 0) pdl_exit(p.chain);
+        if (threadIdx.x == 0) pdl_exit(p.chain, false);
         return;
     }
     int i = find_pair(p, x);
@@ -281,7 +281,7 @@ accumulate_kernel(const __grid_constant__ AccParams p) {
         ++i;
         if (i < p.npairs && p.pair[i].off > x) x = p.pair[i].off;
     }
-    if (threadIdx.x == 0) pdl_exit(p.chain);
+    if (threadIdx.x == 0) pdl_exit(p.chain, false);
 }
 
 // ------------------------------------------------------------------ hook path kernels

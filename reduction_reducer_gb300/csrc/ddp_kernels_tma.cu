@@ -176,7 +176,7 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
     x = x < p.lo ? p.lo : x;
     y = y > p.hi ? p.hi : y;
     if (x >= y) {   // whole CTA, before any copy is issued
-        if (threadIdx.x == 0) pdl_exit(p.chain);
+        if (threadIdx.x == 0) pdl_exit(p.chain, p.piece >= kHoldAllPiece);
         return;
     }
     const int s = find_segment(p.seg_off, p.s0, p.s1, x);
@@ -229,7 +229,7 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
         // every issued copy must land before the CTA may exit
         for (long long j = k > S ? k - S : 0; j < k; ++j)
             mbar_wait(smem_u32(full + j % S), static_cast<uint32_t>(j / S) & 1u, p.status, kStatusDrainTimeout, failed);
-        pdl_exit(p.chain);
+        pdl_exit(p.chain, p.piece >= kHoldAllPiece);
         return;
     }
 
@@ -360,7 +360,7 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
     long long y = x + p.piece;
     y = y > p.total ? p.total : y;
     if (x >= y) {
-        if (threadIdx.x == 0) pdl_exit(p.chain);
+        if (threadIdx.x == 0) pdl_exit(p.chain, false);
         return;
     }
     const int i0 = find_pair(p, x);
@@ -396,7 +396,7 @@ accumulate_tma_kernel(const __grid_constant__ AccParams p) {
             [](int, long long, long long) {});
         for (long long j = k > S ? k - S : 0; j < k; ++j)
             mbar_wait(smem_u32(full + j % S), static_cast<uint32_t>(j / S) & 1u, p.status, kStatusDrainTimeout, failed);
-        pdl_exit(p.chain);
+        pdl_exit(p.chain, false);
         return;
     }
 
