@@ -257,22 +257,49 @@ def traffic_for(kernel_key, alg_bytes_per_launch):
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample_inputs(max_buckets: int = 3):
-    """Host inputs of the CPU-oracle sample: the first buckets of the
-    BERT-large 25 MiB layout, seeded N(0, 1e-3) draws per replica."""
+def oracle_sample_model(name="bert_large", cap_mib=25, n_buckets=3):
+    """Host inputs of a CPU-oracle sample: the tensors of the first
+    ``n_buckets`` buckets of a configuration's layout, as a model of their
+    own (their reverse walk closes the same buckets, so the oracle does the
+    sample's work and allocates an arena of the sample's size, not the whole
+    model's), with seeded N(0, 1e-3) draws per replica in the
+    configuration's dtype."""
     from oracle.buckets import assign_buckets
-    numel = shapes.numels(shapes.bert_large())
-    W = shapes.WORKLOADS["bert_large"]["W"]
-    members, locs = assign_buckets(numel, 4, 25 * MIB)
-    sub = list(range(min(max_buckets, len(members))))
-    vars_ = sorted(v for b in sub for v in members[b])
-    offs, total = gen.packed_offsets([numel[v] for v in vars_])
-    grads = [[None] * len(numel) for _ in range(W)]
+    spec = shapes.WORKLOADS[name]
+    full = shapes.numels(spec["shapes"]())
+    W, dtype = spec["W"], spec["dtype"]
+    s_in = 4 if dtype == "f32" else 2
+    members, _ = assign_buckets(full, s_in, cap_mib * MIB)
+    n_buckets = min(n_buckets, len(members))
+    vars_ = sorted(v for b in range(n_buckets) for v in members[b])
+    numel = [full[v] for v in vars_]
+    sub_members, locs = assign_buckets(numel, s_in, cap_mib * MIB)
+    assert [sorted(vars_[i] for i in m) for m in sub_members] == [sorted(members[b]) for b in range(n_buckets)]
+    offs, total = gen.packed_offsets(numel)
+    grads = []
     for r in range(W):
-        flat = gen.draw_flat_np(total, r)
-        for v, o in zip(vars_, offs):
-            grads[r][v] = flat[o:o + numel[v]]
-    return dict(numel=numel, W=W, members=members, locs=locs, sub=sub, vars=vars_, grads=grads)
+        flat = gen.draw_flat_np(total, r, 0, dtype)
+        grads.append([flat[o:o + n] for o, n in zip(offs, numel)])
+    n_el = sum(numel)
+    desc = (f"buckets 0..{n_buckets - 1} of the {name} {cap_mib} MiB layout ({len(vars_)} tensors, {n_el} elements, "
+            f"W={W}, {dtype})")
+    return dict(numel=numel, W=W, s_in=s_in, members=sub_members, locs=locs, grads=grads, n_el=n_el, desc=desc)
+
+
+def oracle_sample_inputs(max_buckets: int = 3):
+    """The BERT-large sample of ``cpu_baseline`` and the reference arm."""
+    return oracle_sample_model("bert_large", 25, max_buckets)
+
+
+def _time_until(fn, target_s):
+    fn()                                   # untimed first call (page faults of fresh memory)
+    reps, t = 0, 0.0
+    while t < target_s:
+        t0 = time.perf_counter()
+        fn()
+        t += time.perf_counter() - t0
+        reps += 1
+    return reps, t
 
 
 def oracle_sample_gbs(target_s: float, max_buckets: int = 3, inputs=None):
@@ -280,23 +307,46 @@ def oracle_sample_gbs(target_s: float, max_buckets: int = 3, inputs=None):
     oracle work; input generation is outside the timing."""
     from oracle.reduce import reduce_buckets
     d = inputs or oracle_sample_inputs(max_buckets)
-    numel, W, members, locs, sub, vars_, grads = (d[k] for k in ("numel", "W", "members", "locs", "sub", "vars", "grads"))
-    n_el = sum(numel[v] for v in vars_)
-    bytes_per = view_bytes(W, n_el, 4)
-    reps, t = 0, 0.0
-    while t < target_s:
-        t0 = time.perf_counter()
-        reduce_buckets(grads, members, locs, numel, buckets=sub)
-        t += time.perf_counter() - t0
-        reps += 1
-    gbs = bytes_per * reps / t / 1e9
-    sample = (f"buckets 0..{sub[-1]} of the BERT-large 25 MiB layout ({len(vars_)} tensors, "
-              f"{n_el} elements, W={W}) x {reps} repetitions, {t:.1f} s of oracle work")
+    reps, t = _time_until(lambda: reduce_buckets(d["grads"], d["members"], d["locs"], d["numel"]), target_s)
+    gbs = view_bytes(d["W"], d["n_el"], d["s_in"]) * reps / t / 1e9
+    sample = f"{d['desc']} x {reps} repetitions, {t:.1f} s of oracle work"
     return gbs, sample, t
 
 
 def cpu_threads_used():
     return 1   # NumPy elementwise ufuncs run on the calling thread
+
+
+def oracle_config_sample(name, cap_mib, target_s=2.0):
+    """The CPU oracle timed on one configuration's own layout: its first
+    bucket (seeded draws, the configuration's W and dtype), reduced
+    repeatedly until ``target_s`` of oracle work; same byte formula as the
+    GPU line.  For the no_sync configuration the adding micro-step is timed
+    on the same bucket (12 bytes per replica element)."""
+    from oracle.nosync import accumulate
+    from oracle.reduce import reduce_buckets
+    d = oracle_sample_model(name, cap_mib, 1)
+    W, n_el = d["W"], d["n_el"]
+    reps, t = _time_until(lambda: reduce_buckets(d["grads"], d["members"], d["locs"], d["numel"]), target_s)
+    out = {"gbs": round(view_bytes(W, n_el, d["s_in"]) * reps / t / 1e9, 3), "us_per_reduce": round(1e6 * t / reps, 1),
+           "cores": cpu_threads_used(), "kind": "oracle",
+           "sample": f"{d['desc']} x {reps} repetitions, {t:.1f} s of oracle work"}
+    if shapes.WORKLOADS[name].get("K"):
+        acc = [[x.copy() for x in g] for g in d["grads"]]
+        reps_a, t_a = _time_until(lambda: [accumulate(acc[r], d["grads"][r], first_step=False) for r in range(W)],
+                                  target_s)
+        out["accumulate_gbs"] = round(3 * W * n_el * 4 * reps_a / t_a / 1e9, 3)
+    return out
+
+
+def add_cpu_oracle(per_config, target_s=2.0):
+    """A bounded CPU-oracle sample beside each configuration's GPU line."""
+    for key, name, cap in (("linear_w2", "linear", 25), ("resnet50_w8", "resnet50", 25),
+                           ("bert_large_reduce_all", "bert_large", 25),
+                           *((f"gpt2_medium_w8_bf16_cap{c}", "gpt2_medium", c) for c in (0, 1, 5, 25, 100)),
+                           ("nosync_resnet50_w16_k8", "nosync_resnet50", 25)):
+        if key in per_config:
+            per_config[key]["cpu_oracle"] = oracle_config_sample(name, cap, target_s)
 
 
 # ---------------------------------------------------------------- arms
@@ -412,6 +462,8 @@ def run_ours(args):
         gbs_cpu, sample, _ = oracle_sample_gbs(args.cpu_s)
         cpu = {"value": round(gbs_cpu, 3), "unit": "GB/s", "cores": cpu_threads_used(), "kind": "oracle",
                "sample": sample, "host_cpus": os.cpu_count(), "affinity": len(os.sched_getaffinity(0))}
+        if extra:
+            add_cpu_oracle(extra, args.cpu_config_s)
 
     if dist:
         dist.barrier()
@@ -815,6 +867,8 @@ def main():
     ap.add_argument("--hook", default="none", choices=["none", "mean", "bf16_compress"],
                     help="profiling cases: reduce the main workload through a built-in hook")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-config-s", type=float, default=2.0,
+                    help="seconds of oracle work per configuration (per_config cpu_oracle)")
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     args = ap.parse_args()
     if args.impl == "reference":
