@@ -374,7 +374,8 @@ int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);
  * (the results of that launch are not to be trusted). */
 int ddp_get_device_status(ddp_ctx* ctx, int32_t* status);
 
-/* Read and clear the bounds-check record of a bound context (synchronous).
+/* Read and clear the bounds-check record of a bound context (synchronous:
+ * waits for the device).
  * Only a library built with -DDDP_DEBUG (libddpreducer_debug.so) checks, in
  * every kernel, that each range it walks lies inside its segment, launch and
  * stage and that every bulk copy is 16-byte aligned and sized; the first

@@ -632,10 +632,15 @@ int build_table(ddp_ctx* c, int32_t W, const void* const* grads, const void* con
     void* d = nullptr;
     e = cudaMalloc(&d, bytes);
     if (e != cudaSuccess) return cuda_fail(c, e, "cudaMalloc(segment table)");
-    e = cudaMemcpy(d, host.data(), bytes, cudaMemcpyHostToDevice);
+    // A copy from pageable memory may return before its DMA has landed, and
+    // it is ordered only with the default stream, not with the caller's
+    // (non-blocking) streams: wait for it here, so that any later launch on
+    // any stream reads the whole table.
+    e = cudaMemcpyAsync(d, host.data(), bytes, cudaMemcpyHostToDevice, nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
     if (e != cudaSuccess) {
         cudaFree(d);
-        return cuda_fail(c, e, "cudaMemcpy(segment table)");
+        return cuda_fail(c, e, "upload of the segment table");
     }
     auto* base = static_cast<unsigned char*>(d);
     c->dev_table = d;
@@ -1062,11 +1067,14 @@ int ddp_get_device_status(ddp_ctx* c, int32_t* status) {
     *status = 0;
     if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "device status before bind");
     int32_t v = 0;
-    cudaError_t e = cudaMemcpy(&v, c->tab.status, sizeof(v), cudaMemcpyDeviceToHost);
+    // every stream's launches, not only the default stream's, must be done
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, c->tab.status, sizeof(v), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(c, e, "read device status");
     if (v != 0) {
-        const int32_t zero = 0;
-        e = cudaMemcpy(c->tab.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        const int32_t zero = 0;   // landed before returning, like the table upload
+        e = cudaMemcpyAsync(c->tab.status, &zero, sizeof(zero), cudaMemcpyHostToDevice, nullptr);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
         if (e != cudaSuccess) return cuda_fail(c, e, "clear device status");
     }
     *status = v;
@@ -1080,11 +1088,13 @@ int ddp_get_debug_record(ddp_ctx* c, int32_t* code, int64_t* index) {
     if (!c->bound) return fail(c, DDP_ERR_NOT_BOUND, "debug record before bind");
     if (c->dry) return DDP_OK;
     int32_t words[4] = {0, 0, 0, 0};
-    cudaError_t e = cudaMemcpy(words, c->tab.status, sizeof(words), cudaMemcpyDeviceToHost);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(words, c->tab.status, sizeof(words), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(c, e, "read debug record");
     if (words[1] != 0) {
         const int32_t zero[3] = {0, 0, 0};
-        e = cudaMemcpy(c->tab.status + 1, zero, sizeof(zero), cudaMemcpyHostToDevice);
+        e = cudaMemcpyAsync(c->tab.status + 1, zero, sizeof(zero), cudaMemcpyHostToDevice, nullptr);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
         if (e != cudaSuccess) return cuda_fail(c, e, "clear debug record");
     }
     *code = words[1];
