@@ -45,10 +45,18 @@ def _ptr(x) -> int:
     return int(x.data_ptr())
 
 
+_torch = None   # resolved on first use: torch.cuda when a GPU is present, else False
+
+
 def _stream(stream) -> int:
+    """cudaStream_t of a torch stream, an int handle, or (None) torch's
+    current stream; 0 without a GPU (dry runs)."""
+    global _torch
     if stream is None:
-        import torch
-        return int(torch.cuda.current_stream().cuda_stream) if torch.cuda.is_available() else 0
+        if _torch is None:
+            import torch
+            _torch = torch.cuda if torch.cuda.is_available() else False
+        return int(_torch.current_stream().cuda_stream) if _torch else 0
     if isinstance(stream, int):
         return stream
     return int(stream.cuda_stream)
@@ -81,6 +89,8 @@ class Reducer:
         self.B = B.value
         self.P = len(self.numel)
         self._launched = (C.c_int32 * max(self.B, 1))()
+        self._n_launched = C.c_int32()                  # reused by every mark_ready call
+        self._n_ref = C.byref(self._n_launched)
         self._keep = ()
 
     build_buckets = classmethod(lambda cls, numel, dtype="f32", cap_bytes=25 << 20: cls(numel, dtype, cap_bytes))
@@ -159,9 +169,9 @@ class Reducer:
         self._check(self.lib.ddp_abort_iteration(self._h))
 
     def mark_ready(self, var: int, stream=None):
-        n = C.c_int32()
-        self._check(self.lib.ddp_mark_ready(self._h, int(var), self._launched, C.byref(n), _stream(stream)))
-        return [self._launched[i] for i in range(n.value)]
+        n = self._n_launched
+        self._check(self.lib.ddp_mark_ready(self._h, int(var), self._launched, self._n_ref, _stream(stream)))
+        return [self._launched[i] for i in range(n.value)] if n.value else []
 
     def mark_ready_many(self, vars_, stream=None):
         """Ready events in order, in one call; returns how many were processed."""
@@ -225,6 +235,8 @@ class Reducer:
         self.lib.ddp_get_bucket_info(self._h, C.byref(B), None)
         self.B = B.value
         self._launched = (C.c_int32 * max(self.B, 1))()
+        self._n_launched = C.c_int32()                  # reused by every mark_ready call
+        self._n_ref = C.byref(self._n_launched)
 
     # ---------------------------------------------------------------- no allocation
     def reduce_all_noalloc(self, grads, bucket_arena, grad_out=None, stream=None):
