@@ -392,6 +392,28 @@ def run_nosync_only(args):
     return 0
 
 
+def run_gpt2_only(args):
+    """The GPT-2-medium workload alone (W=8 bf16 at --cap-mib, reverse ready
+    order, one mark_ready_many call per step): a compact case for profiling
+    the per-gradient (cap 0) and small-bucket launches."""
+    import torch
+    from reduction_reducer_gb300 import _lib
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=device)
+    wl = Workload("gpt2_medium", torch, device, args.cap_mib, n_out=1, driver=args.driver, layers=args.layers)
+    if args.kernel != "auto":
+        wl.red.set_option(_lib.OPT_KERNEL, KERNEL_FLAG[args.kernel])
+    with torch.cuda.stream(stream):
+        ms, _, _ = time_steps(torch, stream, lambda: wl.step(stream), args.steps, args.warmup)
+    t = ms / args.steps
+    name = "gpt2_medium" if args.layers is None else f"gpt2_medium_{args.layers}layers"
+    print(json.dumps({"workload": f"{name}_w8_bf16_cap{args.cap_mib}", "gbs": round(wl.bytes / (t * 1e-3) / 1e9, 1),
+                      "ms_per_step": round(t, 4), "buckets": wl.B, "kernel": kernel_name(wl)}), flush=True)
+    wl.free()
+    return 0
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -857,9 +879,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--layers", type=int, default=None, help="smaller BERT (profiling case)")
-    ap.add_argument("--workload", default="bert_large", choices=["bert_large", "nosync_resnet50"],
-                    help="nosync_resnet50: the no_sync workload alone (profiling case)")
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers of BERT or GPT-2 (profiling cases)")
+    ap.add_argument("--workload", default="bert_large", choices=["bert_large", "nosync_resnet50", "gpt2_medium"],
+                    help="nosync_resnet50 / gpt2_medium: that workload alone (profiling cases)")
+    ap.add_argument("--cap-mib", type=int, default=0, help="bucket cap of --workload gpt2_medium")
     ap.add_argument("--nosync-k", type=int, default=8, help="micro-steps of --workload nosync_resnet50")
     ap.add_argument("--driver", default="hooks", choices=["hooks", "events", "all"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "tma"],
@@ -875,6 +898,8 @@ def main():
         return run_reference(args)
     if args.workload == "nosync_resnet50":
         return run_nosync_only(args)
+    if args.workload == "gpt2_medium":
+        return run_gpt2_only(args)
     return run_ours(args)
 
 
