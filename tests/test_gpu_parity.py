@@ -77,7 +77,7 @@ def set_kernel(red, kernel):
 
 
 def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_ready", odd=False,
-                 special=False, stream=None, iterations=1, out_odd=False, kernel="ldg"):
+                 special=False, stream=None, iterations=1, out_odd=False, kernel="ldg", options=None):
     elem = 4 if dtype == "f32" else 2
     flats, views, offs = host_grads(numel, W, dtype, odd=odd, special=special)
     members, locs = assign_buckets(numel, elem, cap)
@@ -86,6 +86,8 @@ def full_compare(numel, W, dtype, cap, order="straggler", n_out=1, mode="mark_re
 
     red = Reducer(numel, dtype, cap)
     set_kernel(red, kernel)
+    for opt, value in (options or {}).items():
+        red.set_option(opt, value)
     N = red.arena_numel()
     arena_whole, arena = guarded(N)
     out_offs, out_total = layout(numel, 64, out_odd)
@@ -188,6 +190,35 @@ def test_many_replicas(W, dtype, kernel):
     """W beyond the compiled-in widths: the generic replica loop."""
     numel = [3, 4097, 0, 70001, 16, 1000]
     full_compare(numel, W, dtype, cap=32 * 1024, order="random", n_out=1, kernel=kernel)
+
+
+# Launch shapes other than the defaults: ring depth and stage bytes (a 112 KiB
+# stage leaves room for fewer stages and, at many streams, smaller tiles), two
+# bulk-copy CTAs per SM, 256-thread register-streaming CTAs, a fixed number of
+# CTAs per SM, and no programmatic dependent launch.  Each changes the tile,
+# grid and slice arithmetic the kernels index with.
+O = _lib
+SHAPES = {
+    "tma_2x4k": ("tma", {O.OPT_STAGES: 2, O.OPT_STAGE_BYTES: 4096}),
+    "tma_8x16k": ("tma", {O.OPT_STAGES: 8, O.OPT_STAGE_BYTES: 16 * 1024}),
+    "tma_3x112k": ("tma", {O.OPT_STAGES: 3, O.OPT_STAGE_BYTES: 112 * 1024}),
+    "tma_4x32k_2cta": ("tma", {O.OPT_STAGES: 4, O.OPT_STAGE_BYTES: 32 * 1024, O.OPT_TMA_CTAS_PER_SM: 2}),
+    "tma_nopdl": ("tma", {O.OPT_PDL: 0}),
+    "chained_6x16k_2cta": ("chained", {O.OPT_STAGES: 6, O.OPT_STAGE_BYTES: 16 * 1024, O.OPT_TMA_CTAS_PER_SM: 2}),
+    "ldg_256": ("ldg", {O.OPT_BLOCK_THREADS: 256}),
+    "ldg_1cta": ("ldg", {O.OPT_CTAS_PER_SM: 1}),
+    "ldg_256_3cta": ("ldg", {O.OPT_BLOCK_THREADS: 256, O.OPT_CTAS_PER_SM: 3}),
+    "ldg_nopdl": ("ldg", {O.OPT_PDL: 0}),
+}
+
+
+@pytest.mark.parametrize("shape", list(SHAPES))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W,mode", [(3, "mark_ready_many"), (8, "mark_ready"), (16, "reduce_all")])
+def test_launch_shapes(shape, dtype, W, mode):
+    kernel, options = SHAPES[shape]
+    full_compare(RAGGED, W, dtype, cap=64 * 1024, order="straggler", n_out=1, mode=mode, kernel=kernel,
+                 options=options, odd=(W == 3))
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
