@@ -471,7 +471,11 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(torch, wl, stream, max(1, min(args.steps, args.e2e_steps)), dist)
+        try:
+            e2e = measure_e2e(torch, wl, stream, max(1, min(args.steps, args.e2e_steps)), dist)
+        except (RuntimeError, MemoryError) as exc:   # e.g. pinned host memory exhausted with many ranks
+            e2e = {"value": None, "unit": "GB/s", "error": f"{type(exc).__name__}: {str(exc)[:200]}"}
+            torch.cuda.synchronize()
     wl.free()
     torch.cuda.empty_cache()
 
@@ -530,10 +534,20 @@ def measure_e2e(torch, wl, stream, steps, dist, n_h2d=2, n_d2h=1):
     slice comes back on a second copy stream while later buckets are still
     in flight."""
     import ctypes
-    host_in = [torch.empty(f.numel(), dtype=f.dtype, pin_memory=True) for f in wl.flat]
+    ok = 1
+    try:
+        host_in = [torch.empty(f.numel(), dtype=f.dtype, pin_memory=True) for f in wl.flat]
+        host_out = torch.empty(wl.out_flat.numel(), dtype=torch.float32, pin_memory=True)
+    except (RuntimeError, MemoryError):
+        ok = 0
+    if dist:                     # every rank goes on, or none does (no rank left waiting in a collective)
+        flag = torch.tensor([ok], dtype=torch.int32, device=stream.device)
+        dist.all_reduce(flag, op=dist.ReduceOp.MIN)
+        ok = int(flag.item())
+    if not ok:
+        raise RuntimeError("pinned host buffers for the end-to-end measurement could not be allocated on every rank")
     for h, f in zip(host_in, wl.flat):
         h.copy_(f)
-    host_out = torch.empty(wl.out_flat.numel(), dtype=torch.float32, pin_memory=True)
     # several copy streams: one copy engine alone does not fill the host link
     h2d_streams = [torch.cuda.Stream(device=stream.device) for _ in range(n_h2d)]
     d2h_streams = [torch.cuda.Stream(device=stream.device) for _ in range(n_d2h)]
