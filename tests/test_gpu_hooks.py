@@ -73,6 +73,37 @@ def test_builtin_hooks(hook, dtype, W, n_out):
             assert np.array_equal(host[starts[b]:starts[b + 1]].view(np.uint8), bufs[r][b].view(np.uint8))
 
 
+@pytest.mark.parametrize("hook", ["mean", "bf16_compress"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_builtin_hooks_special_values(hook, dtype):
+    """±0, ±Inf, NaN, subnormals and ±3.4e38 (above the largest bf16, so the
+    compression hook rounds it to ±Inf) at seeded positions: the hooks'
+    device rounding and sums match the oracle bit for bit (NaN as a class)."""
+    numel = RAGGED
+    W, n_out, cap = 4, 1, 16 * 1024
+    flats, views, offs = host_grads(numel, W, dtype, special=True)
+    _, grads_dev = host_to_device_views(flats, numel, offs, dtype, DEV)
+    red = Reducer(numel, dtype, cap)
+    N = red.arena_numel()
+    arena = torch.full((N,), float("nan"), device=DEV)
+    outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+    red.bind(grads_dev, arena, outs)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    red.register_comm_hook(hook, [torch.empty(max(N, 1), dtype=tdt, device=DEV) for _ in range(W)])
+    members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+    fn = hook_mean if hook == "mean" else hook_bf16_compress
+    want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, fn, n_out=n_out)
+    red.begin_iteration()
+    red.mark_ready_many(gen.reverse_order(len(numel)))
+    torch.cuda.synchronize()
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    assert np.isinf(want_arena).any() and np.isnan(want_arena).any()   # the special values reached the result
+    for v in range(len(numel)):
+        assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v]), v
+    assert red.device_status() == 0
+
+
 def test_default_hook_equals_fused_pass():
     numel = shapes.numels(shapes.bert_large(layers=2, vocab=2048))
     W = 4
