@@ -44,3 +44,107 @@ def test_fuzz_bucket_pass(seed):
     c = draw_case(seed)
     full_compare(c["numel"], c["W"], c["dtype"], c["cap"], order="random", n_out=c["n_out"], mode=c["mode"],
                  odd=c["odd"], kernel=c["kernel"])
+
+
+# ---------------------------------------------------------------- unused parameters
+
+def draw_sizes(rng, P):
+    numel = [int(rng.choice(SIZES)) for _ in range(P)]
+    if rng.random() < 0.25:
+        numel[int(rng.integers(P))] = 1 << 20
+    return numel
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_fuzz_unused_parameters(seed):
+    """Random local-use masks (some variables unused on every replica, whose
+    copy-backs must stay untouched) over random layouts, W up to 64."""
+    import torch
+    from oracle.buckets import assign_buckets
+    from oracle.unused import globally_used, reduce_with_unused
+    from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views
+    from test_gpu_unused import _check_outputs, _guarded_outputs, _reducer
+
+    rng = np.random.default_rng(20_000 + seed)
+    P = int(rng.integers(1, 31))
+    numel = draw_sizes(rng, P)
+    W = int(rng.choice([1, 2, 3, 4, 8, 16, 33, 64]))
+    dtype = "f32" if rng.random() < 0.5 else "bf16"
+    cap = int(rng.choice(CAPS))
+    kernel = str(rng.choice(["ldg", "tma"]))
+    n_out = int(rng.choice([1, W]))
+    used = rng.random((W, P)) < float(rng.choice([0.3, 0.7, 0.95]))
+    if not used.any():              # with no gradient anywhere no ready event occurs and nothing is reduced
+        used[0, int(rng.integers(P))] = True
+    flats, views, offs = host_grads(numel, W, dtype, odd=bool(rng.random() < 0.3))
+    members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+    want_arena, want_outs = reduce_with_unused(views, used.tolist(), members, locs, numel, n_out=n_out)
+    _, grads_dev = host_to_device_views(flats, numel, offs, dtype, "cuda")
+    red = _reducer(numel, dtype, cap, kernel)
+    arena = torch.full((red.arena_numel(),), float("nan"), device="cuda")
+    bufs, out_views, out_offs = _guarded_outputs(numel, n_out)
+    red.bind(grads_dev, arena, out_views[0] if n_out == 1 else out_views)
+    red.set_local_used(used.tolist())
+    red.begin_iteration()
+    g = globally_used(used.tolist())
+    order = [int(v) for v in rng.permutation(P) if g[v]]
+    assert red.mark_ready_many(order) == len(order)
+    torch.cuda.synchronize()
+    assert red.device_status() == 0
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    _check_outputs(bufs, out_offs, numel, want_outs, used.tolist())
+    red.destroy()
+
+
+# ---------------------------------------------------------------- fused last micro-step
+
+@pytest.mark.parametrize("seed", range(60))
+def test_fuzz_fused_last_step(seed):
+    """K-1 accumulate micro-steps, then the K-th fused into the reduction,
+    over random layouts, W, K, launch modes and kernels; the accumulated
+    fields must come out unchanged."""
+    import torch
+    from oracle.buckets import assign_buckets
+    from oracle.nosync import accumulate_steps, reduce_last_step
+    from reduction_reducer_gb300 import Reducer, _lib
+    from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views
+    from test_gpu_last_step import KERNEL, _drive, _fields
+
+    rng = np.random.default_rng(30_000 + seed)
+    P = int(rng.integers(1, 31))
+    numel = draw_sizes(rng, P)
+    W = int(rng.choice([1, 2, 3, 4, 5, 8, 16, 33]))
+    K = int(rng.integers(2, 5))
+    cap = int(rng.choice(CAPS))
+    kernel = str(rng.choice(["ldg", "tma", "auto"]))
+    mode = str(rng.choice(MODES))
+    n_out = int(rng.choice([0, 1, W]))
+    steps = [host_grads(numel, W, "f32", step=k) for k in range(K)]
+    offs = steps[0][2]
+    acc_np = [accumulate_steps([steps[k][1][r] for k in range(K - 1)]) for r in range(W)]
+    members, locs = assign_buckets(numel, 4, cap)
+    want_arena, want_outs = reduce_last_step(acc_np, steps[K - 1][1], members, locs, numel, n_out=max(n_out, 1))
+
+    dev = [host_to_device_views(steps[k][0], numel, offs, "f32", "cuda")[1] for k in range(K)]
+    acc_flat, acc = _fields(numel, W, odd=bool(rng.random() < 0.3))
+    red = Reducer(numel, "f32", cap)
+    red.set_option(_lib.OPT_KERNEL, KERNEL[kernel])
+    arena = torch.full((red.arena_numel(),), float("nan"), device="cuda")
+    outs = [[torch.full((n,), float("nan"), device="cuda") for n in numel] for _ in range(max(n_out, 1))]
+    red.bind(acc, arena, None if n_out == 0 else (outs[0] if n_out == 1 else outs))
+    for k in range(K - 1):
+        red.accumulate_nosync(acc, dev[k], first_step=(k == 0))
+    torch.cuda.synchronize()
+    before = [f.clone() for f in acc_flat]
+    red.bind_last_step(dev[K - 1])
+    _drive(red, mode, [int(v) for v in rng.permutation(P)])
+    assert red.device_status() == 0
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    for o in range(n_out):
+        for v in range(P):
+            assert bits_equal(outs[o][v].cpu().numpy(), want_outs[0][v]), (o, v)
+    for r in range(W):
+        assert torch.equal(acc_flat[r].view(torch.int32), before[r].view(torch.int32)), r
+    red.destroy()
