@@ -148,3 +148,100 @@ def test_fuzz_fused_last_step(seed):
     for r in range(W):
         assert torch.equal(acc_flat[r].view(torch.int32), before[r].view(torch.int32)), r
     red.destroy()
+
+
+# ---------------------------------------------------------------- communication hooks
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_hooks(seed):
+    """The built-in hooks (mean, bf16 compression) through gather, hook and
+    copy-back, over random layouts, W up to 33, dtypes, output modes and
+    kernel choices."""
+    import torch
+    from oracle.buckets import assign_buckets
+    from oracle.hooks import hook_bf16_compress, hook_mean, reduce_with_hook
+    from reduction_reducer_gb300 import Reducer, _lib
+    from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views
+
+    rng = np.random.default_rng(40_000 + seed)
+    P = int(rng.integers(1, 31))
+    numel = draw_sizes(rng, P)
+    W = int(rng.choice([1, 2, 3, 4, 8, 16, 33]))
+    dtype = "f32" if rng.random() < 0.5 else "bf16"
+    cap = int(rng.choice(CAPS))
+    hook = str(rng.choice(["mean", "bf16_compress"]))
+    n_out = int(rng.choice([0, 1, W]))
+    kernel = str(rng.choice(["ldg", "tma", "auto"]))
+    flats, views, offs = host_grads(numel, W, dtype, odd=bool(rng.random() < 0.3))
+    _, grads_dev = host_to_device_views(flats, numel, offs, dtype, "cuda")
+    red = Reducer(numel, dtype, cap)
+    red.set_option(_lib.OPT_KERNEL, {"ldg": _lib.KERNEL_LDG, "tma": _lib.KERNEL_TMA, "auto": _lib.KERNEL_AUTO}[kernel])
+    N = red.arena_numel()
+    arena = torch.full((N,), float("nan"), device="cuda")
+    outs = [[torch.full((n,), float("nan"), device="cuda") for n in numel] for _ in range(max(n_out, 1))]
+    red.bind(grads_dev, arena, None if n_out == 0 else (outs[0] if n_out == 1 else outs))
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    red.register_comm_hook(hook, [torch.empty(max(N, 1), dtype=tdt, device="cuda") for _ in range(W)])
+    members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+    fn = hook_mean if hook == "mean" else hook_bf16_compress
+    want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, fn, n_out=max(n_out, 1))
+    red.begin_iteration()
+    assert red.mark_ready_many([int(v) for v in rng.permutation(P)]) == P
+    torch.cuda.synchronize()
+    assert red.device_status() == 0
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    for o in range(n_out):
+        for v in range(P):
+            assert bits_equal(outs[o][v].cpu().numpy(), want_outs[0][v]), (o, v)
+    red.destroy()
+
+
+# ---------------------------------------------------------------- bucket rebuild
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_rebuild(seed):
+    """An iteration records a random ready order; the buckets are re-packed
+    from it with random first and later caps; the next iteration must match
+    the oracle on the rebuilt layout through the same binding."""
+    import torch
+    from oracle.rebuild import rebuild_buckets
+    from oracle.reduce import reduce_buckets
+    from reduction_reducer_gb300 import Reducer, _lib
+    from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views
+
+    rng = np.random.default_rng(50_000 + seed)
+    P = int(rng.integers(1, 31))
+    numel = draw_sizes(rng, P)
+    W = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    dtype = "f32" if rng.random() < 0.5 else "bf16"
+    elem = 4 if dtype == "f32" else 2
+    kernel = str(rng.choice(["ldg", "tma", "auto"]))
+    flats, views, offs = host_grads(numel, W, dtype, odd=bool(rng.random() < 0.3))
+    _, grads_dev = host_to_device_views(flats, numel, offs, dtype, "cuda")
+    red = Reducer(numel, dtype, int(rng.choice(CAPS)))
+    red.set_option(_lib.OPT_KERNEL, {"ldg": _lib.KERNEL_LDG, "tma": _lib.KERNEL_TMA, "auto": _lib.KERNEL_AUTO}[kernel])
+    arena = torch.full((red.arena_numel(),), float("nan"), device="cuda")
+    outs = [torch.full((n,), float("nan"), device="cuda") for n in numel]
+    red.bind(grads_dev, arena, outs)
+    order = [int(v) for v in rng.permutation(P)]
+    red.begin_iteration()
+    red.mark_ready_many(order)
+    torch.cuda.synchronize()
+    assert red.get_ready_trace() == order
+    first_cap, cap = int(rng.choice(CAPS)), int(rng.choice(CAPS))
+    red.rebuild_buckets(None, first_cap, cap)
+    arena.fill_(float("nan"))
+    order2 = [int(v) for v in rng.permutation(P)]
+    red.begin_iteration()
+    red.mark_ready_many(order2)
+    torch.cuda.synchronize()
+    members, locs = rebuild_buckets(numel, elem, order, first_cap, cap)
+    want_arena, want_outs = reduce_buckets(views, members, locs, numel)
+    assert red.B == len(members)
+    assert red.device_status() == 0
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    for v in range(P):
+        assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v]), v
+    red.destroy()
