@@ -470,3 +470,31 @@ def test_debug_record_rules(lib):
     red.set_dry_run(True)
     red.bind([[0x1000, 0x1100]], 0x10000000, None)
     assert red.debug_record() == (0, 0)      # dry run: nothing on a device
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_host_core_fuzz_matches_oracle(lib, seed):
+    """Seeded random models (up to 300 tensors, empty ones included), caps,
+    dtypes and ready orders (random, or reverse with stragglers so buckets
+    park): locators, arena offsets and the launch/park sequence of every
+    event match the oracle exactly."""
+    rng = np.random.default_rng(60_000 + seed)
+    P = int(rng.integers(1, 301))
+    numel = [int(x) for x in rng.choice([0, 1, 3, 64, 1000, 4096, 70001, 1 << 20], size=P,
+                                        p=[0.05, 0.1, 0.1, 0.2, 0.2, 0.2, 0.1, 0.05])]
+    dtype = "f32" if rng.random() < 0.5 else "bf16"
+    elem = 4 if dtype == "f32" else 2
+    cap = int(rng.choice([0, 4096, 65536, 1 << 20, 4 << 20, 25 << 20]))
+    red = _make(numel, dtype, cap)
+    members, locs = assign_buckets(numel, elem, cap)
+    assert red.get_members() == members
+    assert red.get_locators() == [(l.bucket, l.intra, l.offset, l.length) for l in locs]
+    B, offs = red.get_bucket_info()
+    lens = [sum(numel[v] for v in m) for m in members]
+    assert offs == [sum(lens[:b]) for b in range(B + 1)]
+    if rng.random() < 0.5:
+        order = [int(v) for v in rng.permutation(P)]
+    else:
+        order = gen.straggler_order(members, p=0.5, seed=seed)
+    assert _run_dry(red, order) == _oracle_trace(members, order)
+    red.destroy()
