@@ -438,6 +438,8 @@ def run_ours(args):
 
     wl = Workload("bert_large", torch, device, 25, n_out=1, driver=args.driver, layers=args.layers)
     hook_bufs = profiling_setup(torch, device, wl.red, args, wl.W)
+    if args.unused:
+        apply_unused(wl)
     with torch.cuda.stream(stream):
         l0 = wl.red.launch_count()
         ms, t0, t1 = time_steps(torch, stream, lambda: wl.step(stream), args.steps, args.warmup, dist)
@@ -511,8 +513,8 @@ def run_ours(args):
                        "l2": (f"no flush: each step streams {wl.bytes / 1e9:.1f} GB, inputs "
                               f"{wl.W * wl.N * wl.s_in / 1e9:.1f} GB > 129 MB L2"),
                        "parallelism": f"replicas only x{world}",
-                       **({"profiling": {"kernel": args.kernel, "hook": args.hook}}
-                          if args.kernel != "auto" or args.hook != "none" else {})},
+                       **({"profiling": {"kernel": args.kernel, "hook": args.hook, "unused": args.unused}}
+                          if args.kernel != "auto" or args.hook != "none" or args.unused else {})},
             "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
             "grad_elems_per_s": round(elems * world, 1),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": timed_launches * world,
@@ -817,13 +819,15 @@ def hook_config(torch, device, keep, timed, out):
     torch.cuda.empty_cache()
 
 
-def unused_config(wl, timed, out):
-    """find_unused_parameters on BERT-large: the masked launches of one
-    iteration, bytes = the replica reads that happen + bucket writes +
-    copy-backs actually written."""
+def apply_unused(wl):
+    """Make ``wl.step`` an iteration with unused parameters (find_unused): on
+    BERT-large the pooler is unused on every replica and the FFN of every
+    fourth layer on replica 1; ``wl.bytes`` becomes the replica reads that
+    happen + bucket writes + copy-backs actually written.  Returns a function
+    that restores the plain iteration."""
     import ctypes
     from reduction_reducer_gb300 import _lib
-    names = [n for n, _ in shapes.bert_large()]
+    names = [n for n, _ in (shapes.bert_large() if wl.layers is None else shapes.bert_large(layers=wl.layers))]
     used = [[True] * wl.P for _ in range(wl.W)]
     for v, n in enumerate(names):
         if n.startswith("pooler"):
@@ -836,7 +840,6 @@ def unused_config(wl, timed, out):
     order = [v for v in wl.order if gused[v]]
     order_c = (ctypes.c_int32 * len(order))(*order)
     saved_step, saved_bytes = wl.step, wl.bytes
-
     used_c = wl.red.bits(used)                     # marshalled once
 
     def step(stream):
@@ -846,10 +849,20 @@ def unused_config(wl, timed, out):
     wl.step = step
     wl.bytes = (sum(wl.numel[v] * wl.s_in for r in range(wl.W) for v in range(wl.P) if used[r][v])
                 + wl.N * 4 + sum(wl.numel[v] * 4 for v in range(wl.P) if gused[v]))
+
+    def restore():
+        wl.step, wl.bytes = saved_step, saved_bytes
+        wl.red.set_option(_lib.OPT_FIND_UNUSED, 0)
+    return restore
+
+
+def unused_config(wl, timed, out):
+    """find_unused_parameters on BERT-large (see apply_unused), timed as a
+    configuration line."""
+    restore = apply_unused(wl)
     timed(wl, "bert_large_find_unused", "find_unused: pooler unused on every replica, every 4th FFN unused "
           "on replica 1; bytes count only the reads and copy-backs that happen")
-    wl.step, wl.bytes = saved_step, saved_bytes
-    wl.red.set_option(_lib.OPT_FIND_UNUSED, 0)
+    restore()
 
 
 KERNEL_FLAG = {"auto": 2, "ldg": 0, "tma": 1}
@@ -957,6 +970,8 @@ def main():
     ap.add_argument("--driver", default="hooks", choices=["hooks", "events", "all"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "tma"],
                     help="profiling cases: force the bucket-reduce/accumulate kernel")
+    ap.add_argument("--unused", action="store_true",
+                    help="profiling cases: the main workload with unused parameters (find_unused)")
     ap.add_argument("--hook", default="none", choices=["none", "mean", "bf16_compress"],
                     help="profiling cases: reduce the main workload through a built-in hook")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
