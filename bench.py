@@ -669,37 +669,49 @@ def measure_e2e(torch, wl, stream, steps, dist, n_h2d=2, n_d2h=1):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
+        # each step's completion (its last download) is marked on a stream of
+        # its own that only waits and records, so the marks order nothing
+        marker = torch.cuda.Stream(device=stream.device)
         t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
+        done = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         t0.record(stream)
         for i in range(steps):
             pipelined(t0 if i == 0 else None)
-        for ds in d2h_streams:
-            done = torch.cuda.Event()
-            done.record(ds)
-            stream.wait_event(done)
-        t1.record(stream)
+            for ds in d2h_streams:
+                ev = torch.cuda.Event()
+                ev.record(ds)
+                marker.wait_event(ev)
+            done[i].record(marker)
         torch.cuda.synchronize()
-    ms_pipe = t0.elapsed_time(t1) / steps
+    # steady-state period: median interval between consecutive completions
+    # (a step delayed by other traffic on the host link does not skew it)
+    intervals = [done[i - 1].elapsed_time(done[i]) for i in range(1, steps)] or [t0.elapsed_time(done[0])]
+    ms_pipe = statistics.median(intervals)
+    ms_mean = t0.elapsed_time(done[-1]) / steps
     if dist:
         ms_pipe = max_over_ranks(ms_pipe, dist, "cuda")
-    value = wl.bytes / (ms_pipe * 1e-3) / 1e9
-    return {"value": round(value, 2), "unit": "GB/s", "steps": steps,
-            "ms_per_step": round(ms_pipe, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "h2d_gbs": round(h2d / (ms_pipe * 1e-3) / 1e9, 1),
-            "serialized": {"value": round(serial, 2), "ms_per_step": round(ms_step, 3),
-                           "step_ms": {"median": round(ms_step, 3), "min": round(min(per), 3),
-                                       "mean": round(sum(per) / steps, 3), "max": round(max(per), 3)},
-                           "note": "each step starts after the previous one's last download (median step)"},
+        ms_mean = max_over_ranks(ms_mean, dist, "cuda")
+    pipe = wl.bytes / (ms_pipe * 1e-3) / 1e9
+    return {"value": round(serial, 2), "unit": "GB/s", "steps": steps,
+            "ms_per_step": round(ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "step_ms": {"median": round(ms_step, 3), "min": round(min(per), 3), "mean": round(sum(per) / steps, 3),
+                        "max": round(max(per), 3)},
+            "h2d_gbs": round(h2d / (ms_step * 1e-3) / 1e9, 1),
             "host_link": {"h2d_gbs": round(up, 1), "d2h_gbs": round(down, 1), "bound_gbs": round(bound, 1),
-                          "frac_of_bound": round(value / bound, 3),
+                          "frac_of_bound": round(serial / bound, 3),
                           "note": "one pinned whole-buffer copy each way, best of 3, same run; bound = step "
                                   "bytes / max(h2d bytes / h2d rate, d2h bytes / d2h rate)"},
-            "note": ("algorithmic bytes of a step / time per step over consecutive steps, each of which copies the "
-                     "replicas' gradients host->device per bucket, reduces each bucket as it lands "
-                     "(mark_ready_many per bucket) and copies its averaged gradients back; consecutive steps "
-                     "overlap bucket by bucket; pinned host buffers, "
-                     f"{n_h2d} host->device and {n_d2h} device->host copy streams")}
+            "pipelined": {"value": round(pipe, 2), "ms_per_step": round(ms_pipe, 3),
+                          "step_ms": {"median_interval": round(ms_pipe, 3), "min_interval": round(min(intervals), 3),
+                                      "max_interval": round(max(intervals), 3),
+                                      "mean_incl_first_and_tail": round(ms_mean, 3)},
+                          "note": "consecutive steps overlapped bucket by bucket (bucket b's next upload waits for "
+                                  "this step's reduction of b, its next reduction for this step's download of b); "
+                                  "median interval between the completions of consecutive steps"},
+            "note": ("algorithmic bytes of the step / median time of a step that copies the replicas' gradients "
+                     "host->device per bucket, reduces each bucket as it lands (mark_ready_many per bucket) "
+                     f"and copies its averaged gradients back; pinned host buffers, {n_h2d} host->device and "
+                     f"{n_d2h} device->host copy streams")}
 
 
 def extra_configs(torch, device, stream, args, dist, keep):

@@ -335,7 +335,9 @@ int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, fl
 enum ddp_option {
     DDP_OPT_DRY_RUN = 0,          /* 1: run the state machine, launch nothing; ddp_bind records the
                                      pointers without a device table (host tests) */
-    DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 = occupancy maximum */
+    DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 (default) = three times the
+                                     occupancy maximum (three resident waves: SMs that finish a slice early
+                                     take another) */
     DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
     DDP_OPT_BLOCK_THREADS = 3,    /* threads per CTA of the register-streaming kernels: 128 or 256 for
                                      all of them, or 0 (default): 128 for the bucket kernel, 256 for
@@ -348,9 +350,10 @@ enum ddp_option {
     DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB);
                                      raised to 4 KiB per tile for many streams (W > 8, or W > 4 with
                                      a bound last step) */
-    DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernel: CTAs per SM, 1 (default) or 2 */
+    DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernels: CTAs per SM, 1..8, or 0 (default): two resident
+                                     waves (four for the single launch of ddp_reduce_all) */
     DDP_OPT_AUTO_MIN_ELEMS = 8,   /* kernel 2: median bucket length (elements) from which the bulk-copy
-                                     kernel is used (default 2^20) */
+                                     kernel is used (default 6 x 2^20) */
     DDP_OPT_CHAINED = 9,          /* 1: chained launches (default 0).  The caller guarantees that every
                                      gradient of an iteration is final before its first launch and that
                                      nothing else is enqueued on the stream until its last launch (true

@@ -90,15 +90,18 @@ struct ddp_ctx {
     int opt_ctas = 0;
     int opt_block = 0;              // 0: 128 threads for the bucket kernel, 256 for accumulate and hook copies
     // Defaults from the GB300 sweeps: the kernel is chosen per context from
-    // the median bucket length (bulk-copy pipeline with 3 stages of 32 KiB,
-    // one CTA per SM, from 2^20 elements up; register streaming below, where
-    // launches are too small to fill the ring).  One kernel for all launches
-    // of a context, so consecutive launches can overlap.
+    // the median bucket length (bulk-copy pipeline with 3 stages of 32 KiB
+    // from 6 x 2^20 elements up, register streaming below).  Both kernels
+    // launch more CTAs than fit at once (two resident waves for bulk copy,
+    // three for register streaming): SMs that finish a slice early take
+    // another, so a launch ends with a short tail and consecutive launches
+    // interleave.  One kernel for all launches of a context, so consecutive
+    // launches can overlap.
     int opt_kernel = ddpk::KERNEL_AUTO;
     int opt_stages = 3;
     int opt_stage_bytes = 32 * 1024;
-    int opt_tma_ctas = 1;
-    long long opt_auto_min = 1LL << 20;
+    int opt_tma_ctas = 0;           // 0: two resident waves
+    long long opt_auto_min = 6LL << 20;
     bool opt_chain = false;
     int64_t iter_launches = 0;      // launches issued in the current iteration
     void* iter_stream = nullptr;    // stream of the last of them
@@ -227,8 +230,10 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->aux_block = c->opt_block > 0 ? c->opt_block : 256;
     c->cfg.block = block;
     c->cfg.pdl = c->pdl;
+    // default grid: three resident waves (GB300, chained launches: GPT-2-medium
+    // W=8 bf16 at cap 0 6.6 -> 7.0 TB/s against one wave)
     c->cfg.ctas_per_sm = c->opt_ctas > 0 ? c->opt_ctas
-                                         : ddpk::reduce_max_ctas_per_sm(in, c->W, block, c->tab.add != 0);
+                                         : 3 * ddpk::reduce_max_ctas_per_sm(in, c->W, block, c->tab.add != 0);
     if (c->opt_kernel == ddpk::KERNEL_AUTO) {
         std::vector<int64_t> lens;
         for (int32_t b = 0; b < c->B; ++b) lens.push_back(c->bucket_off[b + 1] - c->bucket_off[b]);
@@ -244,6 +249,7 @@ int refresh_launch_cfg(ddp_ctx* c) {
     c->cfg.stages = c->opt_stages;
     c->cfg.stage_bytes = c->opt_stage_bytes;
     c->cfg.tma_ctas_per_sm = c->opt_tma_ctas;
+    c->cfg.tma_waves = 2;
     c->cfg.status = c->tab.status;
 
     c->acc_ctas = c->opt_ctas > 0 ? c->opt_ctas : ddpk::accumulate_max_ctas_per_sm(c->aux_block);
@@ -336,8 +342,9 @@ int hook_range(ddp_ctx* c, int32_t b0, int32_t b1, const ddpk::LaunchCfg& launch
     return DDP_OK;
 }
 
-// One kernel launch over buckets [b0, b1).
-int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
+// One kernel launch over buckets [b0, b1); tma_waves > 0 overrides the
+// bulk-copy kernel's default number of resident waves.
+int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream, int tma_waves = 0) {
     if (c->dry || b1 <= b0) return DDP_OK;
     const long long lo = c->bucket_off[b0], hi = c->bucket_off[b1];
     const int s0 = c->bucket_seg[b0], s1 = c->bucket_seg[b1];
@@ -346,6 +353,7 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream) {
     if (st != DDP_OK) return st;
     const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
     ddpk::LaunchCfg cfg = c->cfg;
+    if (tma_waves > 0) cfg.tma_waves = tma_waves;
     // Chained launches: a launch that directly follows this iteration's
     // previous launch on the same stream need not wait for it when nothing
     // else can sit between them -- always within one API call (the call
@@ -903,7 +911,10 @@ int ddp_reduce_all(ddp_ctx* c, void* stream) {
     }
     c->next = c->B;
     finish_iteration(c);
-    return launch_range(c, first, c->B, stream);
+    // one launch over the whole remaining iteration: four resident waves of
+    // the bulk-copy kernel shorten its tail (two suit the shorter launches of
+    // a readiness-driven iteration)
+    return launch_range(c, first, c->B, stream, 4);
 }
 
 int ddp_get_progress(const ddp_ctx* c, int32_t* next_bucket, int32_t* parked, int32_t* n_parked) {
@@ -1050,7 +1061,8 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             c->opt_stage_bytes = static_cast<int>(value);
             return refresh_launch_cfg(c);
         case DDP_OPT_TMA_CTAS_PER_SM:
-            if (value < 1 || value > 2) return fail(c, DDP_ERR_INVALID_ARG, "bulk-copy CTAs per SM must be 1 or 2");
+            if (value < 0 || value > 8)
+                return fail(c, DDP_ERR_INVALID_ARG, "bulk-copy CTAs per SM must be 0 (two resident waves) .. 8");
             c->opt_tma_ctas = static_cast<int>(value);
             return refresh_launch_cfg(c);
         case DDP_OPT_BLOCK_THREADS:

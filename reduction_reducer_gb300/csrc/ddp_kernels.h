@@ -40,7 +40,8 @@ struct LaunchCfg {
     int kernel;        // KernelKind
     int stages;        // bulk-copy kernel: ring depth
     int stage_bytes;   // bulk-copy kernel: bytes of all replicas' tiles per stage
-    int tma_ctas_per_sm;
+    int tma_ctas_per_sm;        // bulk-copy kernels: CTAs per SM; 0 = tma_waves resident waves
+    int tma_waves;              // resident waves of a bulk-copy launch when tma_ctas_per_sm is 0 (0 = 2)
     int chain;                  // per launch: see pdl_enter in ddp_device.cuh
     int* status;                // device status word of the binding (bulk-copy kernels)
 };
