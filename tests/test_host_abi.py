@@ -498,3 +498,25 @@ def test_host_core_fuzz_matches_oracle(lib, seed):
         order = gen.straggler_order(members, p=0.5, seed=seed)
     assert _run_dry(red, order) == _oracle_trace(members, order)
     red.destroy()
+
+
+def test_launch_shape_options(lib):
+    """Option ranges and defaults of the launch shapes: bulk-copy CTAs per SM
+    0 (resident waves, the default) .. 8, register-streaming CTAs per SM
+    0 (resident waves, the default) .. 64, and the kernel-choice threshold of
+    6 x 2^20 median elements."""
+    from reduction_reducer_gb300 import InvalidArg, _lib as L
+    red = _make([4096] * 8, "f32", 64 << 10)
+    assert red.get_option(L.OPT_TMA_CTAS_PER_SM) == 0
+    assert red.get_option(L.OPT_CTAS_PER_SM) == 0
+    assert red.get_option(L.OPT_AUTO_MIN_ELEMS) == 6 << 20
+    for v in (0, 1, 2, 8):
+        red.set_option(L.OPT_TMA_CTAS_PER_SM, v)
+        assert red.get_option(L.OPT_TMA_CTAS_PER_SM) == v
+    for bad in (-1, 9):
+        with pytest.raises(InvalidArg):
+            red.set_option(L.OPT_TMA_CTAS_PER_SM, bad)
+    for bad in (-1, 65):
+        with pytest.raises(InvalidArg):
+            red.set_option(L.OPT_CTAS_PER_SM, bad)
+    red.destroy()
