@@ -335,9 +335,10 @@ int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, fl
 enum ddp_option {
     DDP_OPT_DRY_RUN = 0,          /* 1: run the state machine, launch nothing; ddp_bind records the
                                      pointers without a device table (host tests) */
-    DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernel: CTAs per SM; 0 (default) = three times the
-                                     occupancy maximum (three resident waves: SMs that finish a slice early
-                                     take another) */
+    DDP_OPT_CTAS_PER_SM = 1,      /* register-streaming kernels: CTAs per SM; 0 (default) = three times the
+                                     bucket kernel's occupancy maximum (three resident waves: SMs that finish
+                                     a slice early take another) and one resident wave of the accumulate
+                                     kernel */
     DDP_OPT_PDL = 2,              /* 1 (default): programmatic dependent launch */
     DDP_OPT_BLOCK_THREADS = 3,    /* threads per CTA of the register-streaming kernels: 128 or 256 for
                                      all of them, or 0 (default): 128 for the bucket kernel, 256 for
