@@ -737,7 +737,7 @@ def extra_configs(torch, device, stream, args, dist, keep):
     timed(wl, "linear_w2", "Linear(10,10), W=2, one mark_ready call per event; latency-bound (one launch)")
     out["linear_w2"]["us_per_step"] = round(out["linear_w2"]["ms_per_step"] * 1e3, 2)
     wl.free()
-    # BERT-large, one persistent launch over all buckets (kernel alone)
+    # BERT-large, one launch over all buckets (kernel alone)
     keep.driver = "all"
     timed(keep, "bert_large_reduce_all", "one reduce_all launch per step")
     # BERT-large, one Python mark_ready call per ready event: each launch waits

@@ -156,7 +156,8 @@ int ddp_mark_ready_many(ddp_ctx* ctx, const int32_t* vars, int32_t n, int32_t* n
 int ddp_reduce_bucket(ddp_ctx* ctx, int32_t bucket, void* stream);
 
 /* Launch every bucket not yet launched in this iteration, in index order, as one
- * persistent kernel launch; the iteration is then finished. */
+ * kernel launch over their whole range (its CTAs each walk their slice of the
+ * segment table); the iteration is then finished. */
 int ddp_reduce_all(ddp_ctx* ctx, void* stream);
 
 /* Cursor and parked set: *next_bucket = index of the next bucket to launch

@@ -15,10 +15,12 @@
 //
 // Both are HBM-streaming kernels (about 0.2 flop per byte): no tensor cores.
 // Design for GB300:
-//   * persistent grid: (SMs x resident CTAs) CTAs, each owning one contiguous,
-//     equal slice of the launch's flat element range, so a bucket range of any
-//     shape (one 125 MiB embedding or hundreds of 1024-element LayerNorm
-//     vectors) costs one launch and balances across all 152 SMs;
+//   * a grid of resident waves (SMs x resident CTAs x waves), each CTA owning
+//     one contiguous, equal slice of the launch's flat element range, so a
+//     bucket range of any shape (one 125 MiB embedding or hundreds of
+//     1024-element LayerNorm vectors) costs one launch and balances across all
+//     152 SMs; with more CTAs than fit at once, SMs that finish a slice early
+//     take another;
 //   * the CTA finds the segment holding its first element with a 32-way
 //     warp-ballot search over the segment offsets, then walks the segments;
 //   * 128-bit loads through the non-coherent path without L1 allocation,

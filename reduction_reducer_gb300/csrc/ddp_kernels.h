@@ -35,7 +35,7 @@ enum KernelKind { KERNEL_LDG = 0, KERNEL_TMA = 1, KERNEL_AUTO = 2 };
 struct LaunchCfg {
     int sms;           // multiprocessors on the device
     int block;         // threads per CTA (register-streaming kernel)
-    int ctas_per_sm;   // persistent CTAs per SM (register-streaming kernel)
+    int ctas_per_sm;   // CTAs per SM of the register-streaming bucket kernel (resident waves x occupancy)
     bool pdl;          // programmatic dependent launch
     int kernel;        // KernelKind
     int stages;        // bulk-copy kernel: ring depth
