@@ -66,3 +66,27 @@ def test_workload_shapes_roundtrip():
     arena, outs, calls = reduce_with_hook(ex["grads"], members, locs, numel, hook_mean)
     assert calls == [(0, 1, True)]
     assert not np.isnan(arena).any()
+
+
+def test_bf16_rounding_matches_library_conversion():
+    """f32 -> bf16 round to nearest even, pinned to a library routine (torch's
+    CPU conversion) over 2^20 random bit patterns of every exponent, exact
+    ties, the overflow edge (values above the largest bf16 round to Inf),
+    subnormals, signed zeros, infinities and NaN (NaN compared as a class).
+    The workloads' input generator rounds the same way."""
+    import torch
+    from workloads.gen import f32_to_bf16_bits
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 1 << 16, size=4096, dtype=np.uint64).astype(np.uint32) << 16) | np.uint32(0x8000)
+    edge = np.array([0x7F7F7FFF, 0x7F7F8000, 0x7F7F8001, 0x7F7FFFFF, 0xFF7FFFFF, 0x00000001, 0x80000001,
+                     0x007FFFFF, 0x00008000, 0x00018000, 0x00000000, 0x80000000, 0x7F800000, 0xFF800000,
+                     0x7FC00000, 0x7F800001, 0xFFFFFFFF], np.uint32)
+    x = np.concatenate([bits, ties, edge]).view(np.float32)
+    want = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(x)
+    for fn in (f32_to_bf16_rne, f32_to_bf16_bits):
+        got = fn(x)
+        assert np.array_equal(got[~nan], want[~nan])
+        # NaN stays NaN: exponent all ones, non-zero mantissa
+        assert np.all((got[nan] & 0x7F80) == 0x7F80) and np.all((got[nan] & 0x007F) != 0)
