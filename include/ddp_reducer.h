@@ -304,11 +304,11 @@ int ddp_bind_last_step(ddp_ctx* ctx, const void* const* g_last);
 /* ---------------------------------------------------------------- no allocation */
 
 /* The fused pass of ddp_reduce_all over every bucket, for callers that may not
- * allocate device memory: code running while a CUDA stream is being captured
- * in a mode that forbids cudaMalloc, code whose framework allocator already
- * owns the device memory budget, and latency-critical loops where an
- * allocation and its implicit device synchronisation are not allowed.  The
- * pages have no counterpart of this call; it exists for such callers.
+ * allocate device memory: a framework whose caching allocator already owns the
+ * device memory budget (a cudaMalloc beside it can fail or fragment what it
+ * holds), and real-time loops where an allocation and the device
+ * synchronisation it implies are not allowed.  The pages have no counterpart
+ * of this call; it exists for such callers.
  *
  * It needs no ddp_bind: the caller passes the replicas' gradients and the
  * outputs exactly as ddp_bind takes them (grads [W*P], bucket_arena, grad_out
@@ -327,6 +327,12 @@ int ddp_bind_last_step(ddp_ctx* ctx, const void* const* g_last);
  *     the status word) and the array keeps the last call's contents; calls
  *     whose work can overlap on the GPU (other streams, other host threads)
  *     race on it.  Calls on one stream are ordered and safe.
+ *   - Launch shape: always the bulk-copy kernel with 3 stages of 32 KiB and
+ *     one CTA per SM; the context's launch options (ddp_set_option) are not
+ *     used.
+ *   - The status word of the kernel's bounded waits lives in the shared array
+ *     and is not reported: ddp_get_device_status reads a bound context's own
+ *     word, not this one.
  * Errors: INVALID_ARG, CUDA. */
 int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_arena,
                            float* const* grad_out, int32_t n_out, void* stream);

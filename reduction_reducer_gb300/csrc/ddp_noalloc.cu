@@ -1,14 +1,15 @@
 // ddp_reduce_all_noalloc: the fused bucket pass over every bucket with no
 // device allocation at all.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA stream is
-// being captured in a mode that forbids it, code whose framework allocator
-// already owns the whole device memory budget, and latency-critical loops
-// where an allocation (and its implicit device synchronisation) is not
-// allowed.  This entry point serves them: the caller passes the gradients
-// and the outputs, and the segment table that the ordinary path keeps in a
+// Some callers cannot call cudaMalloc: a framework whose caching allocator
+// already owns the whole device memory budget, and real-time loops where an
+// allocation (and the device synchronisation it implies) is not allowed.
+// This entry point serves them: the caller passes the gradients and the
+// outputs, and the segment table that the ordinary path keeps in a
 // cudaMalloc'd block (made by ddp_bind) lives instead in a fixed array in the
-// library's static device memory, sized once for every process.
+// library's static device memory, sized once for every process.  The launch
+// shape is fixed (the context's options are not read), and the status word
+// of the kernel's bounded waits is not reported to the caller.
 
 #include <cuda_runtime.h>
 

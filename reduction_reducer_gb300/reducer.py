@@ -241,11 +241,14 @@ class Reducer:
     # ---------------------------------------------------------------- no allocation
     def reduce_all_noalloc(self, grads, bucket_arena, grad_out=None, stream=None):
         """Every bucket in one pass without any device allocation: for callers
-        that may not call cudaMalloc (stream capture that forbids it, a
-        framework allocator owning the memory budget, latency-critical loops).
-        Arguments as in ``bind``; the table goes to the library's static
-        device scratch (256 KiB), shared by all calls.  The first call on a
-        device must come before any stream capture."""
+        that may not call cudaMalloc (a framework whose caching allocator owns
+        the device memory budget, real-time loops where an allocation and the
+        device synchronisation it implies are not allowed).  Arguments as in
+        ``bind``; the table goes to the library's static device scratch
+        (256 KiB), shared by all calls, so calls that can overlap on the GPU
+        race.  The first call on a device looks up the scratch's address and
+        should come before any stream capture.  The context's launch options
+        are not used, and the bounded waits' status is not reported."""
         W = len(grads)
         flat = [_ptr(t) for rep in grads for t in rep]
         if grad_out is None:

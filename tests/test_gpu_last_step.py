@@ -186,10 +186,12 @@ def test_last_step_rules_on_device():
     red.destroy()
 
 
-def test_nosync_resnet50_last_step_full_size_sampled():
+def test_nosync_resnet50_last_step_full_size_every_element():
     """ResNet-50, W = 16, K = 8: seven accumulate micro-steps, then the
-    eighth fused into the reduction; sampled positions against the oracle."""
-    from gpu_util import arena_to_var, sample_positions
+    eighth fused into the reduction; every element of the accumulated fields
+    (left as the seventh step wrote them), the arena and the copy-back
+    against the oracle."""
+    from gpu_util import nosync_full_size_check
     numel = shapes.numels(shapes.resnet50())
     W, K = 16, 8
     offs, total = gen.packed_offsets(numel, 64)
@@ -206,23 +208,5 @@ def test_nosync_resnet50_last_step_full_size_sampled():
     red.bind_last_step(views[K - 1])
     _drive(red, "mark_ready_many", gen.reverse_order(len(numel)))
     assert red.device_status() == 0
-    members, locs = assign_buckets(numel, 4, 25 * MIB)
-    lens = [sum(numel[v] for v in m) for m in members]
-    starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-    pos = sample_positions(numel, locs, starts, n_random=100_000)
-    var, j = arena_to_var(numel, locs, starts, pos)
-    idx = torch.from_numpy(np.array(offs, np.int64)[var] + j).to(DEV)
-    xs = []
-    for r in range(W):
-        per_step = [[steps[k][r].index_select(0, idx).cpu().numpy()] for k in range(K)]
-        a = accumulate_steps(per_step[:K - 1])
-        got_acc = acc_flat[r].index_select(0, idx).cpu().numpy()
-        assert bits_equal(got_acc, a[0]), first_mismatch(got_acc, a[0])      # not written by the reduction
-        xs.append(accumulate(a, per_step[K - 1], first_step=False)[0])
-    want = replica_mean(xs)
-    got = arena.index_select(0, torch.from_numpy(pos).to(DEV)).cpu().numpy()
-    assert bits_equal(got, want), first_mismatch(got, want)
-    got = out_flat.index_select(0, idx).cpu().numpy()
-    assert bits_equal(got, want), first_mismatch(got, want)
-    assert not torch.isnan(arena).any()
     red.destroy()
+    nosync_full_size_check(numel, offs, steps, acc_flat, arena, out_flat, K, True)

@@ -6,9 +6,14 @@ for a tree order (2e-7 relative per element) is not needed.
 
 * small and reduced workloads: every element of the bucket arena and of every
   copied-back gradient against the oracle, plus guard words around them;
-* full-size workloads in the launch configuration the bench times: sampled
-  elements (random positions plus the first and last 40 elements of every
-  parameter) against the oracle computed on exactly those inputs.
+* full-size workloads (BERT-large W=4 in every launch mode, including the
+  bench's own configuration; GPT-2-medium W=8 bf16 at every cap; the no_sync
+  ResNet-50 W=16 K=8 block): every element of the arena, of every copied-back
+  gradient and of the accumulated fields against the oracle run on the same
+  inputs, read back from the device buffers;
+* one tensor of 2^31 + 37 elements (64-bit offsets, not a benchmark
+  configuration): sampled elements, random positions plus the first and last
+  40 elements of every parameter.
 """
 
 import numpy as np
@@ -21,8 +26,8 @@ from oracle.reduce import reduce_buckets, replica_mean
 from reduction_reducer_gb300 import InvalidArg, Reducer, _lib
 from workloads import gen, shapes
 
-from gpu_util import (bits_equal, first_mismatch, host_grads, host_to_device_views, layout,
-                      run_path, sampled_check)
+from gpu_util import (bits_equal, check_every_element, first_mismatch, host_grads, host_to_device_views,
+                      layout, nosync_full_size_check, run_path, sampled_check, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -393,7 +398,7 @@ def test_nosync_small_every_element(kernel):
         assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v])
 
 
-# ---------------------------------------------------------------- full-size workloads, sampled
+# ---------------------------------------------------------------- full-size workloads, every element
 
 def device_replicas(numel, W, dtype, step=0):
     offs, total = gen.packed_offsets(numel, 64)
@@ -402,8 +407,38 @@ def device_replicas(numel, W, dtype, step=0):
     return flat, views, offs
 
 
-def full_size_run(numel, W, dtype, cap, order, mode="mark_ready", kernel="ldg"):
-    flat, views, offs = device_replicas(numel, W, dtype)
+# The inputs of one full-size workload at a time (device buffers drawn by the
+# seeded generator and their host copies), and the oracle's result for one
+# bucket cap at a time: the tests of a workload run back to back and share
+# them.  The kernels never write their inputs.
+_FULL = {}
+
+
+def full_size_inputs(name, numel, W, dtype):
+    key = (name, W, dtype)
+    if key not in _FULL:
+        _FULL.clear()
+        torch.cuda.empty_cache()
+        flat, views, offs = device_replicas(numel, W, dtype)
+        host = [to_host(f, dtype) for f in flat]
+        _FULL[key] = {"flat": flat, "views": views, "offs": offs, "oracle": {},
+                      "host": [[h[o:o + n] for o, n in zip(offs, numel)] for h in host]}
+    return _FULL[key]
+
+
+def oracle_result(inp, numel, dtype, cap):
+    if cap not in inp["oracle"]:
+        inp["oracle"].clear()
+        members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+        inp["oracle"][cap] = reduce_buckets(inp["host"], members, locs, numel)
+    return inp["oracle"][cap]
+
+
+def full_size_run(name, numel, W, dtype, cap, order, mode="mark_ready", kernel="ldg"):
+    """One iteration of a full-size workload through the C ABI, every element
+    of the bucket arena and of the copied-back gradients against the oracle
+    run on the same inputs (read back from the device buffers)."""
+    inp = full_size_inputs(name, numel, W, dtype)
     red = Reducer(numel, dtype, cap)
     if kernel is not None:        # None: the library's defaults
         set_kernel(red, kernel)
@@ -411,48 +446,51 @@ def full_size_run(numel, W, dtype, cap, order, mode="mark_ready", kernel="ldg"):
     out_offs, out_total = gen.packed_offsets(numel, 64)
     out_flat = torch.full((out_total,), float("nan"), device=DEV)
     outs = [out_flat[o:o + n] for o, n in zip(out_offs, numel)]
-    run_path(red, views, arena, outs, order=order, mode=mode)
-    n = sampled_check(numel, dtype, W, cap, flat, offs, arena, [(out_flat, out_offs)], 1)
-    assert not torch.isnan(arena).any(), "arena not fully written"
+    run_path(red, inp["views"], arena, outs, order=order, mode=mode)
     assert red.device_status() == 0
+    launches = red.launch_count()
     red.destroy()
-    return n
+    want_arena, want_outs = oracle_result(inp, numel, dtype, cap)
+    check_every_element(numel, want_arena, want_outs, arena, out_flat, out_offs)
+    return launches
+
+
+def bert_order():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "bert_large_ready_order.txt")
+    return [int(l) for l in open(path) if l.strip() and not l.startswith("#")]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_bert_large_full_size_sampled(kernel):
-    import os
+def test_bert_large_full_size_every_element(kernel):
     numel = shapes.numels(shapes.bert_large())
-    path = os.path.join(os.path.dirname(__file__), "golden", "bert_large_ready_order.txt")
-    order = [int(l) for l in open(path) if l.strip() and not l.startswith("#")]
-    assert full_size_run(numel, 4, "f32", 25 * MIB, order, kernel=kernel) > 100_000
+    full_size_run("bert_large", numel, 4, "f32", 25 * MIB, bert_order(), kernel=kernel)
 
 
 def test_bert_large_full_size_bench_configuration():
     """Exactly what bench.py times: library defaults, the stored straggler
     order reported in one mark_ready_many call, one copy-back."""
-    import os
     numel = shapes.numels(shapes.bert_large())
-    path = os.path.join(os.path.dirname(__file__), "golden", "bert_large_ready_order.txt")
-    order = [int(l) for l in open(path) if l.strip() and not l.startswith("#")]
-    assert full_size_run(numel, 4, "f32", 25 * MIB, order, mode="mark_ready_many", kernel=None) > 100_000
+    n = full_size_run("bert_large", numel, 4, "f32", 25 * MIB, bert_order(), mode="mark_ready_many", kernel=None)
+    assert n == 35          # 37 buckets in 35 launches: two parked buckets go out with the ones that release them
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bert_large_full_size_reduce_all(kernel):
+    numel = shapes.numels(shapes.bert_large())
+    full_size_run("bert_large", numel, 4, "f32", 25 * MIB, None, mode="reduce_all", kernel=kernel)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("cap_mib", [0, 1, 5, 25, 100])
-def test_gpt2_medium_full_size_sampled(cap_mib, kernel):
+def test_gpt2_medium_full_size_every_element(cap_mib, kernel):
     numel = shapes.numels(shapes.gpt2_medium())
-    assert full_size_run(numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel)), kernel=kernel,
-                         mode="mark_ready_many") > 100_000
+    full_size_run("gpt2_medium", numel, 8, "bf16", cap_mib * MIB, gen.reverse_order(len(numel)), kernel=kernel,
+                  mode="mark_ready_many")
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_bert_large_full_size_reduce_all_sampled(kernel):
-    numel = shapes.numels(shapes.bert_large())
-    full_size_run(numel, 4, "f32", 25 * MIB, None, mode="reduce_all", kernel=kernel)
-
-
-def test_nosync_resnet50_full_size_sampled():
+def test_nosync_resnet50_full_size_every_element():
+    _FULL.clear()
     numel = shapes.numels(shapes.resnet50())
     W, K = 16, 8
     steps = [device_replicas(numel, W, "f32", step=k) for k in range(K)]
@@ -467,28 +505,11 @@ def test_nosync_resnet50_full_size_sampled():
     for k in range(K):
         red.accumulate_nosync(acc, steps[k][1], first_step=(k == 0))
     red.begin_iteration()
-    for v in gen.reverse_order(len(numel)):
-        red.mark_ready(v)
+    red.mark_ready_many(gen.reverse_order(len(numel)))
     torch.cuda.synchronize()
-    # oracle on sampled positions: accumulate the K draws, then the mean
-    members, locs = assign_buckets(numel, 4, 25 * MIB)
-    lens = [sum(numel[v] for v in m) for m in members]
-    starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-    from gpu_util import arena_to_var, sample_positions
-    pos = sample_positions(numel, locs, starts, n_random=100_000)
-    var, j = arena_to_var(numel, locs, starts, pos)
-    idx = torch.from_numpy(np.array(offs, np.int64)[var] + j).to(DEV)
-    accs = []
-    for r in range(W):
-        per_step = [[steps[k][0][r].index_select(0, idx).cpu().numpy()] for k in range(K)]
-        accs.append(accumulate_steps(per_step)[0])
-        got_acc = acc_flat[r].index_select(0, idx).cpu().numpy()
-        assert bits_equal(got_acc, accs[r]), first_mismatch(got_acc, accs[r])
-    want = replica_mean(accs)
-    got = arena.index_select(0, torch.from_numpy(pos).to(DEV)).cpu().numpy()
-    assert bits_equal(got, want), first_mismatch(got, want)
-    got = out_flat.index_select(0, idx).cpu().numpy()
-    assert bits_equal(got, want), first_mismatch(got, want)
+    assert red.device_status() == 0
+    red.destroy()
+    nosync_full_size_check(numel, offs, [[f for f in s[0]] for s in steps], acc_flat, arena, out_flat, K, False)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -496,7 +517,19 @@ def test_largest_tensor_64bit_offsets(kernel):
     """One tensor of 2^31 + 37 bf16 elements (past 32-bit indexing) behind a
     small one, W = 2: sampled check including both ends."""
     numel = [1000, (1 << 31) + 37]
-    full_size_run(numel, 2, "bf16", 25 * MIB, [1, 0], kernel=kernel)
+    _FULL.clear()
+    torch.cuda.empty_cache()
+    flat, views, offs = device_replicas(numel, 2, "bf16")
+    red = Reducer(numel, "bf16", 25 * MIB)
+    set_kernel(red, kernel)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    out_offs, out_total = gen.packed_offsets(numel, 64)
+    out_flat = torch.full((out_total,), float("nan"), device=DEV)
+    run_path(red, views, arena, [out_flat[o:o + n] for o, n in zip(out_offs, numel)], order=[1, 0])
+    assert sampled_check(numel, "bf16", 2, 25 * MIB, flat, offs, arena, [(out_flat, out_offs)], 1) > 100_000
+    assert not torch.isnan(arena).any(), "arena not fully written"
+    assert red.device_status() == 0
+    red.destroy()
 
 
 def test_automatic_kernel_choice():

@@ -163,9 +163,11 @@ def test_unused_with_nosync_bitmap(kernel):
     _check_outputs(bufs, out_offs, numel, want_outs, has)
 
 
-def test_unused_bert_large_full_size_sampled():
+def test_unused_bert_large_full_size_every_element():
     """BERT-large W=4 in the bench's layout: the pooler unused on every
-    replica, every fourth encoder layer's FFN unused on replica 1."""
+    replica, every fourth encoder layer's FFN unused on replica 1; every
+    element of the arena and of the copy-back (untouched where the variable
+    is unused everywhere) against the oracle."""
     numel = shapes.numels(shapes.bert_large())
     names = [n for n, _ in shapes.bert_large()]
     P, W = len(numel), 4
@@ -192,19 +194,19 @@ def test_unused_bert_large_full_size_sampled():
     red.mark_ready_many([v for v in range(P - 1, -1, -1) if g[v]])
     torch.cuda.synchronize()
     assert red.device_status() == 0
-    # sampled positions of every variable: first / last 40 elements + random
-    rng = np.random.default_rng(9)
+    members, locs = assign_buckets(numel, 4, 25 * MIB)
+    host = [f.cpu().numpy() for f in flat]
+    want_arena, want_outs = reduce_with_unused([[h[o:o + n] for o, n in zip(offs, numel)] for h in host],
+                                               used.tolist(), members, locs, numel)
+    del host
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    got = out_flat.cpu().numpy()
     for v in range(P):
         n = numel[v]
-        pos = np.unique(np.concatenate([np.arange(min(40, n)), np.arange(max(0, n - 40), n),
-                                        rng.integers(0, n, size=min(n, 2000))]))
-        idx = torch.from_numpy(offs[v] + pos).to(DEV)
-        xs = [(flat[r].index_select(0, idx).cpu().numpy() if used[r, v] else np.zeros(pos.size, np.float32))
-              for r in range(W)]
-        want = replica_mean(xs)
-        got = out_flat.index_select(0, idx).cpu().numpy()
-        if g[v]:
-            assert bits_equal(got, want), (v, first_mismatch(got, want))
+        if want_outs[0][v] is None:
+            assert np.all(got[offs[v]:offs[v] + n].view(np.uint32) == GUARD), v
         else:
-            assert np.all(got.view(np.uint32) == GUARD)
+            assert bits_equal(got[offs[v]:offs[v] + n], want_outs[0][v]), (v, first_mismatch(got[offs[v]:offs[v] + n], want_outs[0][v]))
     assert not torch.isnan(arena).any()
+    red.destroy()

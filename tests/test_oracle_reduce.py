@@ -176,3 +176,73 @@ def test_replicas_identical_after_step(W):
     # ... whereas stepping on the local (unreduced) gradients diverges
     local = [sgd_step(start, ex["grads"][r], 0.001) for r in range(W)]
     assert not np.array_equal(local[0][0], local[1][0])
+
+
+def _f32_from_bits(u):
+    return np.array([u], np.uint32).view(np.float32)
+
+
+def test_sgd_step_hand_derived():
+    """The SGD update p <- fl32(p - fl32(lr * g)) of the worked example (lr
+    0.001, "Distributed Data Parallel" notes, "Example"), on values derived
+    by hand; each case is chosen so that a flipped sign, a dropped or
+    mis-scaled learning rate, or a missing product rounding changes the bits.
+
+    fl32(0.001) = 0x3A83126F = 8589935 * 2^-33.
+    (a) p = 1, g = 2^-10: lr*g = 8589935 * 2^-43 exactly (power-of-two
+        scale); 1 - that lies 16.384 units of 2^-24 below 1, so the result
+        is 1 - 16 * 2^-24 = 1 - 2^-20 = 0x3F7FFFF0.  p + lr*g would give
+        1 + 2^-20 = 0x3F800008, dropping lr 1 - 2^-10 = 0x3F7FC000.
+    (b) p = 2^-10, g = 3: lr*g = 25769805 * 2^-33 = 12884902.5 * 2^-32, a
+        tie between mantissas 12884902 and 12884903; ties go to the even
+        one, so fl32(lr*g) = 12884902 * 2^-32 = 0x3B449BA6, and
+        p - it = (4194304 - 12884902) * 2^-32 = -8690598 * 2^-32, exact:
+        0xBB049BA6.
+    """
+    got = sgd_step([np.array([1.0], F32)], [np.array([2.0 ** -10], F32)], 0.001)[0]
+    assert got.view(np.uint32)[0] == 0x3F7FFFF0
+    for wrong in (0x3F800008, 0x3F7FC000):
+        assert got.view(np.uint32)[0] != wrong
+    got = sgd_step([np.array([2.0 ** -10], F32)], [np.array([3.0], F32)], 0.001)[0]
+    assert got.view(np.uint32)[0] == 0xBB049BA6
+    # the product's rounding, checked on its own: fl32(0.001 * 3) is the even
+    # neighbour of the tie
+    assert (F32(0.001) * F32(3.0)).view(np.uint32) == 0x3B449BA6
+    assert _f32_from_bits(0x3B449BA6)[0] == F32(12884902 * 2.0 ** -32)
+
+
+def _round_f32(q: Fraction) -> np.float32:
+    """Nearest fp32 to a rational in the normal range, ties to even, from
+    integer arithmetic alone (exponent by comparison, scaled mantissa)."""
+    if q == 0:
+        return F32(0.0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = 0
+    while a >= 2:
+        a /= 2
+        e += 1
+    while a < 1:
+        a *= 2
+        e -= 1
+    m = a * (1 << 23)                    # in [2^23, 2^24)
+    lo = m.numerator // m.denominator
+    rem = m - lo
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1):
+        lo += 1
+    return F32(sign * lo * 2.0 ** (e - 23))
+
+
+def test_sgd_step_against_exact_rationals():
+    """Seeded parameters and gradients of mixed magnitude: each result equals
+    two correctly rounded steps of exact rational arithmetic -- the product
+    lr*g rounded to fp32, then p minus it rounded to fp32."""
+    rng = np.random.default_rng(7)
+    p = (rng.standard_normal(400) * rng.choice([1e-3, 1.0, 30.0], 400)).astype(F32)
+    g = (rng.standard_normal(400) * rng.choice([1e-6, 1e-3, 1.0], 400)).astype(F32)
+    got = sgd_step([p], [g], 0.001)[0]
+    lr = Fraction(float(F32(0.001)))
+    for i in range(400):
+        prod = _round_f32(lr * Fraction(float(g[i])))
+        want = _round_f32(Fraction(float(p[i])) - Fraction(float(prod)))
+        assert got[i].view(np.uint32) == want.view(np.uint32), (i, got[i], want)

@@ -1,13 +1,15 @@
-"""The no-allocation entry point, checked against the ordinary one.
+"""The no-allocation entry point, checked against the ordinary one and
+against the oracle.
 
-``ddp_reduce_all_noalloc`` serves callers that may not call cudaMalloc
-(stream capture that forbids it, a framework allocator that owns the
-memory budget, latency-critical loops): its segment table lives in the
-library's static device scratch instead of memory allocated by ddp_bind.
-Here it must give bit for bit what ``ddp_reduce_all`` on a bound context
-gives, on two calls in a row (the second with other inputs and another
-layout, so nothing of the first call's table leaks into it), and it must
-refuse a layout whose table does not fit the scratch.
+``ddp_reduce_all_noalloc`` serves callers that may not call cudaMalloc (a
+framework whose caching allocator owns the device memory budget, real-time
+loops where an allocation and the device synchronisation it implies are not
+allowed): its segment table lives in the library's static device scratch
+instead of memory allocated by ddp_bind.  Here it must give bit for bit what
+``ddp_reduce_all`` on a bound context gives, and what the CPU oracle computes
+from the same inputs, on two calls in a row (the second with other inputs
+and another layout, so nothing of the first call's table leaks into it), and
+it must refuse a layout whose table does not fit the scratch.
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test; it also passes on its own in a
@@ -18,6 +20,8 @@ import numpy as np
 import pytest
 import torch
 
+from oracle.buckets import assign_buckets
+from oracle.reduce import reduce_buckets
 from reduction_reducer_gb300 import InvalidArg, Reducer
 from workloads import gen, shapes
 
@@ -62,6 +66,15 @@ def _case(numel, W, dtype, cap, n_out, seed_step):
         for v in range(len(numel)):
             assert torch.equal(copies[o][v].view(torch.int32), ref_copies[o][v].view(torch.int32)), (o, v)
     assert not torch.isnan(arena).any()
+    # and against the oracle on the same inputs, read back from the device
+    host = [f.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else f.cpu().numpy() for f in flat]
+    members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+    want_arena, want_outs = reduce_buckets([[h[o:o + n] for o, n in zip(offs, numel)] for h in host],
+                                           members, locs, numel)
+    assert np.array_equal(arena.cpu().numpy().view(np.uint32), want_arena.view(np.uint32))
+    for o in range(n_out):
+        for v in range(len(numel)):
+            assert np.array_equal(copies[o][v].cpu().numpy().view(np.uint32), want_outs[0][v].view(np.uint32)), (o, v)
     red.destroy()
 
 
