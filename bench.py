@@ -513,9 +513,10 @@ def run_ours(args):
                        "l2": (f"no flush: each step streams {wl.bytes / 1e9:.1f} GB, inputs "
                               f"{wl.W * wl.N * wl.s_in / 1e9:.1f} GB > 129 MB L2"),
                        "parallelism": f"replicas only x{world}",
-                       **({"profiling": {"kernel": args.kernel, "hook": args.hook, "unused": args.unused}}
+                       **({"profiling": {"kernel": args.kernel, "hook": args.hook, "hook_route": args.hook_route,
+                                         "unused": args.unused}}
                           if args.kernel != "auto" or args.hook != "none" or args.unused else {})},
-            "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+            "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2), "pct_of_measured_copy_bw": round(100 * gbs / peak, 2),
             "grad_elems_per_s": round(elems * world, 1),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": timed_launches * world,
             "clocks": clocks, "per_config": extra,
@@ -727,7 +728,7 @@ def extra_configs(torch, device, stream, args, dist, keep):
         gbs = wl.bytes / (t * 1e-3) / 1e9
         peak, _ = peaks()
         out[key] = {"gbs": round(gbs, 1), "ms_per_step": round(t, 4),
-                    "pct_of_peak": round(100 * gbs / peak, 2), "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                    "pct_of_nominal_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2), "pct_of_measured_copy_bw": round(100 * gbs / peak, 2),
                     "bytes_per_step": wl.bytes, "buckets": wl.B, "W": wl.W, "kernel": kernel_name(wl),
                     "grad_elems_per_s": round(wl.W * wl.N / (t * 1e-3), 1), "note": note}
 
@@ -806,27 +807,41 @@ def graph_config(torch, wl, stream, steps, warm, dist, out, key):
 
 
 def hook_config(torch, device, keep, timed, out):
-    """The communication-hook path (unfused): every bucket is gathered into
-    W replica bucket buffers, reduced by the built-in mean hook and copied
-    back.  Reported against the fused pass's algorithmic bytes (what the
-    iteration must move) and against the bytes the three passes move."""
+    """The communication-hook path on BERT-large W=4.  A registered built-in
+    hook runs inside the fused bucket pass by default (mean, and the bf16
+    compression hook); the gather, hook call and copy-back route is timed
+    beside it, reported against the fused pass's algorithmic bytes (what the
+    iteration must move) and against the bytes its three passes move."""
+    from reduction_reducer_gb300 import _lib
+    for hook in ("mean", "bf16_compress"):
+        wl = Workload("bert_large", torch, device, 25, n_out=1, driver="hooks")
+        rb = [torch.empty(wl.red.arena_numel(), dtype=torch.float32, device=device) for _ in range(wl.W)]
+        wl.red.register_comm_hook(hook, rb)
+        timed(wl, f"bert_large_hook_{hook}", f"register_comm_hook('{hook}'): the hook's arithmetic inside the fused "
+              "bucket pass (one launch per readiness event, nothing gathered), W*N*4 + 2*N*4 bytes")
+        wl.free()
+        del rb
+        torch.cuda.empty_cache()
     wl = Workload("bert_large", torch, device, 25, n_out=1, driver="hooks")
     rb = [torch.empty(wl.red.arena_numel(), dtype=torch.float32, device=device) for _ in range(wl.W)]
     wl.red.register_comm_hook("mean", rb)
-    timed(wl, "bert_large_hook_mean", "register_comm_hook('mean'): gather + hook + copy-back per bucket; "
-          "gbs uses the fused pass's algorithmic bytes")
+    wl.red.set_option(_lib.OPT_HOOK_FUSED, 0)
+    timed(wl, "bert_large_hook_mean_gathered", "register_comm_hook('mean') with DDP_OPT_HOOK_FUSED = 0: gather + "
+          "hook call + copy-back per bucket; gbs uses the fused pass's algorithmic bytes")
     moved = 2 * wl.W * wl.N * 4 + wl.W * wl.N * 4 + wl.N * 4 + 2 * wl.N * 4
-    out["bert_large_hook_mean"]["bytes_moved_per_step"] = moved
-    out["bert_large_hook_mean"]["moved_gbs"] = round(moved / (out["bert_large_hook_mean"]["ms_per_step"] * 1e-3) / 1e9, 1)
+    out["bert_large_hook_mean_gathered"]["bytes_moved_per_step"] = moved
+    out["bert_large_hook_mean_gathered"]["moved_gbs"] = round(
+        moved / (out["bert_large_hook_mean_gathered"]["ms_per_step"] * 1e-3) / 1e9, 1)
     wl.free()
     del rb
     torch.cuda.empty_cache()
-    # the same hook on gradients that are views of the bucket layout: the hook
-    # reads them in place, nothing is gathered and nothing copied back
+    # the hook-call route on gradients that are views of the bucket layout:
+    # the hook reads them in place, nothing is gathered and nothing copied back
     wl = Workload("bert_large", torch, device, 25, n_out=0, driver="hooks", layout="buckets")
     wl.red.register_comm_hook("mean", None)
-    timed(wl, "bert_large_hook_mean_as_view", "register_comm_hook('mean', replica_buffers=None) on bucket views: "
-          "the hook's mean per bucket, W*N*4 + N*4 bytes")
+    wl.red.set_option(_lib.OPT_HOOK_FUSED, 0)
+    timed(wl, "bert_large_hook_mean_as_view", "register_comm_hook('mean', replica_buffers=None) on bucket views, "
+          "hook-call route: the hook's mean per bucket, W*N*4 + N*4 bytes")
     wl.free()
     torch.cuda.empty_cache()
 
@@ -892,6 +907,7 @@ def profiling_setup(torch, device, red, args, W):
     tdt = torch.float32 if red.dtype == "f32" else torch.bfloat16
     bufs = [torch.empty(max(red.arena_numel(), 1), dtype=tdt, device=device) for _ in range(W)]
     red.register_comm_hook(args.hook, bufs)
+    red.set_option(_lib.OPT_HOOK_FUSED, 1 if args.hook_route == "fused" else 0)
     return bufs
 
 
@@ -986,6 +1002,8 @@ def main():
                     help="profiling cases: the main workload with unused parameters (find_unused)")
     ap.add_argument("--hook", default="none", choices=["none", "mean", "bf16_compress"],
                     help="profiling cases: reduce the main workload through a built-in hook")
+    ap.add_argument("--hook-route", default="fused", choices=["fused", "gathered"],
+                    help="profiling cases: --hook inside the fused pass or through gather + hook call + copy-back")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--cpu-config-s", type=float, default=2.0,
                     help="seconds of oracle work per configuration (per_config cpu_oracle)")

@@ -239,14 +239,21 @@ typedef int (*ddp_comm_hook_fn)(void* state, const ddp_grad_bucket* bucket, void
  *                    bases (the gradients themselves; NULL for a bucket without
  *                    elements), and a launch whose bound gradients no longer
  *                    form such views fails with INVALID_ARG.
- * W <= 64; not with DDP_OPT_FIND_UNUSED or a bound last step.
+ * W <= 64; not with DDP_OPT_FIND_UNUSED or a bound last step.  The two
+ * built-in hooks below keep the fused pass instead (DDP_OPT_HOOK_FUSED): the
+ * buffers are then left as they are, and the view check is not made.
  * Errors: INVALID_ARG, NOT_BOUND. */
 int ddp_register_comm_hook(ddp_ctx* ctx, ddp_comm_hook_fn hook, void* state, void* const* replica_buffers);
 
 /* Built-in hooks (state unused): the default, the rank-order fp32 mean of the
  * replicas' buffers x fl32(1/W) -- the fused pass's arithmetic -- and a
  * compression variant that first rounds every replica value to bf16 (round to
- * nearest even), i.e. averages what a bf16 wire would carry. */
+ * nearest even), i.e. averages what a bf16 wire would carry.  Registered on a
+ * context, they are not called per bucket: with DDP_OPT_HOOK_FUSED (default)
+ * their arithmetic runs inside the fused bucket pass, which reads the bound
+ * gradients where they lie, so the replica buffers are neither needed nor
+ * written and the result equals the gather, hook, copy-back route bit for
+ * bit.  Called directly, they launch their mean on `stream` as any hook. */
 int ddp_hook_mean(void* state, const ddp_grad_bucket* bucket, void* stream);
 int ddp_hook_bf16_compress(void* state, const ddp_grad_bucket* bucket, void* stream);
 
@@ -372,9 +379,14 @@ enum ddp_option {
                                      work after the iteration. */
     DDP_OPT_QUERY_KERNEL = 10,    /* read only (ddp_get_option): kernel the bound context launches,
                                      0 or 1; -1 before ddp_bind */
-    DDP_OPT_FIND_UNUSED = 11      /* 1: track unused parameters (find_unused_parameters; default 0):
+    DDP_OPT_FIND_UNUSED = 11,     /* 1: track unused parameters (find_unused_parameters; default 0):
                                      enables ddp_set_local_used and the local-use bits of
                                      ddp_accumulate_nosync_used; segments are never merged; W <= 64 */
+    DDP_OPT_HOOK_FUSED = 12       /* 1 (default): a registered built-in hook (ddp_hook_mean,
+                                     ddp_hook_bf16_compress) runs inside the fused bucket pass -- one
+                                     launch per released bucket range, nothing gathered into the replica
+                                     buffers, no separate copy-back; 0: the gather, hook call and
+                                     copy-back route of every other hook.  Between iterations only. */
 };
 int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
 int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);

@@ -204,18 +204,31 @@ __device__ __forceinline__ bool any_replica(unsigned long long mk, int W) {
     return W >= 64 ? mk != 0ull : (mk & ((1ull << W) - 1ull)) != 0ull;
 }
 
+// fp32 -> bf16 with round to nearest even, widened back to fp32 (a NaN stays
+// a quiet NaN; values past the largest bf16 round to infinity).  Integer
+// arithmetic on the bit pattern: add half an ulp of bf16 (less one when the
+// kept bit is even, so ties go to even), then drop the low 16 bits.
+__device__ __forceinline__ float round_bf16(float x) {
+    const uint32_t u = __float_as_uint(x);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return __uint_as_float((u | 0x00400000u) & 0xffff0000u);
+    const uint32_t r = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
+    return __uint_as_float(r);
+}
+
 // Replica r's input at segment element j: its gradient, or with ADD (fused
 // last micro-step) fl32(accumulated + last-step gradient), whose pointers
-// are src[r] and src[W + r].
-template <bool ADD, typename Tin>
+// are src[r] and src[W + r]; with CMP (the bf16-compression hook fused into
+// the pass) the fp32 value rounded to bf16 first.
+template <bool ADD, bool CMP = false, typename Tin>
 __device__ __forceinline__ float replica_in(const Tin* const* src, int W, int r, long long j) {
     if constexpr (ADD) return __fadd_rn(widen1(src[r][j]), widen1(src[W + r][j]));
+    else if constexpr (CMP) return round_bf16(widen1(src[r][j]));
     else return widen1(src[r][j]);
 }
 
 // Rank-order fp32 mean of one element, scalar path (heads, tails, segments
 // whose pointers do not share the arena's 16-byte phase).
-template <typename Tin, bool ADD = false>
+template <typename Tin, bool ADD = false, bool CMP = false>
 __device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* const* src,
                                               float* const* dst, long long a0, long long x,
                                               long long e, int W, int tid, int nthr,
@@ -223,8 +236,9 @@ __device__ __forceinline__ void reduce_scalar(const ReduceParams& p, const Tin* 
     const bool write_dst = any_replica(mk, W);
     for (long long a = x + tid; a < e; a += nthr) {
         const long long j = a - a0;
-        float acc = has_replica(mk, 0) ? replica_in<ADD>(src, W, 0, j) : 0.0f;
-        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, has_replica(mk, r) ? replica_in<ADD>(src, W, r, j) : 0.0f);
+        float acc = has_replica(mk, 0) ? replica_in<ADD, CMP>(src, W, 0, j) : 0.0f;
+        for (int r = 1; r < W; ++r)
+            acc = __fadd_rn(acc, has_replica(mk, r) ? replica_in<ADD, CMP>(src, W, r, j) : 0.0f);
         const float m = __fmul_rn(acc, p.inv_w);
         p.arena[a] = m;
         if (write_dst)

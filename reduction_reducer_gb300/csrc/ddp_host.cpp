@@ -67,6 +67,8 @@ struct ddp_ctx {
     void* hook_state = nullptr;
     std::vector<void*> hook_rb;                   // W replica bucket buffers (empty: gradients are bucket views)
     bool hook_alias = false;                      // the hook reads the gradients in place
+    int hook_builtin = 0;                         // 1: ddp_hook_mean, 2: ddp_hook_bf16_compress, 0: another hook
+    bool opt_hook_fused = true;                   // built-in hooks run inside the fused bucket pass
 
     // ---- binding
     bool bound = false;
@@ -361,7 +363,13 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream, int tma_waves
     // opted in (DDP_OPT_CHAINED).
     const bool follows_own = c->iter_launches > 0 && stream == c->iter_stream;
     cfg.chain = c->pdl && follows_own && (c->call_launches > 0 || c->opt_chain) ? 1 : 0;
-    if (c->hook) return hook_range(c, b0, b1, cfg, stream);
+    // A built-in hook's arithmetic is the fused pass's (the default hook) or
+    // the fused pass with every replica value rounded to bf16 first (the
+    // compression hook): it runs inside the one-pass kernel, with nothing
+    // gathered into the replica buffers and no separate copy-back.
+    const bool fused_hook = c->hook && c->hook_builtin != 0 && c->opt_hook_fused;
+    if (c->hook && !fused_hook) return hook_range(c, b0, b1, cfg, stream);
+    cfg.compress = fused_hook && c->hook_builtin == 2 && c->dtype == DDP_F32 ? 1 : 0;
     if (!c->iter_masked) {
         long long n = 0;
         cudaError_t e = ddpk::launch_reduce(c->tab, in, c->W, c->n_out, c->arena, lo, hi, s0, s1, c->inv_w,
@@ -761,6 +769,7 @@ int ddp_register_comm_hook(ddp_ctx* c, ddp_comm_hook_fn hook, void* state, void*
     c->hook_state = state;
     c->hook_rb = std::move(rb);
     c->hook_alias = alias;
+    c->hook_builtin = hook == &ddp_hook_mean ? 1 : hook == &ddp_hook_bf16_compress ? 2 : 0;
     return DDP_OK;
 }
 
@@ -1026,6 +1035,10 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
         case DDP_OPT_CHAINED:
             c->opt_chain = value != 0;
             return DDP_OK;
+        case DDP_OPT_HOOK_FUSED:
+            if (c->active) return fail(c, DDP_ERR_INVALID_ARG, "the hook route changes between iterations only");
+            c->opt_hook_fused = value != 0;
+            return DDP_OK;
         case DDP_OPT_QUERY_KERNEL:
             return fail(c, DDP_ERR_INVALID_ARG, "DDP_OPT_QUERY_KERNEL is read with ddp_get_option");
         case DDP_OPT_FIND_UNUSED: {
@@ -1149,6 +1162,7 @@ int ddp_get_option(const ddp_ctx* c, int32_t option, int64_t* value) {
         case DDP_OPT_CHAINED: *value = c->opt_chain; return DDP_OK;
         case DDP_OPT_QUERY_KERNEL: *value = c->bound ? c->cfg.kernel : -1; return DDP_OK;
         case DDP_OPT_FIND_UNUSED: *value = c->opt_find_unused; return DDP_OK;
+        case DDP_OPT_HOOK_FUSED: *value = c->opt_hook_fused; return DDP_OK;
         default: return DDP_ERR_INVALID_ARG;
     }
 }

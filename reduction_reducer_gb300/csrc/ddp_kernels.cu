@@ -72,8 +72,9 @@ __device__ __forceinline__ Raw zero_raw() { return Raw{}; }
 // Vector body, W known at compile time: all NS x U loads in flight at once
 // (NS = WC streams, or 2 WC with ADD: the accumulated fields and the last
 // micro-step's gradients).  Replica r's input is its vector, or with ADD
-// fl32(acc_r + g_r), added into the rank-order sum.
-template <typename Tin, int WC, int U, bool ADD>
+// fl32(acc_r + g_r), or with CMP its vector rounded to bf16, added into the
+// rank-order sum.
+template <typename Tin, int WC, int U, bool ADD, bool CMP>
 __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Tin* const* src,
                                                  float* const* dst, long long a0, long long kb,
                                                  long long ke, unsigned long long mk) {
@@ -110,6 +111,10 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
 #pragma unroll
                     for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
                 }
+                if constexpr (CMP) {
+#pragma unroll
+                    for (int q = 0; q < N; ++q) acc[q] = round_bf16(acc[q]);
+                }
 #pragma unroll
                 for (int r = 1; r < WC; ++r) {
                     V::unpack(raw[u][r], f);
@@ -118,6 +123,10 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
                         V::unpack(raw[u][WC + r], h);
 #pragma unroll
                         for (int q = 0; q < N; ++q) f[q] = __fadd_rn(f[q], h[q]);
+                    }
+                    if constexpr (CMP) {
+#pragma unroll
+                        for (int q = 0; q < N; ++q) f[q] = round_bf16(f[q]);
                     }
 #pragma unroll
                     for (int q = 0; q < N; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
@@ -130,8 +139,9 @@ __device__ __forceinline__ void reduce_vec_fixed(const ReduceParams& p, const Ti
     }
 }
 
-// One replica's 16-byte vector of inputs (ADD: accumulated + last step).
-template <typename Tin, bool ADD>
+// One replica's 16-byte vector of inputs (ADD: accumulated + last step;
+// CMP: rounded to bf16).
+template <typename Tin, bool ADD, bool CMP>
 __device__ __forceinline__ void load_replica(const Tin* const* src, int W, int r, long long j,
                                              unsigned long long mk, float (&f)[Vec<Tin>::N]) {
     using V = Vec<Tin>;
@@ -147,10 +157,14 @@ __device__ __forceinline__ void load_replica(const Tin* const* src, int W, int r
 #pragma unroll
         for (int q = 0; q < V::N; ++q) f[q] = __fadd_rn(f[q], h[q]);
     }
+    if constexpr (CMP) {
+#pragma unroll
+        for (int q = 0; q < V::N; ++q) f[q] = round_bf16(f[q]);
+    }
 }
 
 // Vector body for any W: replicas in groups of 4, still summed in rank order.
-template <typename Tin, bool ADD>
+template <typename Tin, bool ADD, bool CMP>
 __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin* const* src,
                                                float* const* dst, long long a0, long long kb,
                                                long long ke, int W, unsigned long long mk) {
@@ -160,12 +174,12 @@ __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin*
     for (long long k = kb + threadIdx.x; k < ke; k += blockDim.x) {
         const long long j = k * N - a0;
         float acc[N];
-        load_replica<Tin, ADD>(src, W, 0, j, mk, acc);
+        load_replica<Tin, ADD, CMP>(src, W, 0, j, mk, acc);
         for (int r = 1; r < W; r += 4) {
             float f[4][N];
 #pragma unroll
             for (int g = 0; g < 4; ++g)
-                if (r + g < W) load_replica<Tin, ADD>(src, W, r + g, j, mk, f[g]);
+                if (r + g < W) load_replica<Tin, ADD, CMP>(src, W, r + g, j, mk, f[g]);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 if (r + g < W) {
@@ -182,8 +196,9 @@ __device__ __forceinline__ void reduce_vec_any(const ReduceParams& p, const Tin*
 
 // M = NoMask (every replica has every gradient) or SegMask (unused parameters).
 // ADD: fused last micro-step of a no_sync block (2W source streams per
-// segment, see SegTable).
-template <typename Tin, int WC, typename M, bool ADD>
+// segment, see SegTable).  CMP: the bf16-compression hook fused into the
+// pass (each replica value rounded to bf16 before the sum).
+template <typename Tin, int WC, typename M, bool ADD, bool CMP = false>
 __global__ void __launch_bounds__(kMaxBlock)
 bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_constant__ M mask) {
     pdl_enter(p.chain);
@@ -215,14 +230,14 @@ bucket_reduce_kernel(const __grid_constant__ ReduceParams p, const __grid_consta
         const long long kb = (x + N - 1) / N;   // first whole vector
         const long long ke = e / N;             // one past the last whole vector
         if (__ldg(p.seg_vec + s) && kb < ke) {
-            reduce_scalar<Tin, ADD>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x, mk);
+            reduce_scalar<Tin, ADD, CMP>(p, src, dst, a0, x, kb * N, W, threadIdx.x, blockDim.x, mk);
             if constexpr (WC > 0)
-                reduce_vec_fixed<Tin, WC, U, ADD>(p, src, dst, a0, kb, ke, mk);
+                reduce_vec_fixed<Tin, WC, U, ADD, CMP>(p, src, dst, a0, kb, ke, mk);
             else
-                reduce_vec_any<Tin, ADD>(p, src, dst, a0, kb, ke, W, mk);
-            reduce_scalar<Tin, ADD>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x, mk);
+                reduce_vec_any<Tin, ADD, CMP>(p, src, dst, a0, kb, ke, W, mk);
+            reduce_scalar<Tin, ADD, CMP>(p, src, dst, a0, ke * N, e, W, threadIdx.x, blockDim.x, mk);
         } else {
-            reduce_scalar<Tin, ADD>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x, mk);
+            reduce_scalar<Tin, ADD, CMP>(p, src, dst, a0, x, e, W, threadIdx.x, blockDim.x, mk);
         }
         x = e;
         ++s;
@@ -377,14 +392,6 @@ __global__ void __launch_bounds__(kMaxBlock) seg_copy_kernel(const __grid_consta
     }
 }
 
-// bf16 round to nearest even, widened back to fp32 (NaN stays a quiet NaN).
-__device__ __forceinline__ float round_bf16(float x) {
-    const uint32_t u = __float_as_uint(x);
-    if ((u & 0x7fffffffu) > 0x7f800000u) return __uint_as_float((u | 0x00400000u) & 0xffff0000u);
-    const uint32_t r = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
-    return __uint_as_float(r);
-}
-
 struct FlatMeanParams {
     float* out;
     long long n;
@@ -511,6 +518,17 @@ ReduceKernel<M> pick_reduce(InType in, int W) {
     }
 }
 
+// bf16-compression variant: fp32 gradients, every replica present.
+ReduceKernel<NoMask> pick_reduce_cmp(int W) {
+    switch (W) {
+        case 2: return bucket_reduce_kernel<float, 2, NoMask, false, true>;
+        case 4: return bucket_reduce_kernel<float, 4, NoMask, false, true>;
+        case 8: return bucket_reduce_kernel<float, 8, NoMask, false, true>;
+        case 16: return bucket_reduce_kernel<float, 16, NoMask, false, true>;
+        default: return bucket_reduce_kernel<float, 0, NoMask, false, true>;
+    }
+}
+
 // Fused last-step variant: fp32 accumulators, every replica present.
 ReduceKernel<NoMask> pick_reduce_add(int W) {
     switch (W) {
@@ -575,10 +593,12 @@ cudaError_t launch_reduce(const SegTable& t, InType in, int W, int n_out, float*
     p.piece = ceil_div(ceil_div(span, grid), N) * N;
     grid = ceil_div(span, p.piece);
     if (t.add && (mask || in != IN_F32)) return cudaErrorInvalidValue;   // no such variant
+    if (cfg.compress && (t.add || mask || in != IN_F32)) return cudaErrorInvalidValue;
+    const ReduceKernel<NoMask> plain = t.add ? pick_reduce_add(W) : cfg.compress ? pick_reduce_cmp(W)
+                                                                               : pick_reduce<NoMask>(in, W);
     cudaError_t err = mask ? launch(pick_reduce<SegMask>(in, W), static_cast<int>(grid), cfg.block, cfg.pdl,
                                     stream, p, *mask)
-                           : launch(t.add ? pick_reduce_add(W) : pick_reduce<NoMask>(in, W), static_cast<int>(grid),
-                                    cfg.block, cfg.pdl, stream, p, NoMask{});
+                           : launch(plain, static_cast<int>(grid), cfg.block, cfg.pdl, stream, p, NoMask{});
     if (err == cudaSuccess && launches) ++*launches;
     return err;
 }

@@ -144,8 +144,9 @@ __device__ __forceinline__ void walk(const ReduceParams& p, int s, long long x, 
 
 // ADD: fused last micro-step of a no_sync block -- a stage holds 2W tiles
 // (the W accumulated fields, then the W last-step gradients) and replica r
-// contributes fl32(acc_r + g_r).
-template <typename Tin, int WC, typename M, bool ADD>
+// contributes fl32(acc_r + g_r).  CMP: the built-in bf16-compression hook
+// fused into the pass -- replica r contributes its value rounded to bf16.
+template <typename Tin, int WC, typename M, bool ADD, bool CMP = false>
 __global__ void __launch_bounds__(kThreads, 1)
 bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_constant__ M mask) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -262,6 +263,10 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
 #pragma unroll
                     for (int q = 0; q < N; ++q) f[q] = __fadd_rn(f[q], h[q]);
                 }
+                if constexpr (CMP) {
+#pragma unroll
+                    for (int q = 0; q < N; ++q) f[q] = round_bf16(f[q]);
+                }
             };
             for (int v = tc; v < nv; v += nct) {
                 float acc[N], f[N];
@@ -292,7 +297,7 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
         [&](int sg, long long a0, long long lo, long long hi) {
             const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * NS;
             float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
-            reduce_scalar<Tin, ADD>(p, src, dst, a0, lo, hi, W, tc, nct, seg_mask(mask, sg - p.s0));
+            reduce_scalar<Tin, ADD, CMP>(p, src, dst, a0, lo, hi, W, tc, nct, seg_mask(mask, sg - p.s0));
         });
 }
 
@@ -473,6 +478,17 @@ TmaKernel<M> pick_tma(InType in, int W) {
     }
 }
 
+// bf16-compression variant: fp32 gradients, every replica present.
+TmaKernel<NoMask> pick_tma_cmp(int W) {
+    switch (W) {
+        case 2: return bucket_reduce_tma_kernel<float, 2, NoMask, false, true>;
+        case 4: return bucket_reduce_tma_kernel<float, 4, NoMask, false, true>;
+        case 8: return bucket_reduce_tma_kernel<float, 8, NoMask, false, true>;
+        case 16: return bucket_reduce_tma_kernel<float, 16, NoMask, false, true>;
+        default: return bucket_reduce_tma_kernel<float, 0, NoMask, false, true>;
+    }
+}
+
 // Fused last-step variant: fp32 accumulators, every replica present.
 TmaKernel<NoMask> pick_tma_add(int W) {
     switch (W) {
@@ -629,6 +645,7 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
                               const SegMask* mask) {
     if (hi <= lo || s1 <= s0) return cudaSuccess;
     if (t.add && (mask || in != IN_F32)) return cudaErrorInvalidValue;   // no such variant
+    if (cfg.compress && (t.add || mask || in != IN_F32)) return cudaErrorInvalidValue;
     const int N = in == IN_F32 ? 4 : 8;
     const int s_in = in == IN_F32 ? 4 : 2;
     const long long NS = t.add ? 2LL * W : W;   // tiles per stage
@@ -665,7 +682,7 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     p.stages = stages;
     p.tile = static_cast<int>(tile);
     p.chain = cfg.chain;
-    const TmaKernel<NoMask> plain = t.add ? pick_tma_add(W) : pick_tma<NoMask>(in, W);
+    const TmaKernel<NoMask> plain = t.add ? pick_tma_add(W) : cfg.compress ? pick_tma_cmp(W) : pick_tma<NoMask>(in, W);
     cudaError_t e = mask ? ensure_smem_attr(pick_tma<SegMask>(in, W)) : ensure_smem_attr(plain);
     if (e != cudaSuccess) return e;
     const int per_sm = mask ? tma_ctas(cfg, pick_tma<SegMask>(in, W), smem) : tma_ctas(cfg, plain, smem);

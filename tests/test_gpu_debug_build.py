@@ -16,7 +16,7 @@ import pytest
 import torch
 
 from oracle.buckets import assign_buckets
-from oracle.hooks import hook_mean, reduce_with_hook
+from oracle.hooks import hook_bf16_compress, hook_mean, reduce_with_hook
 from oracle.nosync import accumulate_steps, reduce_last_step
 from oracle.reduce import reduce_buckets
 from oracle.unused import reduce_with_unused
@@ -147,18 +147,21 @@ def test_debug_build_unused_parameters(kernel):
     red.destroy()
 
 
-def test_debug_build_hooks():
+@pytest.mark.parametrize("hook,fused", [("mean", 1), ("mean", 0), ("bf16_compress", 1)])
+def test_debug_build_hooks(hook, fused):
     numel = RAGGED
     W, cap = 4, 16 * 1024
     flats, views, offs = host_grads(numel, W, "f32")
     members, locs = assign_buckets(numel, 4, cap)
-    want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, hook_mean)
+    want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel,
+                                                hook_mean if hook == "mean" else hook_bf16_compress)
     _, grads = host_to_device_views(flats, numel, offs, "f32", DEV)
     red = Reducer(numel, "f32", cap, lib_path=DBG)
     arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
     outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
     red.bind(grads, arena, outs)
-    red.register_comm_hook("mean", [torch.empty(red.arena_numel(), device=DEV) for _ in range(W)])
+    red.register_comm_hook(hook, [torch.empty(red.arena_numel(), device=DEV) for _ in range(W)])
+    red.set_option(_lib.OPT_HOOK_FUSED, fused)
     red.begin_iteration()
     red.mark_ready_many(gen.reverse_order(len(numel)))
     torch.cuda.synchronize()

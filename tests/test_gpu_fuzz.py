@@ -154,9 +154,9 @@ def test_fuzz_fused_last_step(seed):
 
 @pytest.mark.parametrize("seed", range(40))
 def test_fuzz_hooks(seed):
-    """The built-in hooks (mean, bf16 compression) through gather, hook and
-    copy-back, over random layouts, W up to 33, dtypes, output modes and
-    kernel choices."""
+    """The built-in hooks (mean, bf16 compression), inside the fused pass
+    (even seeds) or through gather, hook and copy-back (odd seeds), over
+    random layouts, W up to 33, dtypes, output modes and kernel choices."""
     import torch
     from oracle.buckets import assign_buckets
     from oracle.hooks import hook_bf16_compress, hook_mean, reduce_with_hook
@@ -182,6 +182,7 @@ def test_fuzz_hooks(seed):
     red.bind(grads_dev, arena, None if n_out == 0 else (outs[0] if n_out == 1 else outs))
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     red.register_comm_hook(hook, [torch.empty(max(N, 1), dtype=tdt, device="cuda") for _ in range(W)])
+    red.set_option(_lib.OPT_HOOK_FUSED, 1 if seed % 2 == 0 else 0)
     members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
     fn = hook_mean if hook == "mean" else hook_bf16_compress
     want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, fn, n_out=max(n_out, 1))

@@ -1,6 +1,7 @@
-"""GPU parity of the communication-hook path (gather, hook, copy-back)
-against the oracle, bit for bit, and of the hook contract: one call per
-bucket in index order with the bucket's metadata."""
+"""GPU parity of the communication-hook path against the oracle, bit for
+bit -- the built-in hooks inside the fused bucket pass and through gather,
+hook call and copy-back -- and of the hook contract: one call per bucket in
+index order with the bucket's metadata."""
 
 import numpy as np
 import pytest
@@ -44,14 +45,22 @@ def _setup(numel, W, dtype, cap, n_out, odd=False):
     return red, views, arena, outs, rb
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "gathered"])
 @pytest.mark.parametrize("hook", ["mean", "bf16_compress"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("W,n_out", [(1, 1), (3, 1), (4, 4), (8, 0), (33, 1)])
-def test_builtin_hooks(hook, dtype, W, n_out):
+def test_builtin_hooks(hook, dtype, W, n_out, fused):
+    """Both routes of a built-in hook: inside the fused bucket pass (the
+    default; the replica buffers stay as they were) and through gather, hook
+    call and copy-back (the replica buffers hold each replica's buckets)."""
     numel = RAGGED
     cap = 16 * 1024
     red, views, arena, outs, rb = _setup(numel, W, dtype, cap, n_out, odd=(W == 3))
+    for t in rb:
+        t.view(torch.int16).fill_(0x7FC1)        # a NaN pattern (fp32 and bf16) no hook writes
     red.register_comm_hook(hook, rb)
+    red.set_option(_lib.OPT_HOOK_FUSED, 1 if fused else 0)
+    launches0 = red.launch_count()
     members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
     fn = hook_mean if hook == "mean" else hook_bf16_compress
     want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, fn, n_out=max(n_out, 1))
@@ -63,6 +72,13 @@ def test_builtin_hooks(hook, dtype, W, n_out):
     for o in range(n_out):
         for v in range(len(numel)):
             assert bits_equal(outs[o][v].cpu().numpy(), want_outs[0][v]), (o, v)
+    assert red.device_status() == 0
+    if fused:
+        # one launch per readiness event that releases buckets, nothing gathered
+        assert red.launch_count() - launches0 <= len(members)
+        for t in rb:
+            assert bool((t.view(torch.int16) == 0x7FC1).all())
+        return
     # the replica buffers hold each replica's gathered buckets
     bufs = gather_buckets(views, members, locs, numel)
     lens = [sum(numel[v] for v in m) for m in members]
@@ -73,9 +89,10 @@ def test_builtin_hooks(hook, dtype, W, n_out):
             assert np.array_equal(host[starts[b]:starts[b + 1]].view(np.uint8), bufs[r][b].view(np.uint8))
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "gathered"])
 @pytest.mark.parametrize("hook", ["mean", "bf16_compress"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_builtin_hooks_special_values(hook, dtype):
+def test_builtin_hooks_special_values(hook, dtype, fused):
     """±0, ±Inf, NaN, subnormals and ±3.4e38 (above the largest bf16, so the
     compression hook rounds it to ±Inf) at seeded positions: the hooks'
     device rounding and sums match the oracle bit for bit (NaN as a class)."""
@@ -90,6 +107,7 @@ def test_builtin_hooks_special_values(hook, dtype):
     red.bind(grads_dev, arena, outs)
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     red.register_comm_hook(hook, [torch.empty(max(N, 1), dtype=tdt, device=DEV) for _ in range(W)])
+    red.set_option(_lib.OPT_HOOK_FUSED, 1 if fused else 0)
     members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
     fn = hook_mean if hook == "mean" else hook_bf16_compress
     want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, fn, n_out=n_out)
@@ -236,6 +254,7 @@ def test_hook_on_bucket_views_detects_a_broken_layout():
     arena = torch.empty(red.arena_numel(), device=DEV)
     red.bind(views, arena, None)
     red.register_comm_hook("mean", None)
+    red.set_option(_lib.OPT_HOOK_FUSED, 0)        # the hook-call route reads the views in place
     # rebinding in registration order breaks the view layout: the launch fails
     other = [torch.zeros(sum(numel), device=DEV) for _ in range(W)]
     offs = [0, 100, 300]

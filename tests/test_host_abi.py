@@ -379,6 +379,16 @@ def test_hook_registration_rules(lib):
     with pytest.raises(InvalidArg):
         red.set_option(L.OPT_FIND_UNUSED, 1)
     assert lib.ddp_status_string(-8) == b"DDP_ERR_HOOK"
+    # the route of a built-in hook: fused by default, switchable between iterations only
+    assert red.get_option(L.OPT_HOOK_FUSED) == 1
+    red.set_option(L.OPT_HOOK_FUSED, 0)
+    assert red.get_option(L.OPT_HOOK_FUSED) == 0
+    red.begin_iteration()
+    red.mark_ready(1)                                         # bucket 0 = [1]; bucket 1 = [0] still pending
+    with pytest.raises(InvalidArg):
+        red.set_option(L.OPT_HOOK_FUSED, 1)
+    red.mark_ready(0)
+    red.set_option(L.OPT_HOOK_FUSED, 1)
 
 
 def test_last_step_binding_rules(lib):
