@@ -143,10 +143,13 @@ int ddp_mark_ready(ddp_ctx* ctx, int32_t var, int32_t* launched, int32_t* n_laun
  * every listed variable must be final on `stream` when the call is made.
  * Launches after the first one of the call follow it directly on the stream
  * (nothing else can be enqueued in between), so they start without waiting
- * for it and wait only before exiting.
+ * for it and wait only before exiting.  Consecutive bucket runs released by
+ * the call's events merge into one launch until it spans DDP_OPT_COALESCE_ELEMS
+ * elements (the state and the results are those of one launch per event).
  *   vars    host array [n] of variable indices
  *   n_done  receives the number of events processed (all of them on success;
- *           on error, the failing event's index; earlier events stay applied)
+ *           on error, the failing event's index; earlier events stay applied
+ *           and their released buckets are launched before the call returns)
  * Errors: as ddp_mark_ready. */
 int ddp_mark_ready_many(ddp_ctx* ctx, const int32_t* vars, int32_t n, int32_t* n_done, void* stream);
 
@@ -382,11 +385,17 @@ enum ddp_option {
     DDP_OPT_FIND_UNUSED = 11,     /* 1: track unused parameters (find_unused_parameters; default 0):
                                      enables ddp_set_local_used and the local-use bits of
                                      ddp_accumulate_nosync_used; segments are never merged; W <= 64 */
-    DDP_OPT_HOOK_FUSED = 12       /* 1 (default): a registered built-in hook (ddp_hook_mean,
+    DDP_OPT_HOOK_FUSED = 12,      /* 1 (default): a registered built-in hook (ddp_hook_mean,
                                      ddp_hook_bf16_compress) runs inside the fused bucket pass -- one
                                      launch per released bucket range, nothing gathered into the replica
                                      buffers, no separate copy-back; 0: the gather, hook call and
                                      copy-back route of every other hook.  Between iterations only. */
+    DDP_OPT_COALESCE_ELEMS = 13   /* ddp_mark_ready_many: consecutive bucket runs released by the events
+                                     of one call go out as one launch until it spans at least this many
+                                     elements (default 2^21; 0: one launch per releasing event); results, readiness
+                                     state and hook order are unchanged, only launch boundaries move.
+                                     Every listed gradient is final when the call is made, so no launch
+                                     is held back behind work it could overlap. */
 };
 int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
 int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);

@@ -29,7 +29,7 @@ STATUS = {
 OPT_DRY_RUN, OPT_CTAS_PER_SM, OPT_PDL, OPT_BLOCK_THREADS = 0, 1, 2, 3
 OPT_KERNEL, OPT_STAGES, OPT_STAGE_BYTES, OPT_TMA_CTAS_PER_SM = 4, 5, 6, 7
 OPT_AUTO_MIN_ELEMS, OPT_CHAINED, OPT_QUERY_KERNEL, OPT_FIND_UNUSED = 8, 9, 10, 11
-OPT_HOOK_FUSED = 12
+OPT_HOOK_FUSED, OPT_COALESCE_ELEMS = 12, 13
 KERNEL_LDG, KERNEL_TMA, KERNEL_AUTO = 0, 1, 2
 
 

@@ -44,6 +44,10 @@ constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 constexpr int kMaxDynSmem = 232448;                // 227 KiB opt-in per CTA
 constexpr int kHeaderBytes = 128;                  // mbarriers, ring starts after
 constexpr long long kMinCopyBytes = 4096;          // smallest per-stream copy a stage is sized for
+#ifndef DDP_PREFETCH_STAGES
+#define DDP_PREFETCH_STAGES 2
+#endif
+constexpr long long kPrefetchStages = DDP_PREFETCH_STAGES;   // stages prefetched before a launch's wait
 
 // status codes written by bounded waits
 constexpr int kStatusEmptyTimeout = 1;
@@ -99,6 +103,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
         }
     }
     return true;
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (no destination, no barrier):
+// a hint that moves no data the program can observe.  src 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // One-dimensional bulk copy global -> shared, completion counted in bytes
@@ -169,18 +180,46 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
         }
         fence_barrier_init();
     }
-    __syncthreads();
-    pdl_enter(p.chain);
+    // A chained launch (see pdl_enter) lets its successor start at once.
+    if (p.chain) pdl_trigger();
 
+    // The CTA's slice and its first segment come from the library's own
+    // segment table, final before the launch: found before the wait for the
+    // preceding grid, so a launch that must wait spends none of the time
+    // after it on the search.
     long long x = p.base + static_cast<long long>(blockIdx.x) * p.piece;
     long long y = x + p.piece;
     x = x < p.lo ? p.lo : x;
     y = y > p.hi ? p.hi : y;
-    if (x >= y) {   // whole CTA, before any copy is issued
+    const bool idle = x >= y;   // the same for every thread of the CTA
+    const int s = idle ? p.s0 : find_segment(p.seg_off, p.s0, p.s1, x);
+    // A launch that waits for the preceding grid asks L2 for the inputs of its
+    // first stages meanwhile.  Its CTAs become resident only as the preceding
+    // launch's CTAs retire (two resident waves fill the SMs until then), so
+    // the lines arrive during that launch's tail and the first bulk copies
+    // after the wait hit L2.  A prefetch moves nothing the program observes:
+    // inputs a preceding grid is still writing are read again, coherently, by
+    // the copies after the wait.
+    if (!idle && !p.chain && kPrefetchStages > 0 && warp == 0) {
+        long long k = 0;
+        walk<N>(
+            p, s, x, y,
+            [&](int sg, long long a0, long long c, long long L) {
+                if (k++ >= kPrefetchStages) return;
+                const unsigned long long mk = seg_mask(mask, sg - p.s0);
+                const Tin* const* src = reinterpret_cast<const Tin* const*>(p.seg_src) + static_cast<long long>(sg) * NS;
+                for (int q = lane; q < NS; q += 32)
+                    if (has_replica(mk, q % W))
+                        bulk_prefetch_l2(src[q] + (c - a0), static_cast<uint32_t>(L * sizeof(Tin)));
+            },
+            [](int, long long, long long, long long) {});
+    }
+    __syncthreads();
+    if (!p.chain) pdl_enter(0);   // wait for every earlier grid, then let the successor start
+    if (idle) {   // whole CTA, before any copy is issued
         if (threadIdx.x == 0) pdl_exit(p.chain, p.piece >= kHoldAllPiece);
         return;
     }
-    const int s = find_segment(p.seg_off, p.s0, p.s1, x);
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer warp

@@ -670,3 +670,25 @@ def test_nosync_failed_step_changes_nothing():
         for v in range(len(numel)):
             assert bits_equal(acc[r][v].cpu().numpy(), want[v]), (r, v)
     red.destroy()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("coalesce", [1, 4096, 1 << 16, 1 << 40])
+def test_coalesced_launches(coalesce, kernel):
+    """DDP_OPT_COALESCE_ELEMS: the runs released by one mark_ready_many call
+    merge into launches of at least that many elements; every element still
+    equals the oracle, and the launch count drops accordingly (one launch
+    for the whole call when nothing reaches the threshold)."""
+    numel = shapes.numels(shapes.gpt2_medium(layers=2, vocab=3000, n_ctx=256))
+    per_event = full_compare(numel, 8, "bf16", 0, order="reverse", mode="mark_ready_many", kernel=kernel,
+                             options={_lib.OPT_COALESCE_ELEMS: 0})
+    n = full_compare(numel, 8, "bf16", 0, order="reverse", mode="mark_ready_many", kernel=kernel,
+                     options={_lib.OPT_COALESCE_ELEMS: coalesce})
+    assert n <= per_event
+    if coalesce == 1:
+        assert n == per_event
+    if coalesce == 1 << 40:
+        assert n == 1
+    # a straggler order parks buckets: merged runs still go out in index order
+    full_compare(RAGGED, 4, "f32", 16 * 1024, order="straggler", mode="mark_ready_many", kernel=kernel,
+                 options={_lib.OPT_COALESCE_ELEMS: coalesce}, iterations=2)
