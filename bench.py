@@ -414,6 +414,65 @@ def run_gpt2_only(args):
     return 0
 
 
+def run_sharded(args):
+    """The bucket all-reduce across ranks that each hold one replica (one
+    rank per GPU under torchrun, NCCL): every rank reduces its own BERT-large
+    gradients (W = 1 per rank, 25 MiB buckets) through the sharded hook --
+    per bucket, in bucket-index order, gather into the bucket buffer,
+    all-to-all of the raw chunks, the owner's rank-order mean, all-gather,
+    copy-back.  Bytes per rank and step: N*4 read + 2*N*4 written (the
+    fused pass's algorithmic bytes at W = 1); value = those bytes over all
+    ranks / the slowest rank's time (weak scaling: per-rank work is fixed)."""
+    import torch
+    import torch.distributed as dist
+    from reduction_reducer_gb300.sharded import sharded_hook
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1 or "MASTER_ADDR" in os.environ:
+        dist.init_process_group("nccl", device_id=device)
+    else:
+        dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1, device_id=device)
+    stream = torch.cuda.Stream(device=device)
+    from reduction_reducer_gb300 import Reducer
+    numel = shapes.numels(shapes.bert_large())
+    offs, total = gen.packed_offsets(numel, 64)
+    flat = gen.draw_flat_torch(total, rank, 0, "f32", device)
+    grads = [[flat[o:o + n] for o, n in zip(offs, numel)]]
+    red = Reducer(numel, "f32", 25 * MIB)
+    arena = torch.empty(red.arena_numel(), device=device)
+    out_flat = torch.empty(total, device=device)
+    red.bind(grads, arena, [out_flat[o:o + n] for o, n in zip(offs, numel)])
+    rb = torch.empty(red.arena_numel(), device=device)
+    red.register_comm_hook(sharded_hook(dist, rb, arena, dtype="f32"), [rb])
+    order = read_order()
+
+    def step():
+        red.begin_iteration()
+        red.mark_ready_many(order, stream)
+
+    with torch.cuda.stream(stream):
+        ms, _, _ = time_steps(torch, stream, step, args.steps, args.warmup, dist if world > 1 else None)
+    N = sum(numel)
+    per_rank = N * 4 + 2 * N * 4
+    t = ms / args.steps
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": round(per_rank * world / (t * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1e-3) gradients generated on the device, one replica per rank)",
+            "config": {"workload": "bert_large", "W": world, "replicas_per_rank": 1, "P": len(numel), "N": N,
+                       "cap_mib": 25, "buckets": red.B, "mode": "copy-back (n_out=1)",
+                       "parallelism": f"sharded all-reduce x{world} (all-to-all of raw chunks, owner mean, all-gather)",
+                       "bytes_per_rank_step": per_rank}}), flush=True)
+    red.destroy()
+    dist.destroy_process_group()
+    return 0
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -774,6 +833,12 @@ def extra_configs(torch, device, stream, args, dist, keep):
     for cap in (0, 1, 5, 25, 100):
         wl = Workload("gpt2_medium", torch, device, cap, n_out=1, driver="hooks")
         timed(wl, f"gpt2_medium_w8_bf16_cap{cap}", f"GPT-2-medium bf16 W=8, cap {cap} MiB")
+        if cap == 0:
+            # the same per-gradient buckets with one launch per releasing event
+            from reduction_reducer_gb300 import _lib
+            wl.red.set_option(_lib.OPT_COALESCE_ELEMS, 0)
+            timed(wl, "gpt2_medium_w8_bf16_cap0_launch_per_event",
+                  "GPT-2-medium bf16 W=8, cap 0, DDP_OPT_COALESCE_ELEMS = 0: one launch per releasing event")
         wl.free()
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
@@ -1004,6 +1069,9 @@ def main():
                     help="profiling cases: reduce the main workload through a built-in hook")
     ap.add_argument("--hook-route", default="fused", choices=["fused", "gathered"],
                     help="profiling cases: --hook inside the fused pass or through gather + hook call + copy-back")
+    ap.add_argument("--sharded", action="store_true",
+                    help="one replica per rank: the bucket all-reduce across ranks (NCCL; reduce-scatter as an "
+                         "all-to-all of raw chunks + owner mean, then all-gather)")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--cpu-config-s", type=float, default=2.0,
                     help="seconds of oracle work per configuration (per_config cpu_oracle)")
@@ -1011,6 +1079,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sharded:
+        return run_sharded(args)
     if args.workload == "nosync_resnet50":
         return run_nosync_only(args)
     if args.workload == "gpt2_medium":

@@ -347,6 +347,34 @@ int ddp_bind_last_step(ddp_ctx* ctx, const void* const* g_last);
 int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_arena,
                            float* const* grad_out, int32_t n_out, void* stream);
 
+/* ---------------------------------------------------------------- ranks that each hold one replica */
+
+/* Ownership plan of the bucket all-reduce split across G ranks ("PyTorch
+ * Distributed Training Internals", section "3. The All-Reduce Itself": a
+ * reduce-scatter, in which every rank ends up owning the reduced values of one
+ * contiguous chunk of the bucket's flat range, then an all-gather of the
+ * chunks; "NCCL 专家课程 30", section "Bucket 必须按序发起": every rank issues
+ * the buckets' collectives in bucket-index order).  For a range of n elements
+ * every chunk has *chunk = ceil(n / G) elements rounded up to a multiple of 8
+ * (16-byte aligned chunk starts for fp32 and bf16); rank g owns
+ * [*lo, *hi) = [min(n, g * chunk), min(n, (g + 1) * chunk)), so the chunks
+ * tile [0, n) in rank order and ranks past the last non-empty chunk own
+ * nothing.  Pure host arithmetic; any pointer may be NULL.
+ * Errors: INVALID_ARG (n < 0, G < 1, g outside [0, G)). */
+int ddp_shard_range(int64_t n, int32_t G, int32_t g, int64_t* chunk, int64_t* lo, int64_t* hi);
+
+/* The owner's step of that all-reduce: out[i] = fl32(1/G) x the fp32 sum, in
+ * rank order c = 0 .. G-1 starting from chunks[0][i], of the widened values
+ * chunks[c][i], i < n -- the one-GPU pass's arithmetic over the G replicas,
+ * so the sharded result equals it bit for bit when the reduce-scatter moves
+ * the replicas' raw chunks (an all-to-all) instead of partial sums.
+ *   chunks  host array [G] of device pointers: replica c's n values of the
+ *           owned chunk, in `dtype` (16-byte aligned for 128-bit loads; any
+ *           alignment is correct)
+ *   out     device fp32 [n]
+ * Asynchronous on `stream`.  G <= 64.  Errors: INVALID_ARG, CUDA. */
+int ddp_shard_mean(int32_t G, ddp_dtype dtype, const void* const* chunks, float* out, int64_t n, void* stream);
+
 /* ---------------------------------------------------------------- options, info */
 
 enum ddp_option {

@@ -80,6 +80,9 @@ SIGNATURES = {
     "ddp_selftest_bounded_wait": (C.c_int, [C.c_int64, C.POINTER(C.c_int32)]),
     "ddp_reduce_all_noalloc": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.c_void_p,
                                          C.POINTER(C.c_void_p), C.c_int32, C.c_void_p]),
+    "ddp_shard_range": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
+                                  C.POINTER(C.c_int64)]),
+    "ddp_shard_mean": (C.c_int, [C.c_int32, C.c_int, C.POINTER(C.c_void_p), C.c_void_p, C.c_int64, C.c_void_p]),
     "ddp_status_string": (C.c_char_p, [C.c_int]),
     "ddp_last_error": (C.c_char_p, [C.c_void_p]),
     "ddp_destroy": (None, [C.c_void_p]),

@@ -32,7 +32,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NOALLOC_SCRATCH_BYTES = 256 * 1024
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I" + INCLUDE, "-I" + CSRC,
           f"-DDDP_NOALLOC_SCRATCH_BYTES={NOALLOC_SCRATCH_BYTES}"]
-SOURCES = ["ddp_host.cpp", "ddp_kernels.cu", "ddp_kernels_tma.cu", "ddp_noalloc.cu"]
+SOURCES = ["ddp_host.cpp", "ddp_kernels.cu", "ddp_kernels_tma.cu", "ddp_noalloc.cu", "ddp_shard.cpp"]
 
 
 def nvcc() -> str:

@@ -37,6 +37,12 @@ _ERRORS = {-1: InvalidArg, -2: AlreadyReady, -3: OutOfOrder, -4: PriorReductionU
            -5: NotBound, -6: CudaError, -7: NoMemory, -8: HookError}
 
 
+def _check_status(st: int, detail) -> None:
+    """Raise the exception of a nonzero status (``detail``: message or None)."""
+    if st != 0:
+        raise _ERRORS.get(st, DDPError)(st, detail or _lib.STATUS.get(st, ""))
+
+
 def _ptr(x) -> int:
     if x is None:
         return 0

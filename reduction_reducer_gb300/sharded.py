@@ -1,0 +1,126 @@
+"""The bucket all-reduce across ranks that each hold one replica.
+
+Each rank runs its own reducer (W = 1: its replica's gradients) with a
+communication hook from this module.  The library calls the hook for every
+launched bucket, in bucket-index order on every rank ("NCCL 专家课程 30",
+section "Bucket 必须按序发起"), with the bucket's gradients gathered into a
+flat buffer, and copies the hook's result back into the gradients.  The hook
+performs the all-reduce as the pages describe it ("PyTorch Distributed
+Training Internals", section "3. The All-Reduce Itself"): a reduce-scatter,
+after which rank g owns the reduced values of chunk g of the bucket
+(``ddp_shard_range``), then an all-gather of the chunks.
+
+The reduce-scatter is exact: an all-to-all moves the replicas' raw values of
+each chunk to its owner, and the owner sums them itself in rank order and
+scales by fl32(1/G) (``ddp_shard_mean``, the library's kernel), so every rank
+ends with the bits the one-GPU pass computes over the same G replicas.
+
+Only plumbing lives here: the exchange runs through ``torch.distributed``
+(NCCL between GPUs; any backend with all_to_all_single and
+all_gather_into_tensor), the ownership plan and the arithmetic through the C
+ABI.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _lib
+from .reducer import DTYPES, _check_status, _ptr, _ptr_array
+
+
+def shard_range(n: int, G: int, g: int):
+    """(chunk, lo, hi): rank g's part [lo, hi) of a flat range of n elements
+    split in chunks of ``chunk`` elements (``ddp_shard_range``)."""
+    lib = _lib.load()
+    c, lo, hi = C.c_int64(), C.c_int64(), C.c_int64()
+    _check_status(lib.ddp_shard_range(int(n), int(G), int(g), C.byref(c), C.byref(lo), C.byref(hi)), None)
+    return c.value, lo.value, hi.value
+
+
+def shard_mean(chunks, out, dtype: str, stream: int):
+    """out[i] = rank-order fp32 mean of chunks[c][i] (device tensors or
+    addresses, ``out.numel()`` values each) on ``stream``
+    (``ddp_shard_mean``)."""
+    lib = _lib.load()
+    n = out.numel()
+    arr = _ptr_array([_ptr(t) for t in chunks])
+    _check_status(lib.ddp_shard_mean(len(chunks), DTYPES[dtype], arr, _ptr(out), n, stream), None)
+
+
+class ShardedAllReduce:
+    """The exact reduce-scatter + all-gather of one flat bucket over the
+    ranks of ``group`` (every rank holds one replica).
+
+    ``mean(chunks, out)`` is the owner's arithmetic; by default the
+    library's ``ddp_shard_mean`` on the current CUDA stream.  Buffers for the
+    exchange are allocated once per bucket size and reused.
+    """
+
+    def __init__(self, dist, group=None, dtype: str = "f32", mean=None):
+        self.dist = dist
+        self.group = group
+        self.G = dist.get_world_size(group)
+        self.rank = dist.get_rank(group)
+        self.dtype = dtype
+        self.mean = mean
+        self._bufs = {}
+
+    def _buf(self, key, n, dtype, like):
+        t = self._bufs.get(key)
+        if t is None or t.numel() < n or t.dtype != dtype or t.device != like.device:
+            import torch
+            t = torch.empty(n, dtype=dtype, device=like.device)
+            self._bufs[key] = t
+        return t[:n]
+
+    def __call__(self, local, out):
+        """local: this rank's bucket (1-D, gradient dtype); out: fp32 tensor
+        of the same length that receives the mean over all ranks."""
+        import torch
+        n = local.numel()
+        G = self.G
+        chunk, lo, hi = shard_range(n, G, self.rank)
+        send = self._buf("send", G * chunk, local.dtype, local)
+        send[:n].copy_(local)
+        if G * chunk > n:
+            send[n:].zero_()                 # the last chunk's tail: sent, never used
+        recv = self._buf("recv", G * chunk, local.dtype, local)
+        self.dist.all_to_all_single(recv, send, group=self.group)
+        mine = self._buf("mine", chunk, torch.float32, local)
+        parts = [recv[c * chunk:c * chunk + (hi - lo)] for c in range(G)]   # replica c's values of my chunk
+        if hi > lo:
+            if self.mean is not None:
+                self.mean(parts, mine[:hi - lo])
+            else:
+                shard_mean(parts, mine[:hi - lo], self.dtype, int(torch.cuda.current_stream().cuda_stream))
+        if chunk > hi - lo:
+            mine[hi - lo:].zero_()
+        gathered = self._buf("gathered", G * chunk, torch.float32, local)
+        self.dist.all_gather_into_tensor(gathered, mine, group=self.group)
+        out.copy_(gathered[:n])              # the chunks tile [0, n) in rank order
+
+
+def sharded_hook(dist, replica_buffer, arena, group=None, dtype: str = "f32"):
+    """A communication hook (for ``Reducer.register_comm_hook(hook,
+    [replica_buffer])`` on a reducer bound with W = 1) that all-reduces every
+    bucket across the ranks of ``group`` with ``ShardedAllReduce``.
+    ``replica_buffer`` and ``arena`` are the tensors the reducer gathers
+    into and reduces into; the hook runs its exchange on the library's
+    stream."""
+    import torch
+    reduce = ShardedAllReduce(dist, group, dtype)
+    esz = replica_buffer.element_size()
+
+    def hook(bucket, stream):
+        n = int(bucket.numel)
+        if n == 0:
+            return 0
+        at = (int(bucket.replicas[0]) - replica_buffer.data_ptr()) // esz
+        res = (int(bucket.result) - arena.data_ptr()) // 4
+        st = torch.cuda.ExternalStream(int(stream), device=arena.device) if stream else \
+            torch.cuda.default_stream(arena.device)
+        with torch.cuda.stream(st):
+            reduce(replica_buffer[at:at + n], arena[res:res + n])
+        return 0
+    return hook

@@ -1,0 +1,100 @@
+"""GPU side of the bucket all-reduce across ranks that each hold one replica.
+
+* ``ddp_shard_mean`` (the owner's rank-order mean of G replicas' chunks)
+  against the oracle's mean, bit for bit, for G up to 64, fp32 and bf16,
+  aligned and unaligned chunk pointers, ragged lengths, special values;
+* the whole path through a reducer (W = 1 per rank, the sharded hook) with
+  a real NCCL process group: on this one-GPU machine the group has one rank,
+  so the exchange is NCCL's all-to-all and all-gather with itself and the
+  result is the rank's own gradients (x 1/1), against the oracle.  Larger
+  groups run on the CPU over gloo (``tests/test_shard_plan.py``).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.buckets import assign_buckets
+from oracle.reduce import reduce_buckets, replica_mean
+from reduction_reducer_gb300 import Reducer, _lib
+from workloads import gen, shapes
+
+from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views, to_host
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import os
+    from reduction_reducer_gb300 import build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    _lib.load()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 16, 33, 64])
+def test_shard_mean_equals_oracle(G, dtype):
+    from reduction_reducer_gb300.sharded import shard_mean
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    for n, shift in [(1, 0), (7, 0), (4096, 0), (70001, 0), (70001, 3), (300007, 1)]:
+        # one receive buffer of G chunks, as the all-to-all leaves it; shift
+        # moves every chunk off its 16-byte boundary
+        chunk = -(-n // 8) * 8 + shift
+        xs = [gen.draw_flat_np(n, c, 5, dtype) for c in range(G)]
+        if dtype == "f32" and G >= 4 and n >= 8:       # signed zeros, infinities, NaN, a subnormal, overflow
+            xs[1][:8] = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 2.0 ** -149, 3.4e38, -1.0], np.float32)
+            xs[2][:8] = np.array([-0.0, -0.0, 1.0, np.inf, 1.0, 2.0 ** -149, 3.4e38, 1.0], np.float32)
+        flat = np.zeros(G * chunk + shift, xs[0].dtype)
+        for c in range(G):
+            flat[shift + c * chunk:shift + c * chunk + n] = xs[c]
+        dev = torch.from_numpy(flat.view(np.int16)).to(DEV).view(tdt) if dtype == "bf16" else torch.from_numpy(flat).to(DEV)
+        parts = [dev[shift + c * chunk:shift + c * chunk + n] for c in range(G)]
+        out = torch.full((n,), float("nan"), device=DEV)
+        shard_mean(parts, out, dtype, int(torch.cuda.current_stream().cuda_stream))
+        torch.cuda.synchronize()
+        want = replica_mean(xs)
+        got = out.cpu().numpy()
+        assert bits_equal(got, want), (n, shift, first_mismatch(got, want))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sharded_hook_nccl_single_rank(dtype):
+    """A reducer with the sharded hook in a one-rank NCCL group: every bucket
+    goes through the hook (all-to-all, owner mean, all-gather) and the
+    library's copy-back, in bucket order; the result is the oracle's mean of
+    the one replica."""
+    import torch.distributed as dist
+    from reduction_reducer_gb300.sharded import sharded_hook
+    numel = shapes.numels(shapes.bert_large(layers=2, vocab=2048))
+    cap = 1 << 20
+    store = dist.HashStore()
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1, device_id=torch.device(DEV, 0))
+    try:
+        flats, views, offs = host_grads(numel, 1, dtype)
+        _, grads_dev = host_to_device_views(flats, numel, offs, dtype, DEV)
+        red = Reducer(numel, dtype, cap)
+        arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+        outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+        red.bind(grads_dev, arena, outs)
+        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        rb = torch.empty(red.arena_numel(), dtype=tdt, device=DEV)
+        red.register_comm_hook(sharded_hook(dist, rb, arena, dtype=dtype), [rb])
+        s = torch.cuda.Stream()
+        for _ in range(2):
+            red.begin_iteration()
+            red.mark_ready_many(gen.reverse_order(len(numel)), s)
+        torch.cuda.synchronize()
+        members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+        want_arena, want_outs = reduce_buckets(views, members, locs, numel)
+        got = arena.cpu().numpy()
+        assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+        for v in range(len(numel)):
+            assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v]), v
+        red.destroy()
+    finally:
+        dist.destroy_process_group()

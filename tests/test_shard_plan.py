@@ -1,0 +1,127 @@
+"""The bucket all-reduce across ranks that each hold one replica, on the CPU.
+
+* the ownership plan (``ddp_shard_range``, host arithmetic of the library):
+  the chunks of a flat range tile it in rank order, start 16-byte aligned
+  for fp32 and bf16, are equal but for the last non-empty one, and differ
+  from the ideal 1/G share by less than one alignment unit;
+* the exchange (``reduction_reducer_gb300.sharded.ShardedAllReduce``) over
+  ``gloo`` with world sizes 2 and 3: every rank holds one replica of a
+  ragged model, all-reduces its buckets in bucket-index order (all-to-all of
+  the raw chunks, the owner's rank-order mean, all-gather), and must end with
+  the oracle's unsharded mean over the same replicas, bit for bit.  The
+  owner's arithmetic, a CUDA kernel in the library, is stood in for here by
+  the oracle's mean (this test covers the plan and the exchange; the GPU
+  tests cover the kernel).
+"""
+
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.buckets import assign_buckets
+from oracle.hooks import gather_buckets
+from oracle.reduce import reduce_buckets, replica_mean
+from workloads import gen
+
+
+@pytest.fixture(scope="module")
+def built():
+    from reduction_reducer_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.load()
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 8, 16, 33, 64])
+def test_chunks_tile_the_range(built, G):
+    from reduction_reducer_gb300.sharded import shard_range
+    for n in [0, 1, 2, 7, 8, 9, 15, 16, 17, 63, 64, 65, 100, 1000, 4097, 70001, 25 << 18, (1 << 31) + 37]:
+        at = 0
+        sizes = []
+        for g in range(G):
+            c, lo, hi = shard_range(n, G, g)
+            assert c % 8 == 0 and (n == 0 or c > 0)
+            assert lo == at and lo <= hi <= n                  # in rank order, no gap, no overlap
+            assert lo % 8 == 0 or lo == n                      # 16-byte aligned starts
+            assert n == 0 or c * G >= n                        # G chunks cover the range
+            assert c - 8 < -(-n // G) <= c or n == 0           # the ideal share, rounded up to 8
+            sizes.append(hi - lo)
+            at = hi
+        assert at == n
+        nonempty = [s for s in sizes if s]
+        assert all(s == c for s in nonempty[:-1])            # equal but for the last non-empty chunk
+
+
+def test_bad_arguments(built):
+    import ctypes as C
+    from reduction_reducer_gb300 import InvalidArg
+    from reduction_reducer_gb300.sharded import shard_range
+    for args in [(-1, 2, 0), (10, 0, 0), (10, 2, 2), (10, 2, -1)]:
+        with pytest.raises(InvalidArg):
+            shard_range(*args)
+    assert built.ddp_shard_range(10, 2, 1, None, None, None) == 0
+    assert built.ddp_shard_mean(0, 0, None, None, 4, None) == -1      # G < 1
+    assert built.ddp_shard_mean(65, 0, None, None, 4, None) == -1     # G > 64
+    assert built.ddp_shard_mean(2, 7, None, None, 4, None) == -1      # dtype
+    assert built.ddp_shard_mean(2, 0, None, None, 0, None) == 0       # nothing to do
+    assert built.ddp_shard_mean(2, 0, (C.c_void_p * 2)(None, None), None, 4, None) == -1
+
+
+RAGGED = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 7001, 0, 9, 30007, 16, 31]
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _to_np(t, dtype):
+    return t.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else t.numpy()
+
+
+def _rank(rank, world, port, dtype, cap):
+    import torch.distributed as dist
+    from reduction_reducer_gb300.sharded import ShardedAllReduce
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        elem = 4 if dtype == "f32" else 2
+        members, locs = assign_buckets(RAGGED, elem, cap)
+        # every replica's gradients (seeded per replica); this rank holds its own
+        offs, total = gen.packed_offsets(RAGGED, 1)
+        grads = []
+        for r in range(world):
+            flat = gen.draw_flat_np(total, r, 0, dtype)
+            grads.append([flat[o:o + n] for o, n in zip(offs, RAGGED)])
+        want_arena, _ = reduce_buckets(grads, members, locs, RAGGED)
+        mine = gather_buckets([grads[rank]], members, locs, RAGGED)[0]
+
+        def oracle_mean(parts, out):
+            out.copy_(torch.from_numpy(replica_mean([_to_np(p, dtype) for p in parts])))
+
+        reduce = ShardedAllReduce(dist, None, dtype, mean=oracle_mean)
+        lens = [sum(RAGGED[v] for v in m) for m in members]
+        starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        for b in range(len(members)):            # bucket-index order on every rank
+            local = torch.from_numpy(mine[b].view(np.int16)).view(torch.bfloat16) if dtype == "bf16" \
+                else torch.from_numpy(mine[b].copy())
+            out = torch.full((lens[b],), float("nan"))
+            reduce(local, out)
+            got = out.numpy()
+            want = want_arena[starts[b]:starts[b + 1]]
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (rank, b)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,dtype,cap", [(2, "f32", 16 * 1024), (3, "bf16", 8 * 1024), (3, "f32", 0)])
+def test_sharded_allreduce_gloo_equals_unsharded_oracle(built, world, dtype, cap):
+    import torch.multiprocessing as mp
+    mp.start_processes(_rank, args=(world, _free_port(), dtype, cap), nprocs=world, join=True, start_method="spawn")
