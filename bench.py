@@ -473,6 +473,73 @@ def run_sharded(args):
     return 0
 
 
+def run_mix_rates(args):
+    """Roofline context: the streaming rate GB300's HBM gives plain torch
+    kernels by read:write mix (4 GiB fp32 buffers, best of 20 with CUDA
+    events), beside the fused pass on the BERT-large shapes for W = 1 .. 32
+    replicas (one mark_ready_many call, reverse order, library defaults).
+    The pass at W replicas reads W and writes 2 units per element: at W = 4
+    it has the 2:1 mix of torch.add."""
+    import torch
+    from reduction_reducer_gb300 import Reducer
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+
+    def best_ms(fn, reps=20, warm=3):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    n = 1 << 30
+    x = torch.empty(n, device=dev).normal_()
+    y = torch.empty(n, device=dev).normal_()
+    z = torch.empty(n, device=dev)
+    out = {}
+    for name, fn, nbytes in (("torch copy_ (1 read : 1 write)", lambda: z.copy_(x), 8 * n),
+                             ("torch add (2 reads : 1 write)", lambda: torch.add(x, y, out=z), 12 * n),
+                             ("torch fill_ (write only)", lambda: z.fill_(1.0), 4 * n),
+                             ("torch sum (read only)", lambda: x.sum(), 4 * n)):
+        ms = best_ms(fn)
+        out[name] = {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 3)}
+    del x, y, z
+    torch.cuda.empty_cache()
+    numel = shapes.numels(shapes.bert_large())
+    offs, total = gen.packed_offsets(numel, 64)
+    order = gen.reverse_order(len(numel))
+    stream = torch.cuda.Stream(device=dev)
+    N = sum(numel)
+    for W in (1, 2, 4, 8, 16, 32):
+        flat = [gen.draw_flat_torch(total, r, 0, "f32", dev) for r in range(W)]
+        grads = [[f[o:o + k] for o, k in zip(offs, numel)] for f in flat]
+        red = Reducer(numel, "f32", 25 * MIB)
+        arena = torch.empty(red.arena_numel(), device=dev)
+        res = torch.empty(total, device=dev)
+        red.bind(grads, arena, [res[o:o + k] for o, k in zip(offs, numel)])
+
+        def step():
+            red.begin_iteration()
+            red.mark_ready_many(order, stream)
+        with torch.cuda.stream(stream):
+            ms, _, _ = time_steps(torch, stream, step, args.steps, args.warmup)
+        t = ms / args.steps
+        out[f"fused pass, BERT-large shapes, W={W} ({W} reads : 2 writes)"] = {
+            "gbs": round(view_bytes(W, N, 4) / (t * 1e-3) / 1e9, 1), "ms": round(t, 4)}
+        red.destroy()
+        del flat, grads, arena, res
+        torch.cuda.empty_cache()
+    print(json.dumps({"mix_rates": out}), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -1072,6 +1139,8 @@ def main():
     ap.add_argument("--sharded", action="store_true",
                     help="one replica per rank: the bucket all-reduce across ranks (NCCL; reduce-scatter as an "
                          "all-to-all of raw chunks + owner mean, then all-gather)")
+    ap.add_argument("--mix-rates", action="store_true",
+                    help="roofline context: torch streaming rates by read:write mix and the fused pass for W = 1 .. 32")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--cpu-config-s", type=float, default=2.0,
                     help="seconds of oracle work per configuration (per_config cpu_oracle)")
@@ -1081,6 +1150,8 @@ def main():
         return run_reference(args)
     if args.sharded:
         return run_sharded(args)
+    if args.mix_rates:
+        return run_mix_rates(args)
     if args.workload == "nosync_resnet50":
         return run_nosync_only(args)
     if args.workload == "gpt2_medium":

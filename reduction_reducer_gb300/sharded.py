@@ -80,25 +80,28 @@ class ShardedAllReduce:
         import torch
         n = local.numel()
         G = self.G
-        chunk, lo, hi = shard_range(n, G, self.rank)
-        send = self._buf("send", G * chunk, local.dtype, local)
-        send[:n].copy_(local)
-        if G * chunk > n:
-            send[n:].zero_()                 # the last chunk's tail: sent, never used
-        recv = self._buf("recv", G * chunk, local.dtype, local)
-        self.dist.all_to_all_single(recv, send, group=self.group)
+        plan = [shard_range(n, G, c) for c in range(G)]
+        chunk, lo, hi = plan[self.rank]
+        mine_n = hi - lo
+        # reduce-scatter, exact: chunk c of the local bucket goes to rank c as
+        # it is (uneven splits: the last non-empty chunk is shorter), and this
+        # rank receives every replica's values of its own chunk, in rank order
+        recv = self._buf("recv", G * mine_n, local.dtype, local)
+        self.dist.all_to_all_single(recv, local, output_split_sizes=[mine_n] * G,
+                                    input_split_sizes=[h - l for _, l, h in plan], group=self.group)
         mine = self._buf("mine", chunk, torch.float32, local)
-        parts = [recv[c * chunk:c * chunk + (hi - lo)] for c in range(G)]   # replica c's values of my chunk
-        if hi > lo:
+        if mine_n > 0:
+            parts = [recv[c * mine_n:(c + 1) * mine_n] for c in range(G)]   # replica c's values of my chunk
             if self.mean is not None:
-                self.mean(parts, mine[:hi - lo])
+                self.mean(parts, mine[:mine_n])
             else:
-                shard_mean(parts, mine[:hi - lo], self.dtype, int(torch.cuda.current_stream().cuda_stream))
-        if chunk > hi - lo:
-            mine[hi - lo:].zero_()
+                shard_mean(parts, mine[:mine_n], self.dtype, int(torch.cuda.current_stream().cuda_stream))
+        if chunk > mine_n:
+            mine[mine_n:].zero_()            # padding of a short chunk: gathered, never used
+        # all-gather of equal (padded) chunks; they tile [0, n) in rank order
         gathered = self._buf("gathered", G * chunk, torch.float32, local)
         self.dist.all_gather_into_tensor(gathered, mine, group=self.group)
-        out.copy_(gathered[:n])              # the chunks tile [0, n) in rank order
+        out.copy_(gathered[:n])
 
 
 def sharded_hook(dist, replica_buffer, arena, group=None, dtype: str = "f32"):
