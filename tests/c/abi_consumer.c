@@ -74,6 +74,23 @@ int main(void) {
     CHECK(ddp_begin_iteration(ctx) == DDP_OK);
     CHECK(ddp_status_string(DDP_ERR_ALREADY_READY) != NULL);
 
+    /* launch options of the batched call and of built-in hooks */
+    int64_t value = -1;
+    CHECK(ddp_get_option(ctx, DDP_OPT_COALESCE_ELEMS, &value) == DDP_OK && value == (int64_t)1 << 21);
+    CHECK(ddp_set_option(ctx, DDP_OPT_COALESCE_ELEMS, -1) == DDP_ERR_INVALID_ARG);
+    CHECK(ddp_get_option(ctx, DDP_OPT_HOOK_FUSED, &value) == DDP_OK && value == 1);
+
+    /* ownership plan of the all-reduce across ranks: 100 elements over 3
+     * ranks -> chunks of 40 (ceil(100 / 3) = 34, rounded up to 8) */
+    int64_t chunk = 0, lo = -1, hi = -1, at = 0;
+    for (int32_t g = 0; g < 3; ++g) {
+        CHECK(ddp_shard_range(100, 3, g, &chunk, &lo, &hi) == DDP_OK);
+        CHECK(chunk == 40 && lo == at);
+        at = hi;
+    }
+    CHECK(at == 100 && lo == 80);
+    CHECK(ddp_shard_range(100, 3, 3, &chunk, &lo, &hi) == DDP_ERR_INVALID_ARG);
+
     ddp_destroy(ctx);
     if (failures) return 1;
     printf("c abi ok\n");
