@@ -16,8 +16,10 @@ elements per second are W*N / time.  Inputs (5.4 GB read per step) exceed
 the 129 MB L2, so no flush is needed between steps.
 
 Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
-own independent replica of the workload (the path needs no collective on one
-GPU: "replicas only"); value = total bytes over ranks / max time over ranks.
+own independent replica of the workload (the W replicas of one emulation
+live on one GPU and need no collective: "replicas only"); value = total
+bytes over ranks / max time over ranks.  ``--sharded`` instead puts one
+replica on each rank and all-reduces every bucket across the ranks (NCCL).
 
 ``--impl reference`` times the CPU oracle (the plain NumPy restatement of the
 same path) on a bounded sample of the same workload on the host cores.
@@ -141,7 +143,8 @@ class ClockSampler:
 class Workload:
     """Device buffers, reducer and step function of one configuration."""
 
-    def __init__(self, name, torch, device, cap_mib=25, n_out=1, driver="hooks", layout="params", layers=None):
+    def __init__(self, name, torch, device, cap_mib=25, n_out=1, driver="hooks", layout="params", layers=None,
+                 lib_path=None):
         from reduction_reducer_gb300 import Reducer
         self.torch = torch
         spec = shapes.WORKLOADS[name]
@@ -156,7 +159,7 @@ class Workload:
         self.cap = cap_mib * MIB
         self.n_out = n_out
         self.driver = driver
-        self.red = Reducer(self.numel, self.dtype, self.cap)
+        self.red = Reducer(self.numel, self.dtype, self.cap, **({"lib_path": lib_path} if lib_path else {}))
         self.B = self.red.B
         if layout == "params":          # per-parameter tensors, registration order
             offs, total = gen.packed_offsets(self.numel, 64)
@@ -537,6 +540,67 @@ def run_mix_rates(args):
         del flat, grads, arena, res
         torch.cuda.empty_cache()
     print(json.dumps({"mix_rates": out}), flush=True)
+    return 0
+
+
+def run_trace(args):
+    """Launch boundaries of one BERT-large iteration taken apart, from the
+    trace build's per-CTA %globaltimer stamps (libddpreducer_trace.so, built
+    here when missing): for every pair of consecutive launches A -> B, with
+    one mark_ready call per event (B waits for A) and in one mark_ready_many
+    call (B chained after A).  Stamps: t0 CTA entry, t1 past the wait (past
+    the trigger when chained), t2 first stage consumed, t3 last stage
+    consumed.  Per pair: A's tail (last t3 - median t3 of A), B's release
+    (first t1 of B - last t3 of A), B's first data after its release, and
+    the gap between A's last and B's first consumed stage (negative: they
+    overlap)."""
+    import torch
+    from reduction_reducer_gb300 import _lib, build
+    from reduction_reducer_gb300.reducer import read_launch_trace
+    if not os.path.exists(_lib.TRACE_LIB_PATH):
+        build.build_trace()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    wl = Workload("bert_large", torch, dev, 25, n_out=1, driver="events", layers=args.layers,
+                  lib_path=_lib.TRACE_LIB_PATH)
+    out = {}
+    for drv in ("events", "hooks"):
+        wl.driver = drv
+        with torch.cuda.stream(stream):
+            ms, _, _ = time_steps(torch, stream, lambda: wl.step(stream), 10, 3)
+            torch.cuda.synchronize()
+            _, _, seq0 = read_launch_trace()
+            wl.step(stream)
+            torch.cuda.synchronize()
+        buf, grid, seq1 = read_launch_trace()
+        n = seq1 - seq0
+        if n > _lib.TRACE_LAUNCHES:
+            raise RuntimeError("more launches in one iteration than trace slots")
+        spans = []
+        for i in range(seq0, seq1):
+            slot = i % _lib.TRACE_LAUNCHES
+            t = buf[slot, :min(grid[slot], _lib.TRACE_CTAS)].astype(np.int64)
+            busy = t[:, 3] > 0                        # CTAs that consumed staged work (0: none)
+            first = t[t[:, 2] > 0, 2]
+            spans.append({"entry0": int(t[:, 0].min()), "release0": int(t[:, 1].min()),
+                          "first0": int(first.min()), "end_med": int(np.median(t[busy, 3])),
+                          "end": int(t[busy, 3].max()), "ctas": int(t.shape[0])})
+        pairs = list(zip(spans[:-1], spans[1:]))
+        med = lambda xs: round(float(np.median(xs)) / 1e3, 2)
+        stamps = np.unique(buf[buf > 0])
+        res = int(np.diff(stamps).min()) if stamps.size > 1 else None
+        out[drv] = {"launches": n, "ms_per_step_untraced_timing": round(ms / 10, 4),
+                    "median_us": {"A_tail": med([a["end"] - a["end_med"] for a, _ in pairs]),
+                                  "B_release_after_A_end": med([b["release0"] - a["end"] for a, b in pairs]),
+                                  "B_first_data_after_release": med([b["first0"] - b["release0"] for _, b in pairs]),
+                                  "gap_A_last_to_B_first_stage": med([b["first0"] - a["end"] for a, b in pairs]),
+                                  "launch_span": med([s["end"] - s["first0"] for s in spans])},
+                    "timer_resolution_ns": res,
+                    "step_span_us": round((spans[-1]["end"] - spans[0]["entry0"]) / 1e3, 1)}
+    wl.free()
+    print(json.dumps({"trace": out, "workload": "bert_large" + (f"_{args.layers}layers" if args.layers else ""),
+                      "kernel": "bucket_reduce_tma_kernel (trace build)"}), flush=True)
     return 0
 
 
@@ -950,7 +1014,7 @@ def hook_config(torch, device, keep, timed, out):
         rb = [torch.empty(wl.red.arena_numel(), dtype=torch.float32, device=device) for _ in range(wl.W)]
         wl.red.register_comm_hook(hook, rb)
         timed(wl, f"bert_large_hook_{hook}", f"register_comm_hook('{hook}'): the hook's arithmetic inside the fused "
-              "bucket pass (one launch per readiness event, nothing gathered), W*N*4 + 2*N*4 bytes")
+              "bucket pass (nothing gathered), W*N*4 + 2*N*4 bytes")
         wl.free()
         del rb
         torch.cuda.empty_cache()
@@ -1139,6 +1203,8 @@ def main():
     ap.add_argument("--sharded", action="store_true",
                     help="one replica per rank: the bucket all-reduce across ranks (NCCL; reduce-scatter as an "
                          "all-to-all of raw chunks + owner mean, then all-gather)")
+    ap.add_argument("--trace", action="store_true",
+                    help="launch boundaries of one BERT-large iteration from the trace build's per-CTA timestamps")
     ap.add_argument("--mix-rates", action="store_true",
                     help="roofline context: torch streaming rates by read:write mix and the fused pass for W = 1 .. 32")
     ap.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
@@ -1152,6 +1218,8 @@ def main():
         return run_sharded(args)
     if args.mix_rates:
         return run_mix_rates(args)
+    if args.trace:
+        return run_trace(args)
     if args.workload == "nosync_resnet50":
         return run_nosync_only(args)
     if args.workload == "gpt2_medium":

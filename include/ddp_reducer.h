@@ -397,7 +397,7 @@ enum ddp_option {
                                      raised to 4 KiB per tile for many streams (W > 8, or W > 4 with
                                      a bound last step) */
     DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernels: CTAs per SM, 1..8, or 0 (default): two resident
-                                     waves (four for the single launch of ddp_reduce_all) */
+                                     waves (eight for the single launch of ddp_reduce_all) */
     DDP_OPT_AUTO_MIN_ELEMS = 8,   /* kernel 2: median bucket length (elements) from which the bulk-copy
                                      kernel is used (default 6 x 2^20) */
     DDP_OPT_CHAINED = 9,          /* 1: chained launches (default 0).  The caller guarantees that every
@@ -453,6 +453,22 @@ int ddp_get_debug_record(ddp_ctx* ctx, int32_t* code, int64_t* index);
  * wait ended as designed).  Synchronous; allocates and frees 4 bytes.  The
  * pages have no counterpart.  Errors: INVALID_ARG (limit out of range), CUDA. */
 int ddp_selftest_bounded_wait(int64_t limit_cycles, int32_t* code);
+
+/* Launch trace of a library built with -DDDP_TRACE (libddpreducer_trace.so,
+ * `python -m reduction_reducer_gb300.build --trace`): for the last
+ * DDP_TRACE_LAUNCHES launches of the bulk-copy bucket kernel (all contexts of
+ * the process), per CTA (the first DDP_TRACE_CTAS of each grid), four
+ * %globaltimer stamps in ns: entry, past the wait for the preceding grid (a
+ * chained launch: past its trigger), the consumers' first stage and their
+ * last.  Launch number i (from 0) sits in slot i % DDP_TRACE_LAUNCHES.
+ *   out   host array [DDP_TRACE_LAUNCHES * DDP_TRACE_CTAS * 4] or NULL
+ *   grid  host array [DDP_TRACE_LAUNCHES] or NULL: CTAs of each slot's launch
+ *   seq   receives the number of launches traced so far (-1: not a trace build)
+ * Synchronous (waits for the device).  Diagnostics only; the pages have no
+ * counterpart.  Errors: CUDA. */
+#define DDP_TRACE_LAUNCHES 64
+#define DDP_TRACE_CTAS 4096
+int ddp_read_launch_trace(uint64_t* out, int32_t* grid, int64_t* seq);
 
 /* Kernel launches issued by this context since creation. */
 int ddp_get_launch_count(const ddp_ctx* ctx, int64_t* launches);

@@ -83,6 +83,7 @@ SIGNATURES = {
     "ddp_shard_range": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
                                   C.POINTER(C.c_int64)]),
     "ddp_shard_mean": (C.c_int, [C.c_int32, C.c_int, C.POINTER(C.c_void_p), C.c_void_p, C.c_int64, C.c_void_p]),
+    "ddp_read_launch_trace": (C.c_int, [C.POINTER(C.c_uint64), C.POINTER(C.c_int32), C.POINTER(C.c_int64)]),
     "ddp_status_string": (C.c_char_p, [C.c_int]),
     "ddp_last_error": (C.c_char_p, [C.c_void_p]),
     "ddp_destroy": (None, [C.c_void_p]),
@@ -92,6 +93,8 @@ _lib = None
 
 
 DEBUG_LIB_PATH = os.path.join(PKG, "libddpreducer_debug.so")
+TRACE_LIB_PATH = os.path.join(PKG, "libddpreducer_trace.so")
+TRACE_LAUNCHES, TRACE_CTAS = 64, 4096
 _variants = {}
 
 

@@ -1,6 +1,6 @@
 """Build the C-ABI library ``libddpreducer.so`` in-tree with nvcc for sm_103a.
 
-    python -m reduction_reducer_gb300.build [-v] [--all]
+    python -m reduction_reducer_gb300.build [-v] [--all | --trace]
 
 Translation units are compiled in parallel into ``_build/`` next to this
 file and linked (static CUDA runtime) into ``libddpreducer.so`` beside the
@@ -78,6 +78,18 @@ def build_debug(verbose: bool = False) -> str:
     return build(verbose, extra_flags=("-DDDP_DEBUG=1",), lib_path=DEBUG_LIB, build_dir=DEBUG_BUILD)
 
 
+# Launch-trace variant (-DDDP_TRACE): the bulk-copy kernel records
+# %globaltimer stamps per CTA (ddp_read_launch_trace).  Built on demand, not by
+# build_all: a diagnostics build.
+TRACE_BUILD = os.path.join(PKG, "_build_trace")
+TRACE_LIB = os.path.join(PKG, "libddpreducer_trace.so")
+
+
+def build_trace(verbose: bool = False) -> str:
+    """The launch-trace variant at ``TRACE_LIB``."""
+    return build(verbose, extra_flags=("-DDDP_TRACE=1",), lib_path=TRACE_LIB, build_dir=TRACE_BUILD)
+
+
 def build_all(verbose: bool = False):
     """Release and bounds-checking builds, compiled side by side."""
     with cf.ThreadPoolExecutor(max_workers=2) as ex:
@@ -87,4 +99,7 @@ def build_all(verbose: bool = False):
 
 
 if __name__ == "__main__":
-    print(build_all(verbose="-v" in sys.argv) if "--all" in sys.argv else build(verbose="-v" in sys.argv))
+    if "--trace" in sys.argv:
+        print(build_trace(verbose="-v" in sys.argv))
+    else:
+        print(build_all(verbose="-v" in sys.argv) if "--all" in sys.argv else build(verbose="-v" in sys.argv))

@@ -153,6 +153,8 @@ struct ReduceParams {
     int stages;         // pipelined kernel: ring depth
     int tile;           // pipelined kernel: elements per replica per stage
     int chain;          // 1: follows a launch of the same iteration (see pdl_enter)
+    int first_wave;     // pipelined kernel: CTAs resident at once (the first wave of the grid)
+    int trace_slot;     // trace builds (-DDDP_TRACE): the launch's row of the launch trace
 };
 
 // Entry/exit ordering with the previous launch in the stream.

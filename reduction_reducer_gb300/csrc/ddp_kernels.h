@@ -114,6 +114,10 @@ cudaError_t launch_accumulate_tma(const AccPair* pairs, int n, const LaunchCfg& 
 // bounded wait writes its timeout code into *status (ddp_kernels_tma.cu).
 cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t stream);
 
+// The launch trace of a -DDDP_TRACE build (see ddp_read_launch_trace);
+// *seq = -1 in other builds.
+cudaError_t read_launch_trace(unsigned long long* out, int* grid, long long* seq);
+
 // Bulk-copy (TMA) pipelined variant of launch_reduce, in ddp_kernels_tma.cu.
 cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, float* arena,
                               long long lo, long long hi, int s0, int s1, float inv_w,

@@ -31,6 +31,7 @@
 
 #include "ddp_device.cuh"
 #include "ddp_kernels.h"
+#include "ddp_reducer.h"
 
 namespace ddpk {
 
@@ -48,6 +49,40 @@ constexpr long long kMinCopyBytes = 4096;          // smallest per-stream copy a
 #define DDP_PREFETCH_STAGES 2
 #endif
 constexpr long long kPrefetchStages = DDP_PREFETCH_STAGES;   // stages prefetched before a launch's wait
+#ifndef DDP_PREFETCH_WAVES
+#define DDP_PREFETCH_WAVES 2
+#endif
+constexpr int kPrefetchWaves = DDP_PREFETCH_WAVES;            // waves of CTAs that prefetch (0: every CTA)
+
+// Launch trace (builds with -DDDP_TRACE only; ddp_read_launch_trace): per
+// launch of the bucket pass, per CTA, four %globaltimer stamps -- entry, past
+// the wait for the preceding grid (chained launches: past the trigger), the
+// first stage the consumers take, and the last -- so that the boundary between
+// two launches can be taken apart: the predecessor's tail, the release of the
+// wait, the first data.  Release builds record nothing.
+#ifdef DDP_TRACE
+constexpr bool kTrace = true;
+__device__ unsigned long long g_launch_trace[DDP_TRACE_LAUNCHES][DDP_TRACE_CTAS][4];
+int g_trace_grid[DDP_TRACE_LAUNCHES];
+long long g_trace_seq = 0;
+std::mutex g_trace_mutex;
+#else
+constexpr bool kTrace = false;
+#endif
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void trace_stamp(const ReduceParams& p, int which, unsigned long long t) {
+#ifdef DDP_TRACE
+    if (blockIdx.x < DDP_TRACE_CTAS) g_launch_trace[p.trace_slot][blockIdx.x][which] = t;
+#else
+    (void)p; (void)which; (void)t;
+#endif
+}
 
 // status codes written by bounded waits
 constexpr int kStatusEmptyTimeout = 1;
@@ -173,6 +208,13 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    if constexpr (kTrace) {   // entry; the consumers' stamps start empty (0) for this launch
+        if (threadIdx.x == 0) {
+            trace_stamp(p, 0, global_ns());
+            trace_stamp(p, 2, 0);
+            trace_stamp(p, 3, 0);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(full + i), 1);
@@ -199,8 +241,14 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
     // the lines arrive during that launch's tail and the first bulk copies
     // after the wait hit L2.  A prefetch moves nothing the program observes:
     // inputs a preceding grid is still writing are read again, coherently, by
-    // the copies after the wait.
-    if (!idle && !p.chain && kPrefetchStages > 0 && warp == 0) {
+    // the copies after the wait.  The CTAs of the first two waves prefetch:
+    // the first wave waits for the preceding grid, the second starts as the
+    // first retires and ramps faster with two more stages in flight; later
+    // waves gain nothing from it.  GB300, against every CTA prefetching:
+    // one reduce_all launch over ResNet-50 W=8 +1.7 %, BERT-large ties in
+    // every driving mode; the first wave alone lost 0.7 % per event.
+    if (!idle && !p.chain && kPrefetchStages > 0 && warp == 0 &&
+        (kPrefetchWaves == 0 || static_cast<int>(blockIdx.x) < kPrefetchWaves * p.first_wave)) {
         long long k = 0;
         walk<N>(
             p, s, x, y,
@@ -216,6 +264,9 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
     }
     __syncthreads();
     if (!p.chain) pdl_enter(0);   // wait for every earlier grid, then let the successor start
+    if constexpr (kTrace) {
+        if (threadIdx.x == 0) trace_stamp(p, 1, global_ns());
+    }
     if (idle) {   // whole CTA, before any copy is issued
         if (threadIdx.x == 0) pdl_exit(p.chain, p.piece >= kHoldAllPiece);
         return;
@@ -284,6 +335,9 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
             const int st = static_cast<int>(k % S);
             const uint32_t use = static_cast<uint32_t>(k / S);
             mbar_wait(smem_u32(full + st), use & 1u, p.status, kStatusFullTimeout, failed);
+            if constexpr (kTrace) {
+                if (k == 0 && tc == 0) trace_stamp(p, 2, global_ns());
+            }
             const Tin* base = ring + st * stage_elems;
             float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
             const unsigned long long mk = seg_mask(mask, sg - p.s0);
@@ -338,6 +392,9 @@ bucket_reduce_tma_kernel(const __grid_constant__ ReduceParams p, const __grid_co
             float* const* dst = p.seg_dst + static_cast<long long>(sg) * p.n_out;
             reduce_scalar<Tin, ADD, CMP>(p, src, dst, a0, lo, hi, W, tc, nct, seg_mask(mask, sg - p.s0));
         });
+    if constexpr (kTrace) {
+        if (tc == 0) trace_stamp(p, 3, global_ns());
+    }
 }
 
 // ------------------------------------------------------------------ accumulate
@@ -605,7 +662,7 @@ int resident_ctas(K k, long long smem) {
 // against one CTA per SM: BERT-large W=4 7.05 -> 7.12 TB/s, GPT-2-medium at
 // cap 25 and 100 +1.6 / +1.3 %, ResNet-50 W=8 +0.7 %, no_sync ResNet-50 W=16
 // micro-steps +6 %.  A single launch over a whole iteration (reduce_all)
-// takes four: BERT-large 6.78 -> 6.97, ResNet-50 6.71 -> 6.77 TB/s.
+// takes eight: BERT-large 6.78 (one wave) -> 6.97 (four) -> 7.07 TB/s.
 template <typename K>
 int tma_ctas(const LaunchCfg& cfg, K k, long long smem) {
     const int waves = cfg.tma_waves > 0 ? cfg.tma_waves : 2;
@@ -725,6 +782,7 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     cudaError_t e = mask ? ensure_smem_attr(pick_tma<SegMask>(in, W)) : ensure_smem_attr(plain);
     if (e != cudaSuccess) return e;
     const int per_sm = mask ? tma_ctas(cfg, pick_tma<SegMask>(in, W), smem) : tma_ctas(cfg, plain, smem);
+    p.first_wave = cfg.sms * (mask ? resident_ctas(pick_tma<SegMask>(in, W), smem) : resident_ctas(plain, smem));
 
     const long long span = hi - p.base;
     long long grid = static_cast<long long>(cfg.sms) * per_sm;
@@ -743,10 +801,38 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = cfg.pdl ? 1 : 0;
+#ifdef DDP_TRACE
+    {
+        std::lock_guard<std::mutex> lock(g_trace_mutex);
+        p.trace_slot = static_cast<int>(g_trace_seq % DDP_TRACE_LAUNCHES);
+        g_trace_grid[p.trace_slot] = static_cast<int>(grid);
+        ++g_trace_seq;
+    }
+#endif
     e = mask ? cudaLaunchKernelEx(&lc, pick_tma<SegMask>(in, W), p, *mask)
              : cudaLaunchKernelEx(&lc, plain, p, NoMask{});
     if (e == cudaSuccess && launches) ++*launches;
     return e;
+}
+
+cudaError_t read_launch_trace(unsigned long long* out, int* grid, long long* seq) {
+#ifdef DDP_TRACE
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    if (out) {
+        e = cudaMemcpyFromSymbol(out, g_launch_trace, sizeof(g_launch_trace));
+        if (e != cudaSuccess) return e;
+    }
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    if (grid)
+        for (int i = 0; i < DDP_TRACE_LAUNCHES; ++i) grid[i] = g_trace_grid[i];
+    if (seq) *seq = g_trace_seq;
+#else
+    (void)out;
+    (void)grid;
+    if (seq) *seq = -1;
+#endif
+    return cudaSuccess;
 }
 
 }  // namespace ddpk

@@ -75,6 +75,19 @@ def _ptr_array(ptrs):
     return arr
 
 
+def read_launch_trace(lib_path: str = _lib.TRACE_LIB_PATH):
+    """The launch trace of the trace build (``ddp_read_launch_trace``):
+    (stamps [TRACE_LAUNCHES, TRACE_CTAS, 4] uint64 ns, grid per slot, launches
+    traced so far; -1 for a build without the trace)."""
+    import numpy as np
+    lib = _lib.load(lib_path)
+    buf = np.zeros((_lib.TRACE_LAUNCHES, _lib.TRACE_CTAS, 4), np.uint64)
+    grid = (C.c_int32 * _lib.TRACE_LAUNCHES)()
+    seq = C.c_int64()
+    _check_status(lib.ddp_read_launch_trace(buf.ctypes.data_as(C.POINTER(C.c_uint64)), grid, C.byref(seq)), None)
+    return buf, list(grid), seq.value
+
+
 class Reducer:
     """One bucketed reducer context (``ddp_ctx``)."""
 
