@@ -550,10 +550,10 @@ def run_trace(args):
     one mark_ready call per event (B waits for A) and in one mark_ready_many
     call (B chained after A).  Stamps: t0 CTA entry, t1 past the wait (past
     the trigger when chained), t2 first stage consumed, t3 last stage
-    consumed.  Per pair: A's tail (last t3 - median t3 of A), B's release
-    (first t1 of B - last t3 of A), B's first data after its release, and
-    the gap between A's last and B's first consumed stage (negative: they
-    overlap)."""
+    consumed.  Per pair: A's tail (last t3 - 90th percentile of A's t3: the
+    time its last tenth of CTAs takes to finish), B's release (first t1 of
+    B - last t3 of A), B's first data after its release, and the gap between
+    A's last and B's first consumed stage (negative: they overlap)."""
     import torch
     from reduction_reducer_gb300 import _lib, build
     from reduction_reducer_gb300.reducer import read_launch_trace
@@ -584,14 +584,14 @@ def run_trace(args):
             busy = t[:, 3] > 0                        # CTAs that consumed staged work (0: none)
             first = t[t[:, 2] > 0, 2]
             spans.append({"entry0": int(t[:, 0].min()), "release0": int(t[:, 1].min()),
-                          "first0": int(first.min()), "end_med": int(np.median(t[busy, 3])),
+                          "first0": int(first.min()), "end_p90": int(np.percentile(t[busy, 3], 90)),
                           "end": int(t[busy, 3].max()), "ctas": int(t.shape[0])})
         pairs = list(zip(spans[:-1], spans[1:]))
         med = lambda xs: round(float(np.median(xs)) / 1e3, 2)
         stamps = np.unique(buf[buf > 0])
         res = int(np.diff(stamps).min()) if stamps.size > 1 else None
         out[drv] = {"launches": n, "ms_per_step_untraced_timing": round(ms / 10, 4),
-                    "median_us": {"A_tail": med([a["end"] - a["end_med"] for a, _ in pairs]),
+                    "median_us": {"A_last_tenth_of_ctas": med([a["end"] - a["end_p90"] for a, _ in pairs]),
                                   "B_release_after_A_end": med([b["release0"] - a["end"] for a, b in pairs]),
                                   "B_first_data_after_release": med([b["first0"] - b["release0"] for _, b in pairs]),
                                   "gap_A_last_to_B_first_stage": med([b["first0"] - a["end"] for a, b in pairs]),
