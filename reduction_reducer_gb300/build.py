@@ -79,8 +79,7 @@ def build_debug(verbose: bool = False) -> str:
 
 
 # Launch-trace variant (-DDDP_TRACE): the bulk-copy kernel records
-# %globaltimer stamps per CTA (ddp_read_launch_trace).  Built on demand, not by
-# build_all: a diagnostics build.
+# %globaltimer stamps per CTA (ddp_read_launch_trace); a diagnostics build.
 TRACE_BUILD = os.path.join(PKG, "_build_trace")
 TRACE_LIB = os.path.join(PKG, "libddpreducer_trace.so")
 
@@ -91,11 +90,12 @@ def build_trace(verbose: bool = False) -> str:
 
 
 def build_all(verbose: bool = False):
-    """Release and bounds-checking builds, compiled side by side."""
-    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+    """Release, bounds-checking and launch-trace builds, compiled side by side."""
+    with cf.ThreadPoolExecutor(max_workers=3) as ex:
         rel = ex.submit(build, verbose)
         dbg = ex.submit(build_debug, verbose)
-        return rel.result(), dbg.result()
+        trc = ex.submit(build_trace, verbose)
+        return rel.result(), dbg.result(), trc.result()
 
 
 if __name__ == "__main__":
