@@ -106,16 +106,21 @@ class ShardedAllReduce:
 
 def sharded_hook(dist, replica_buffer, arena, group=None, dtype: str = "f32"):
     """A communication hook (for ``Reducer.register_comm_hook(hook,
-    [replica_buffer])`` on a reducer bound with W = 1) that all-reduces every
-    bucket across the ranks of ``group`` with ``ShardedAllReduce``.
-    ``replica_buffer`` and ``arena`` are the tensors the reducer gathers
-    into and reduces into; the hook runs its exchange on the library's
-    stream."""
+    [replica_buffer])`` on a reducer bound with W = 1: this rank's replica)
+    that all-reduces every bucket across the ranks of ``group`` with
+    ``ShardedAllReduce``.  ``replica_buffer`` is the tensor the bucket's
+    gradients lie in -- the registered replica buffer, or, when the hook was
+    registered without one, the flat gradient tensor whose views in bucket
+    order the reducer was bound to -- and ``arena`` the bucket arena the
+    reducer reduces into.  The hook runs its exchange on the library's
+    stream; a bucket of another replica count fails the launch (HookError)."""
     import torch
     reduce = ShardedAllReduce(dist, group, dtype)
     esz = replica_buffer.element_size()
 
     def hook(bucket, stream):
+        if bucket.W != 1:
+            return 1                          # one replica per rank: the others are the other ranks'
         n = int(bucket.numel)
         if n == 0:
             return 0
