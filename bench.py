@@ -970,6 +970,13 @@ def extra_configs(torch, device, stream, args, dist, keep):
             wl.red.set_option(_lib.OPT_COALESCE_ELEMS, 0)
             timed(wl, "gpt2_medium_w8_bf16_cap0_launch_per_event",
                   "GPT-2-medium bf16 W=8, cap 0, DDP_OPT_COALESCE_ELEMS = 0: one launch per releasing event")
+        if cap in (0, 25):
+            # one mark_ready call per event, as a backward pass reports its hooks:
+            # per-gradient buckets against 25 MiB ones (the pages' bucketing experiment)
+            wl.driver = "events"
+            timed(wl, f"gpt2_medium_w8_bf16_cap{cap}_event_calls",
+                  f"GPT-2-medium bf16 W=8, cap {cap} MiB, one mark_ready call per event (launches wait for their "
+                  "predecessor)")
         wl.free()
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
