@@ -98,3 +98,94 @@ def test_sharded_hook_nccl_single_rank(dtype):
         red.destroy()
     finally:
         dist.destroy_process_group()
+
+
+class _ThreadGroup:
+    """G ranks of one process, one host thread each, on this GPU: the two
+    collectives the sharded all-reduce uses, exchanged through host-side
+    slots between barriers (no kernel waits for another)."""
+
+    def __init__(self, G):
+        import threading
+        self.G = G
+        self.barrier = threading.Barrier(G, timeout=60)
+        self.slots = [None] * G
+
+    def member(self, rank):
+        grp = self
+
+        class _Dist:
+            def get_world_size(self, group=None):
+                return grp.G
+
+            def get_rank(self, group=None):
+                return rank
+
+            def _publish(self, value):
+                torch.cuda.synchronize()          # what this rank enqueued is done before others read it
+                grp.slots[rank] = value
+                grp.barrier.wait()
+
+            def all_to_all_single(self, out, inp, output_split_sizes=None, input_split_sizes=None, group=None):
+                self._publish(torch.split(inp, input_split_sizes))
+                out.copy_(torch.cat([grp.slots[c][rank] for c in range(grp.G)]))
+                torch.cuda.synchronize()
+                grp.barrier.wait()                # slots are reused by the next collective
+
+            def all_gather_into_tensor(self, out, inp, group=None):
+                self._publish(inp)
+                out.copy_(torch.cat([grp.slots[c] for c in range(grp.G)]))
+                torch.cuda.synchronize()
+                grp.barrier.wait()
+        return _Dist()
+
+
+@pytest.mark.parametrize("G,dtype,cap", [(2, "f32", 1 << 20), (3, "bf16", 1 << 19), (4, "f32", 0)])
+def test_sharded_hook_thread_ranks_on_one_gpu(G, dtype, cap):
+    """G ranks as host threads, each with its own reducer (W = 1, its
+    replica) and the sharded hook: every bucket goes through gather, the
+    all-to-all of raw chunks, the owner's mean (the library's kernel), the
+    all-gather and the copy-back, in bucket order on every rank; every rank's
+    arena and copied-back gradients equal the oracle's mean over the G
+    replicas bit for bit."""
+    import threading
+    from reduction_reducer_gb300.sharded import sharded_hook
+    numel = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 70001, 0, 9, 300007, 16, 31, 123457]
+    flats, views, offs = host_grads(numel, G, dtype)
+    members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
+    want_arena, want_outs = reduce_buckets(views, members, locs, numel)
+    grp = _ThreadGroup(G)
+    results, errors = [None] * G, []
+
+    def rank_main(r):
+        try:
+            torch.cuda.set_device(0)
+            _, grads_dev = host_to_device_views([flats[r]], numel, offs, dtype, DEV)
+            red = Reducer(numel, dtype, cap)
+            arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+            outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+            red.bind(grads_dev, arena, outs)
+            tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+            rb = torch.empty(max(red.arena_numel(), 1), dtype=tdt, device=DEV)
+            red.register_comm_hook(sharded_hook(grp.member(r), rb, arena, dtype=dtype), [rb])
+            for _ in range(2):
+                red.begin_iteration()
+                red.mark_ready_many(gen.reverse_order(len(numel)))
+            torch.cuda.synchronize()
+            results[r] = (arena.cpu().numpy(), [o.cpu().numpy() for o in outs])
+            red.destroy()
+        except Exception as exc:      # noqa: BLE001 -- reported by the main thread
+            errors.append((r, repr(exc)))
+            grp.barrier.abort()
+
+    threads = [threading.Thread(target=rank_main, args=(r,)) for r in range(G)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errors, errors
+    for r in range(G):
+        arena, outs = results[r]
+        assert bits_equal(arena, want_arena), (r, first_mismatch(arena, want_arena))
+        for v in range(len(numel)):
+            assert bits_equal(outs[v], want_outs[0][v]), (r, v)
