@@ -6,7 +6,8 @@ sizes, sizes around the vector and tile widths, an occasional large one),
 W (including widths without a compiled-in body), f32 or bf16, the cap
 (per-gradient to one bucket), the output mode (as-view, one copy, W
 copies), misaligned views, a random ready order, every launch mode and
-every kernel choice.  Each case is compared bit for bit with the oracle,
+every kernel choice, and (for the batched call) the launch-coalescing
+threshold.  Each case is compared bit for bit with the oracle,
 with guard words around the arena and every output (see full_compare).
 """
 
@@ -23,6 +24,8 @@ CAPS = [0, 1024, 16 * 1024, 256 * 1024, 1 << 20, 64 << 20]
 WS = [1, 2, 3, 4, 5, 7, 8, 9, 16, 33]
 MODES = ["mark_ready", "mark_ready_many", "reduce_all", "reduce_bucket"]
 KERNELS = ["ldg", "tma", "auto", "chained"]
+# DDP_OPT_COALESCE_ELEMS of mark_ready_many: one launch per event, tiny to large merges, the whole call
+COALESCE = [0, 1, 1000, 65536, 1 << 21, 1 << 40]
 
 
 def draw_case(seed):
@@ -35,15 +38,18 @@ def draw_case(seed):
     dtype = "f32" if rng.random() < 0.5 else "bf16"
     cap = int(rng.choice(CAPS))
     n_out = int(rng.choice([0, 1, W]))
-    return dict(numel=numel, W=W, dtype=dtype, cap=cap, n_out=n_out, odd=bool(rng.random() < 0.3),
+    case = dict(numel=numel, W=W, dtype=dtype, cap=cap, n_out=n_out, odd=bool(rng.random() < 0.3),
                 mode=str(rng.choice(MODES)), kernel=str(rng.choice(KERNELS)))
+    case["coalesce"] = int(rng.choice(COALESCE))
+    return case
 
 
 @pytest.mark.parametrize("seed", range(200))
 def test_fuzz_bucket_pass(seed):
     c = draw_case(seed)
+    from reduction_reducer_gb300 import _lib
     full_compare(c["numel"], c["W"], c["dtype"], c["cap"], order="random", n_out=c["n_out"], mode=c["mode"],
-                 odd=c["odd"], kernel=c["kernel"])
+                 odd=c["odd"], kernel=c["kernel"], options={_lib.OPT_COALESCE_ELEMS: c["coalesce"]})
 
 
 # ---------------------------------------------------------------- unused parameters
@@ -85,6 +91,8 @@ def test_fuzz_unused_parameters(seed):
     bufs, out_views, out_offs = _guarded_outputs(numel, n_out)
     red.bind(grads_dev, arena, out_views[0] if n_out == 1 else out_views)
     red.set_local_used(used.tolist())
+    from reduction_reducer_gb300 import _lib
+    red.set_option(_lib.OPT_COALESCE_ELEMS, int(rng.choice(COALESCE)))
     red.begin_iteration()
     g = globally_used(used.tolist())
     order = [int(v) for v in rng.permutation(P) if g[v]]
@@ -138,7 +146,9 @@ def test_fuzz_fused_last_step(seed):
     torch.cuda.synchronize()
     before = [f.clone() for f in acc_flat]
     red.bind_last_step(dev[K - 1])
-    _drive(red, mode, [int(v) for v in rng.permutation(P)])
+    order = [int(v) for v in rng.permutation(P)]
+    red.set_option(_lib.OPT_COALESCE_ELEMS, int(rng.choice(COALESCE)))
+    _drive(red, mode, order)
     assert red.device_status() == 0
     got = arena.cpu().numpy()
     assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
@@ -183,6 +193,7 @@ def test_fuzz_hooks(seed):
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     red.register_comm_hook(hook, [torch.empty(max(N, 1), dtype=tdt, device="cuda") for _ in range(W)])
     red.set_option(_lib.OPT_HOOK_FUSED, 1 if seed % 2 == 0 else 0)
+    red.set_option(_lib.OPT_COALESCE_ELEMS, int(rng.choice(COALESCE)))
     members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
     fn = hook_mean if hook == "mean" else hook_bf16_compress
     want_arena, want_outs, _ = reduce_with_hook(views, members, locs, numel, fn, n_out=max(n_out, 1))
@@ -234,6 +245,7 @@ def test_fuzz_rebuild(seed):
     red.rebuild_buckets(None, first_cap, cap)
     arena.fill_(float("nan"))
     order2 = [int(v) for v in rng.permutation(P)]
+    red.set_option(_lib.OPT_COALESCE_ELEMS, int(rng.choice(COALESCE)))
     red.begin_iteration()
     red.mark_ready_many(order2)
     torch.cuda.synchronize()
