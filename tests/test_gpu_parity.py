@@ -692,3 +692,43 @@ def test_coalesced_launches(coalesce, kernel):
     # a straggler order parks buckets: merged runs still go out in index order
     full_compare(RAGGED, 4, "f32", 16 * 1024, order="straggler", mode="mark_ready_many", kernel=kernel,
                  options={_lib.OPT_COALESCE_ELEMS: coalesce}, iterations=2)
+
+
+@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+def test_coalesced_launches_flushed_before_an_error(kernel):
+    """A mark_ready_many call that fails at event i (a variable reported
+    twice) still launches what events 0 .. i-1 released, although the
+    coalescing threshold would have held those buckets back for a larger
+    launch: their arena slices and copy-backs equal the oracle's, the rest
+    of the arena is untouched."""
+    from reduction_reducer_gb300 import AlreadyReady
+    numel = RAGGED
+    W, cap = 4, 16 * 1024
+    flats, views, offs = host_grads(numel, W, "f32")
+    members, locs = assign_buckets(numel, 4, cap)
+    want_arena, want_outs = reduce_buckets(views, members, locs, numel)
+    _, grads_dev = host_to_device_views(flats, numel, offs, "f32", DEV)
+    red = Reducer(numel, "f32", cap)
+    set_kernel(red, kernel)
+    red.set_option(_lib.OPT_COALESCE_ELEMS, 1 << 40)          # nothing reaches it: one launch per call
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
+    red.bind(grads_dev, arena, outs)
+    order = gen.reverse_order(len(numel))
+    released = [b for b in range(len(members)) if all(v in order[:8] for v in members[b])]
+    assert 0 < len(released) < len(members)
+    red.begin_iteration()
+    with pytest.raises(AlreadyReady):
+        red.mark_ready_many(order[:8] + [order[3]] + order[8:])
+    torch.cuda.synchronize()
+    got = arena.cpu().numpy()
+    lens = [sum(numel[v] for v in m) for m in members]
+    starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    done = int(starts[len(released)])
+    assert bits_equal(got[:done], want_arena[:done]), first_mismatch(got[:done], want_arena[:done])
+    assert np.isnan(got[done:]).all()
+    for b in released:
+        for v in members[b]:
+            assert bits_equal(outs[v].cpu().numpy(), want_outs[0][v]), v
+    assert red.launch_count() == 1
+    red.destroy()
