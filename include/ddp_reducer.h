@@ -420,10 +420,10 @@ enum ddp_option {
                                      copy-back route of every other hook.  Between iterations only. */
     DDP_OPT_COALESCE_ELEMS = 13   /* ddp_mark_ready_many: consecutive bucket runs released by the events
                                      of one call go out as one launch until it spans at least this many
-                                     elements (default 2^21; 0: one launch per releasing event); results, readiness
-                                     state and hook order are unchanged, only launch boundaries move.
-                                     Every listed gradient is final when the call is made, so no launch
-                                     is held back behind work it could overlap. */
+                                     elements (default 2^21; 0: one launch per releasing event); results,
+                                     readiness state and hook order are unchanged, only launch boundaries
+                                     move.  Every listed gradient is final when the call is made, so no
+                                     launch is held back behind work it could overlap. */
 };
 int ddp_set_option(ddp_ctx* ctx, int32_t option, int64_t value);
 int ddp_get_option(const ddp_ctx* ctx, int32_t option, int64_t* value);
