@@ -428,7 +428,7 @@ def run_sharded(args):
     ranks / the slowest rank's time (weak scaling: per-rank work is fixed)."""
     import torch
     import torch.distributed as dist
-    from reduction_reducer_gb300.sharded import sharded_hook
+    from reduction_reducer_gb300.sharded import sharded_hook, verify_layout
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -449,6 +449,7 @@ def run_sharded(args):
     out_flat = torch.empty(total, device=device)
     red.bind(grads, arena, [out_flat[o:o + n] for o, n in zip(offs, numel)])
     rb = torch.empty(red.arena_numel(), device=device)
+    verify_layout(dist, red)                      # every rank must pair the same buckets
     red.register_comm_hook(sharded_hook(dist, rb, arena, dtype="f32"), [rb])
     order = read_order()
 

@@ -29,6 +29,37 @@ from . import _lib
 from .reducer import DTYPES, _check_status, _ptr, _ptr_array
 
 
+def verify_layout(dist, red, group=None, device=None):
+    """Construction check across ranks ("PyTorch Distributed" paper summary:
+    the sizes are compared across processes with a MIN and a MAX all-reduce
+    before training starts): every rank of ``group`` must hold the same
+    bucket layout -- parameter count, dtype, bucket count, arena size and the
+    bucket offsets and members -- since the buckets' collectives must pair
+    up in bucket order on every rank.  Raises RuntimeError naming what
+    differs.  ``device``: where the all-reduced tensor lives (default: cuda
+    for the NCCL backend, cpu otherwise)."""
+    import hashlib
+    import torch
+    B, offs = red.get_bucket_info()
+    locs = red.get_locators()
+    h = hashlib.sha256()
+    h.update(",".join(str(x) for x in offs).encode())
+    h.update(";".join(f"{b}.{i}.{o}.{n}" for (b, i, o, n) in locs).encode())
+    d = h.digest()
+    fields = {"parameter count": red.P, "dtype": DTYPES[red.dtype], "bucket count": B, "arena size": int(offs[-1]),
+              "layout digest (low)": int.from_bytes(d[:7], "little"),
+              "layout digest (high)": int.from_bytes(d[7:14], "little")}
+    if device is None:
+        device = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    v = torch.tensor(list(fields.values()), dtype=torch.int64, device=device)
+    lo, hi = v.clone(), v.clone()
+    dist.all_reduce(lo, op=dist.ReduceOp.MIN, group=group)
+    dist.all_reduce(hi, op=dist.ReduceOp.MAX, group=group)
+    bad = [k for k, a, b in zip(fields, lo.tolist(), hi.tolist()) if a != b]
+    if bad:
+        raise RuntimeError("the ranks' bucket layouts differ in: " + ", ".join(bad))
+
+
 def shard_range(n: int, G: int, g: int):
     """(chunk, lo, hi): rank g's part [lo, hi) of a flat range of n elements
     split in chunks of ``chunk`` elements (``ddp_shard_range``)."""

@@ -137,6 +137,14 @@ class _ThreadGroup:
                 out.copy_(torch.cat([grp.slots[c] for c in range(grp.G)]))
                 torch.cuda.synchronize()
                 grp.barrier.wait()
+
+            ReduceOp = torch.distributed.ReduceOp
+
+            def all_reduce(self, t, op=None, group=None):
+                self._publish(t.clone())
+                stack = torch.stack([grp.slots[c] for c in range(grp.G)])
+                t.copy_(stack.min(0).values if op == torch.distributed.ReduceOp.MIN else stack.max(0).values)
+                grp.barrier.wait()
         return _Dist()
 
 
@@ -149,7 +157,7 @@ def test_sharded_hook_thread_ranks_on_one_gpu(G, dtype, cap):
     arena and copied-back gradients equal the oracle's mean over the G
     replicas bit for bit."""
     import threading
-    from reduction_reducer_gb300.sharded import sharded_hook
+    from reduction_reducer_gb300.sharded import sharded_hook, verify_layout
     numel = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 70001, 0, 9, 300007, 16, 31, 123457]
     flats, views, offs = host_grads(numel, G, dtype)
     members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
@@ -167,6 +175,7 @@ def test_sharded_hook_thread_ranks_on_one_gpu(G, dtype, cap):
             red.bind(grads_dev, arena, outs)
             tdt = torch.float32 if dtype == "f32" else torch.bfloat16
             rb = torch.empty(max(red.arena_numel(), 1), dtype=tdt, device=DEV)
+            verify_layout(grp.member(r), red, device=DEV)
             red.register_comm_hook(sharded_hook(grp.member(r), rb, arena, dtype=dtype), [rb])
             for _ in range(2):
                 red.begin_iteration()

@@ -106,6 +106,9 @@ def _rank(rank, world, port, dtype, cap):
         def oracle_mean(parts, out):
             out.copy_(torch.from_numpy(replica_mean([_to_np(p, dtype) for p in parts])))
 
+        from reduction_reducer_gb300 import Reducer
+        from reduction_reducer_gb300.sharded import verify_layout
+        verify_layout(dist, Reducer(RAGGED, dtype, cap))            # the same layout on every rank
         reduce = ShardedAllReduce(dist, None, dtype, mean=oracle_mean)
         lens = [sum(RAGGED[v] for v in m) for m in members]
         starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
@@ -125,3 +128,30 @@ def _rank(rank, world, port, dtype, cap):
 def test_sharded_allreduce_gloo_equals_unsharded_oracle(built, world, dtype, cap):
     import torch.multiprocessing as mp
     mp.start_processes(_rank, args=(world, _free_port(), dtype, cap), nprocs=world, join=True, start_method="spawn")
+
+
+def _rank_mismatch(rank, world, port):
+    import torch.distributed as dist
+    from reduction_reducer_gb300 import Reducer
+    from reduction_reducer_gb300.sharded import verify_layout
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        cap = 16 * 1024 if rank == 0 else 0                       # rank 1: one bucket per tensor
+        with pytest.raises(RuntimeError, match="bucket count"):
+            verify_layout(dist, Reducer(RAGGED, "f32", cap))
+        numel = list(RAGGED)
+        if rank == 1:
+            numel[4], numel[5] = numel[5], numel[4]              # same sizes, other order: same count and arena
+        with pytest.raises(RuntimeError, match="layout digest"):
+            verify_layout(dist, Reducer(numel, "f32", 16 * 1024))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_layouts_that_differ_across_ranks_are_refused(built):
+    """The construction check: a MIN and a MAX all-reduce of each rank's
+    layout summary; every rank raises when one rank's buckets differ."""
+    import torch.multiprocessing as mp
+    mp.start_processes(_rank_mismatch, args=(2, _free_port()), nprocs=2, join=True, start_method="spawn")
