@@ -364,6 +364,8 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream, int tma_waves
     const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
     ddpk::LaunchCfg cfg = c->cfg;
     if (tma_waves > 0) cfg.tma_waves = tma_waves;
+    // the iteration's final launch has no successor to overlap its tail
+    cfg.last = b1 == c->B ? 1 : 0;
     // Chained launches: a launch that directly follows this iteration's
     // previous launch on the same stream need not wait for it when nothing
     // else can sit between them -- always within one API call (the call

@@ -43,6 +43,7 @@ struct LaunchCfg {
     int tma_ctas_per_sm;        // bulk-copy kernels: CTAs per SM; 0 = tma_waves resident waves
     int tma_waves;              // resident waves of a bulk-copy launch when tma_ctas_per_sm is 0 (0 = 2)
     int chain;                  // per launch: see pdl_enter in ddp_device.cuh
+    int last;                   // per launch: the iteration's final launch (nothing follows to overlap its tail)
     int compress;               // bucket reduce: each replica value rounded to bf16 first (fp32 inputs,
                                 // no mask, no fused last step): the bf16-compression hook in the pass
     int* status;                // device status word of the binding (bulk-copy kernels)
