@@ -418,14 +418,15 @@ def run_gpt2_only(args):
 
 
 def run_sharded(args):
-    """The bucket all-reduce across ranks that each hold one replica (one
-    rank per GPU under torchrun, NCCL): every rank reduces its own BERT-large
-    gradients (W = 1 per rank, 25 MiB buckets) through the sharded hook --
-    per bucket, in bucket-index order, gather into the bucket buffer,
-    all-to-all of the raw chunks, the owner's rank-order mean, all-gather,
-    copy-back.  Bytes per rank and step: N*4 read + 2*N*4 written (the
-    fused pass's algorithmic bytes at W = 1); value = those bytes over all
-    ranks / the slowest rank's time (weak scaling: per-rank work is fixed)."""
+    """The bucket all-reduce across ranks that each hold Wl replicas
+    (--replicas-per-rank, default one; one rank per GPU under torchrun,
+    NCCL): every rank reduces its own BERT-large gradients (25 MiB buckets)
+    through the sharded hook -- per bucket, in bucket-index order, gather
+    into the bucket buffers, all-to-alls of the raw chunks, the owner's mean
+    in replica order, all-gather, copy-back.  Bytes per rank and step:
+    Wl*N*4 read + 2*N*4 written (the fused pass's algorithmic bytes at W =
+    Wl); value = those bytes over all ranks / the slowest rank's time (weak
+    scaling: per-rank work is fixed)."""
     import torch
     import torch.distributed as dist
     from reduction_reducer_gb300.sharded import sharded_hook, verify_layout
@@ -440,17 +441,18 @@ def run_sharded(args):
         dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1, device_id=device)
     stream = torch.cuda.Stream(device=device)
     from reduction_reducer_gb300 import Reducer
+    Wl = args.replicas_per_rank
     numel = shapes.numels(shapes.bert_large())
     offs, total = gen.packed_offsets(numel, 64)
-    flat = gen.draw_flat_torch(total, rank, 0, "f32", device)
-    grads = [[flat[o:o + n] for o, n in zip(offs, numel)]]
+    flats = [gen.draw_flat_torch(total, rank * Wl + r, 0, "f32", device) for r in range(Wl)]
+    grads = [[f[o:o + n] for o, n in zip(offs, numel)] for f in flats]
     red = Reducer(numel, "f32", 25 * MIB)
     arena = torch.empty(red.arena_numel(), device=device)
     out_flat = torch.empty(total, device=device)
     red.bind(grads, arena, [out_flat[o:o + n] for o, n in zip(offs, numel)])
-    rb = torch.empty(red.arena_numel(), device=device)
+    rbs = [torch.empty(red.arena_numel(), device=device) for _ in range(Wl)]
     verify_layout(dist, red)                      # every rank must pair the same buckets
-    red.register_comm_hook(sharded_hook(dist, rb, arena, dtype="f32"), [rb])
+    red.register_comm_hook(sharded_hook(dist, rbs, arena, dtype="f32"), rbs)
     order = read_order()
 
     def step():
@@ -460,15 +462,15 @@ def run_sharded(args):
     with torch.cuda.stream(stream):
         ms, _, _ = time_steps(torch, stream, step, args.steps, args.warmup, dist if world > 1 else None)
     N = sum(numel)
-    per_rank = N * 4 + 2 * N * 4
+    per_rank = Wl * N * 4 + 2 * N * 4
     t = ms / args.steps
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": round(per_rank * world / (t * 1e-3) / 1e9, 1), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded N(0,1e-3) gradients generated on the device, one replica per rank)",
-            "config": {"workload": "bert_large", "W": world, "replicas_per_rank": 1, "P": len(numel), "N": N,
+            "data": f"synthetic (seeded N(0,1e-3) gradients generated on the device, {Wl} replica(s) per rank)",
+            "config": {"workload": "bert_large", "W": world * Wl, "replicas_per_rank": Wl, "P": len(numel), "N": N,
                        "cap_mib": 25, "buckets": red.B, "mode": "copy-back (n_out=1)",
                        "parallelism": f"sharded all-reduce x{world} (all-to-all of raw chunks, owner mean, all-gather)",
                        "bytes_per_rank_step": per_rank}}), flush=True)
@@ -1209,8 +1211,10 @@ def main():
     ap.add_argument("--hook-route", default="fused", choices=["fused", "gathered"],
                     help="profiling cases: --hook inside the fused pass or through gather + hook call + copy-back")
     ap.add_argument("--sharded", action="store_true",
-                    help="one replica per rank: the bucket all-reduce across ranks (NCCL; reduce-scatter as an "
-                         "all-to-all of raw chunks + owner mean, then all-gather)")
+                    help="the bucket all-reduce across ranks (NCCL; reduce-scatter as all-to-alls of raw chunks "
+                         "+ owner mean, then all-gather)")
+    ap.add_argument("--replicas-per-rank", type=int, default=1,
+                    help="--sharded: replicas each rank holds (the same on every rank)")
     ap.add_argument("--trace", action="store_true",
                     help="launch boundaries of one BERT-large iteration from the trace build's per-CTA timestamps")
     ap.add_argument("--mix-rates", action="store_true",

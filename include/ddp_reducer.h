@@ -347,7 +347,7 @@ int ddp_bind_last_step(ddp_ctx* ctx, const void* const* g_last);
 int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_arena,
                            float* const* grad_out, int32_t n_out, void* stream);
 
-/* ---------------------------------------------------------------- ranks that each hold one replica */
+/* ---------------------------------------------------------------- ranks that each hold some of the replicas */
 
 /* Ownership plan of the bucket all-reduce split across G ranks ("PyTorch
  * Distributed Training Internals", section "3. The All-Reduce Itself": a
@@ -364,10 +364,12 @@ int ddp_reduce_all_noalloc(ddp_ctx* ctx, int32_t W, const void* const* grads, fl
 int ddp_shard_range(int64_t n, int32_t G, int32_t g, int64_t* chunk, int64_t* lo, int64_t* hi);
 
 /* The owner's step of that all-reduce: out[i] = fl32(1/G) x the fp32 sum, in
- * rank order c = 0 .. G-1 starting from chunks[0][i], of the widened values
- * chunks[c][i], i < n -- the one-GPU pass's arithmetic over the G replicas,
- * so the sharded result equals it bit for bit when the reduce-scatter moves
- * the replicas' raw chunks (an all-to-all) instead of partial sums.
+ * order c = 0 .. G-1 starting from chunks[0][i], of the widened values
+ * chunks[c][i], i < n -- the one-GPU pass's arithmetic over G replicas, so
+ * the sharded result equals it bit for bit when the reduce-scatter moves the
+ * replicas' raw chunks (all-to-alls) instead of partial sums.  With Wl
+ * replicas on each rank, G here is the number of replicas in all (ranks x
+ * Wl) and chunks[c] is replica c in the one-GPU order.
  *   chunks  host array [G] of device pointers: replica c's n values of the
  *           owned chunk, in `dtype` (16-byte aligned for 128-bit loads; any
  *           alignment is correct)

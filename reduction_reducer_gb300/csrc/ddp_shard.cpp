@@ -1,5 +1,5 @@
-// The bucket all-reduce split across ranks that each hold one replica: the
-// ownership plan and the owner's reduction.
+// The bucket all-reduce split across ranks that each hold some of the
+// replicas: the ownership plan and the owner's reduction.
 //
 // "PyTorch Distributed Training Internals", section "3. The All-Reduce
 // Itself", describes the all-reduce of a bucket as a reduce-scatter followed
@@ -9,11 +9,11 @@
 // per rank).  "NCCL 专家课程 30", section "Bucket 必须按序发起", fixes the
 // order: every rank issues its buckets' collectives in bucket-index order.
 //
-// Exactness: the reduce-scatter here moves the replicas' raw values (an
-// all-to-all of chunks) and the owner sums them itself, rank 0 .. G-1 in
-// order, then scales by fl32(1/G) -- the single-GPU pass's definition -- so
-// the sharded result equals the one-GPU emulation bit for bit.  A ring
-// reduce-scatter would add partial sums in another order.
+// Exactness: the reduce-scatter here moves the replicas' raw values
+// (all-to-alls of chunks) and the owner sums them itself, replica 0 .. W-1 in
+// the one-GPU order, then scales by fl32(1/W) -- the single-GPU pass's
+// definition -- so the sharded result equals the one-GPU emulation bit for
+// bit.  A ring reduce-scatter would add partial sums in another order.
 
 #include "ddp_reducer.h"
 

@@ -1,19 +1,21 @@
-"""The bucket all-reduce across ranks that each hold one replica.
+"""The bucket all-reduce across ranks that each hold some of the replicas.
 
-Each rank runs its own reducer (W = 1: its replica's gradients) with a
+Each rank runs its own reducer over the replicas it holds (Wl of them, the
+same number on every rank; Wl = 1 when every rank holds one) with a
 communication hook from this module.  The library calls the hook for every
 launched bucket, in bucket-index order on every rank ("NCCL 专家课程 30",
-section "Bucket 必须按序发起"), with the bucket's gradients gathered into a
-flat buffer, and copies the hook's result back into the gradients.  The hook
-performs the all-reduce as the pages describe it ("PyTorch Distributed
+section "Bucket 必须按序发起"), with the bucket's gradients gathered into
+flat buffers, and copies the hook's result back into the gradients.  The
+hook performs the all-reduce as the pages describe it ("PyTorch Distributed
 Training Internals", section "3. The All-Reduce Itself"): a reduce-scatter,
 after which rank g owns the reduced values of chunk g of the bucket
 (``ddp_shard_range``), then an all-gather of the chunks.
 
-The reduce-scatter is exact: an all-to-all moves the replicas' raw values of
-each chunk to its owner, and the owner sums them itself in rank order and
-scales by fl32(1/G) (``ddp_shard_mean``, the library's kernel), so every rank
-ends with the bits the one-GPU pass computes over the same G replicas.
+The reduce-scatter is exact: all-to-alls move the replicas' raw values of
+each chunk to its owner, and the owner sums them itself in global replica
+order (rank g's replica r is replica g*Wl + r) and scales by fl32(1/W),
+W = G*Wl (``ddp_shard_mean``, the library's kernel), so every rank ends with
+the bits the one-GPU pass computes over the same W replicas.
 
 Only plumbing lives here: the exchange runs through ``torch.distributed``
 (NCCL between GPUs; any backend with all_to_all_single and
@@ -47,6 +49,7 @@ def verify_layout(dist, red, group=None, device=None):
     h.update(";".join(f"{b}.{i}.{o}.{n}" for (b, i, o, n) in locs).encode())
     d = h.digest()
     fields = {"parameter count": red.P, "dtype": DTYPES[red.dtype], "bucket count": B, "arena size": int(offs[-1]),
+              "replicas per rank": int(getattr(red, "W", 0)),
               "layout digest (low)": int.from_bytes(d[:7], "little"),
               "layout digest (high)": int.from_bytes(d[7:14], "little")}
     if device is None:
@@ -70,9 +73,9 @@ def shard_range(n: int, G: int, g: int):
 
 
 def shard_mean(chunks, out, dtype: str, stream: int):
-    """out[i] = rank-order fp32 mean of chunks[c][i] (device tensors or
-    addresses, ``out.numel()`` values each) on ``stream``
-    (``ddp_shard_mean``)."""
+    """out[i] = fp32 mean of chunks[c][i] in the order of ``chunks`` (device
+    tensors or addresses, ``out.numel()`` values each, at most 64 of them) on
+    ``stream`` (``ddp_shard_mean``)."""
     lib = _lib.load()
     n = out.numel()
     arr = _ptr_array([_ptr(t) for t in chunks])
@@ -81,7 +84,8 @@ def shard_mean(chunks, out, dtype: str, stream: int):
 
 class ShardedAllReduce:
     """The exact reduce-scatter + all-gather of one flat bucket over the
-    ranks of ``group`` (every rank holds one replica).
+    ranks of ``group``, every rank holding the same number Wl of replicas
+    (G*Wl <= 64).
 
     ``mean(chunks, out)`` is the owner's arithmetic; by default the
     library's ``ddp_shard_mean`` on the current CUDA stream.  Buffers for the
@@ -106,23 +110,37 @@ class ShardedAllReduce:
         return t[:n]
 
     def __call__(self, local, out):
-        """local: this rank's bucket (1-D, gradient dtype); out: fp32 tensor
-        of the same length that receives the mean over all ranks."""
+        """local: this rank's bucket, one 1-D tensor of the gradient dtype
+        (one replica per rank) or a list of the Wl replicas' buckets, each of
+        the same length; out: fp32 tensor of that length that receives the
+        mean over all G*Wl replicas in global replica order."""
         import torch
-        n = local.numel()
+        reps = [local] if torch.is_tensor(local) else list(local)
+        Wl = len(reps)
         G = self.G
+        if Wl < 1 or G * Wl > 64:
+            raise ValueError(f"{G} ranks x {Wl} replicas: between 1 and 64 replicas in all")
+        n = reps[0].numel()
+        if any(t.numel() != n for t in reps) or out.numel() != n:
+            raise ValueError("the replicas' buckets and the output differ in length")
         plan = [shard_range(n, G, c) for c in range(G)]
         chunk, lo, hi = plan[self.rank]
         mine_n = hi - lo
-        # reduce-scatter, exact: chunk c of the local bucket goes to rank c as
-        # it is (uneven splits: the last non-empty chunk is shorter), and this
-        # rank receives every replica's values of its own chunk, in rank order
-        recv = self._buf("recv", G * mine_n, local.dtype, local)
-        self.dist.all_to_all_single(recv, local, output_split_sizes=[mine_n] * G,
-                                    input_split_sizes=[h - l for _, l, h in plan], group=self.group)
-        mine = self._buf("mine", chunk, torch.float32, local)
+        splits = [h - l for _, l, h in plan]
+        # reduce-scatter, exact: chunk c of each local replica's bucket goes to
+        # rank c as it is (uneven splits: the last non-empty chunk is
+        # shorter), and this rank receives every rank's values of its own
+        # chunk, rank after rank; one all-to-all per local replica
+        recv = []
+        for r, t in enumerate(reps):
+            buf = self._buf(("recv", r), G * mine_n, t.dtype, t)
+            self.dist.all_to_all_single(buf, t, output_split_sizes=[mine_n] * G,
+                                        input_split_sizes=splits, group=self.group)
+            recv.append(buf)
+        mine = self._buf("mine", chunk, torch.float32, reps[0])
         if mine_n > 0:
-            parts = [recv[c * mine_n:(c + 1) * mine_n] for c in range(G)]   # replica c's values of my chunk
+            # replica g*Wl + r is rank g's replica r: the one-GPU pass's order
+            parts = [recv[r][g * mine_n:(g + 1) * mine_n] for g in range(G) for r in range(Wl)]
             if self.mean is not None:
                 self.mean(parts, mine[:mine_n])
             else:
@@ -130,36 +148,41 @@ class ShardedAllReduce:
         if chunk > mine_n:
             mine[mine_n:].zero_()            # padding of a short chunk: gathered, never used
         # all-gather of equal (padded) chunks; they tile [0, n) in rank order
-        gathered = self._buf("gathered", G * chunk, torch.float32, local)
+        gathered = self._buf("gathered", G * chunk, torch.float32, reps[0])
         self.dist.all_gather_into_tensor(gathered, mine, group=self.group)
         out.copy_(gathered[:n])
 
 
-def sharded_hook(dist, replica_buffer, arena, group=None, dtype: str = "f32"):
+def sharded_hook(dist, replica_buffers, arena, group=None, dtype: str = "f32"):
     """A communication hook (for ``Reducer.register_comm_hook(hook,
-    [replica_buffer])`` on a reducer bound with W = 1: this rank's replica)
-    that all-reduces every bucket across the ranks of ``group`` with
-    ``ShardedAllReduce``.  ``replica_buffer`` is the tensor the bucket's
-    gradients lie in -- the registered replica buffer, or, when the hook was
-    registered without one, the flat gradient tensor whose views in bucket
-    order the reducer was bound to -- and ``arena`` the bucket arena the
-    reducer reduces into.  The hook runs its exchange on the library's
-    stream; a bucket of another replica count fails the launch (HookError)."""
+    replica_buffers)`` on a reducer bound with this rank's Wl replicas) that
+    all-reduces every bucket across the ranks of ``group`` with
+    ``ShardedAllReduce``.  ``replica_buffers``: the tensor (Wl = 1) or the Wl
+    tensors the buckets' gradients lie in, replica by replica -- the
+    registered replica buffers, or, when the hook was registered without
+    them, the flat gradient tensors whose views in bucket order the reducer
+    was bound to -- and ``arena`` the bucket arena the reducer reduces into.
+    The hook runs its exchange on the library's stream; a bucket of another
+    replica count fails the launch (HookError)."""
     import torch
+    bufs = [replica_buffers] if torch.is_tensor(replica_buffers) else list(replica_buffers)
     reduce = ShardedAllReduce(dist, group, dtype)
-    esz = replica_buffer.element_size()
+    Wl = len(bufs)
 
     def hook(bucket, stream):
-        if bucket.W != 1:
-            return 1                          # one replica per rank: the others are the other ranks'
+        if bucket.W != Wl:
+            return 1                          # every rank holds Wl replicas; the others are the other ranks'
         n = int(bucket.numel)
         if n == 0:
             return 0
-        at = (int(bucket.replicas[0]) - replica_buffer.data_ptr()) // esz
+        local = []
+        for r, t in enumerate(bufs):
+            at = (int(bucket.replicas[r]) - t.data_ptr()) // t.element_size()
+            local.append(t[at:at + n])
         res = (int(bucket.result) - arena.data_ptr()) // 4
         st = torch.cuda.ExternalStream(int(stream), device=arena.device) if stream else \
             torch.cuda.default_stream(arena.device)
         with torch.cuda.stream(st):
-            reduce(replica_buffer[at:at + n], arena[res:res + n])
+            reduce(local, arena[res:res + n])
         return 0
     return hook

@@ -1,13 +1,17 @@
-"""GPU side of the bucket all-reduce across ranks that each hold one replica.
+"""GPU side of the bucket all-reduce across ranks that each hold some of the replicas.
 
-* ``ddp_shard_mean`` (the owner's rank-order mean of G replicas' chunks)
-  against the oracle's mean, bit for bit, for G up to 64, fp32 and bf16,
-  aligned and unaligned chunk pointers, ragged lengths, special values;
-* the whole path through a reducer (W = 1 per rank, the sharded hook) with
-  a real NCCL process group: on this one-GPU machine the group has one rank,
-  so the exchange is NCCL's all-to-all and all-gather with itself and the
-  result is the rank's own gradients (x 1/1), against the oracle.  Larger
-  groups run on the CPU over gloo (``tests/test_shard_plan.py``).
+* ``ddp_shard_mean`` (the owner's mean of the replicas' chunks, in their
+  order) against the oracle's mean, bit for bit, for up to 64 chunks, fp32
+  and bf16, aligned and unaligned chunk pointers, ragged lengths, special
+  values;
+* the whole path through a reducer (Wl = 1 or 2 replicas per rank, the
+  sharded hook) with a real NCCL process group: on this one-GPU machine the
+  group has one rank, so the exchange is NCCL's all-to-all and all-gather
+  with itself and the result is the mean of the rank's own replicas,
+  against the oracle;
+* the whole path with G = 2, 3 and 4 ranks as host threads on the one GPU
+  (one or two replicas each).  Larger groups of processes run on the CPU
+  over gloo (``tests/test_shard_plan.py``).
 """
 
 import numpy as np
@@ -62,12 +66,13 @@ def test_shard_mean_equals_oracle(G, dtype):
         assert bits_equal(got, want), (n, shift, first_mismatch(got, want))
 
 
+@pytest.mark.parametrize("Wl", [1, 2])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_sharded_hook_nccl_single_rank(dtype):
+def test_sharded_hook_nccl_single_rank(dtype, Wl):
     """A reducer with the sharded hook in a one-rank NCCL group: every bucket
-    goes through the hook (all-to-all, owner mean, all-gather) and the
-    library's copy-back, in bucket order; the result is the oracle's mean of
-    the one replica."""
+    goes through the hook (all-to-all per replica, owner mean, all-gather)
+    and the library's copy-back, in bucket order; the result is the oracle's
+    mean of the rank's Wl replicas."""
     import torch.distributed as dist
     from reduction_reducer_gb300.sharded import sharded_hook
     numel = shapes.numels(shapes.bert_large(layers=2, vocab=2048))
@@ -75,15 +80,15 @@ def test_sharded_hook_nccl_single_rank(dtype):
     store = dist.HashStore()
     dist.init_process_group("nccl", store=store, rank=0, world_size=1, device_id=torch.device(DEV, 0))
     try:
-        flats, views, offs = host_grads(numel, 1, dtype)
+        flats, views, offs = host_grads(numel, Wl, dtype)
         _, grads_dev = host_to_device_views(flats, numel, offs, dtype, DEV)
         red = Reducer(numel, dtype, cap)
         arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
         outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
         red.bind(grads_dev, arena, outs)
         tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-        rb = torch.empty(red.arena_numel(), dtype=tdt, device=DEV)
-        red.register_comm_hook(sharded_hook(dist, rb, arena, dtype=dtype), [rb])
+        rbs = [torch.empty(red.arena_numel(), dtype=tdt, device=DEV) for _ in range(Wl)]
+        red.register_comm_hook(sharded_hook(dist, rbs[0] if Wl == 1 else rbs, arena, dtype=dtype), rbs)
         s = torch.cuda.Stream()
         for _ in range(2):
             red.begin_iteration()
@@ -148,18 +153,20 @@ class _ThreadGroup:
         return _Dist()
 
 
-@pytest.mark.parametrize("G,dtype,cap", [(2, "f32", 1 << 20), (3, "bf16", 1 << 19), (4, "f32", 0)])
-def test_sharded_hook_thread_ranks_on_one_gpu(G, dtype, cap):
-    """G ranks as host threads, each with its own reducer (W = 1, its
-    replica) and the sharded hook: every bucket goes through gather, the
-    all-to-all of raw chunks, the owner's mean (the library's kernel), the
-    all-gather and the copy-back, in bucket order on every rank; every rank's
-    arena and copied-back gradients equal the oracle's mean over the G
-    replicas bit for bit."""
+@pytest.mark.parametrize("G,dtype,cap,Wl", [(2, "f32", 1 << 20, 1), (3, "bf16", 1 << 19, 1), (4, "f32", 0, 1),
+                                            (2, "f32", 1 << 20, 2), (3, "f32", 1 << 19, 2), (4, "bf16", 0, 2)])
+def test_sharded_hook_thread_ranks_on_one_gpu(G, dtype, cap, Wl):
+    """G ranks as host threads, each with its own reducer over its Wl
+    replicas (rank g holds replicas g*Wl ... g*Wl + Wl - 1) and the sharded
+    hook: every bucket goes through gather, the all-to-alls of raw chunks,
+    the owner's mean (the library's kernel), the all-gather and the
+    copy-back, in bucket order on every rank; every rank's arena and
+    copied-back gradients equal the oracle's mean over the G*Wl replicas bit
+    for bit."""
     import threading
     from reduction_reducer_gb300.sharded import sharded_hook, verify_layout
     numel = [0, 1, 2, 3, 5, 7, 8, 13, 64, 67, 100, 1000, 4095, 4097, 70001, 0, 9, 300007, 16, 31, 123457]
-    flats, views, offs = host_grads(numel, G, dtype)
+    flats, views, offs = host_grads(numel, G * Wl, dtype)
     members, locs = assign_buckets(numel, 4 if dtype == "f32" else 2, cap)
     want_arena, want_outs = reduce_buckets(views, members, locs, numel)
     grp = _ThreadGroup(G)
@@ -168,15 +175,15 @@ def test_sharded_hook_thread_ranks_on_one_gpu(G, dtype, cap):
     def rank_main(r):
         try:
             torch.cuda.set_device(0)
-            _, grads_dev = host_to_device_views([flats[r]], numel, offs, dtype, DEV)
+            _, grads_dev = host_to_device_views(flats[r * Wl:(r + 1) * Wl], numel, offs, dtype, DEV)
             red = Reducer(numel, dtype, cap)
             arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
             outs = [torch.full((n,), float("nan"), device=DEV) for n in numel]
             red.bind(grads_dev, arena, outs)
             tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-            rb = torch.empty(max(red.arena_numel(), 1), dtype=tdt, device=DEV)
+            rbs = [torch.empty(max(red.arena_numel(), 1), dtype=tdt, device=DEV) for _ in range(Wl)]
             verify_layout(grp.member(r), red, device=DEV)
-            red.register_comm_hook(sharded_hook(grp.member(r), rb, arena, dtype=dtype), [rb])
+            red.register_comm_hook(sharded_hook(grp.member(r), rbs if Wl > 1 else rbs[0], arena, dtype=dtype), rbs)
             for _ in range(2):
                 red.begin_iteration()
                 red.mark_ready_many(gen.reverse_order(len(numel)))

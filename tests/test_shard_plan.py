@@ -1,17 +1,17 @@
-"""The bucket all-reduce across ranks that each hold one replica, on the CPU.
+"""The bucket all-reduce across ranks that each hold some of the replicas, on the CPU.
 
 * the ownership plan (``ddp_shard_range``, host arithmetic of the library):
   the chunks of a flat range tile it in rank order, start 16-byte aligned
   for fp32 and bf16, are equal but for the last non-empty one, and differ
   from the ideal 1/G share by less than one alignment unit;
 * the exchange (``reduction_reducer_gb300.sharded.ShardedAllReduce``) over
-  ``gloo`` with world sizes 2 and 3: every rank holds one replica of a
-  ragged model, all-reduces its buckets in bucket-index order (all-to-all of
-  the raw chunks, the owner's rank-order mean, all-gather), and must end with
-  the oracle's unsharded mean over the same replicas, bit for bit.  The
-  owner's arithmetic, a CUDA kernel in the library, is stood in for here by
-  the oracle's mean (this test covers the plan and the exchange; the GPU
-  tests cover the kernel).
+  ``gloo`` with world sizes 2 and 3: every rank holds one or two replicas of
+  a ragged model, all-reduces its buckets in bucket-index order (all-to-alls
+  of the raw chunks, the owner's mean in global replica order, all-gather),
+  and must end with the oracle's unsharded mean over all the replicas, bit
+  for bit.  The owner's arithmetic, a CUDA kernel in the library, is stood
+  in for here by the oracle's mean (this test covers the plan and the
+  exchange; the GPU tests cover the kernel).
 """
 
 import os
@@ -85,7 +85,7 @@ def _to_np(t, dtype):
     return t.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else t.numpy()
 
 
-def _rank(rank, world, port, dtype, cap):
+def _rank(rank, world, port, dtype, cap, Wl):
     import torch.distributed as dist
     from reduction_reducer_gb300.sharded import ShardedAllReduce
     os.environ["MASTER_ADDR"] = "127.0.0.1"
@@ -94,14 +94,15 @@ def _rank(rank, world, port, dtype, cap):
     try:
         elem = 4 if dtype == "f32" else 2
         members, locs = assign_buckets(RAGGED, elem, cap)
-        # every replica's gradients (seeded per replica); this rank holds its own
+        # every replica's gradients (seeded per replica); rank g holds replicas
+        # g*Wl ... g*Wl + Wl - 1
         offs, total = gen.packed_offsets(RAGGED, 1)
         grads = []
-        for r in range(world):
+        for r in range(world * Wl):
             flat = gen.draw_flat_np(total, r, 0, dtype)
             grads.append([flat[o:o + n] for o, n in zip(offs, RAGGED)])
         want_arena, _ = reduce_buckets(grads, members, locs, RAGGED)
-        mine = gather_buckets([grads[rank]], members, locs, RAGGED)[0]
+        mine = gather_buckets(grads[rank * Wl:(rank + 1) * Wl], members, locs, RAGGED)
 
         def oracle_mean(parts, out):
             out.copy_(torch.from_numpy(replica_mean([_to_np(p, dtype) for p in parts])))
@@ -113,10 +114,10 @@ def _rank(rank, world, port, dtype, cap):
         lens = [sum(RAGGED[v] for v in m) for m in members]
         starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
         for b in range(len(members)):            # bucket-index order on every rank
-            local = torch.from_numpy(mine[b].view(np.int16)).view(torch.bfloat16) if dtype == "bf16" \
-                else torch.from_numpy(mine[b].copy())
+            local = [torch.from_numpy(m[b].view(np.int16)).view(torch.bfloat16) if dtype == "bf16"
+                     else torch.from_numpy(m[b].copy()) for m in mine]
             out = torch.full((lens[b],), float("nan"))
-            reduce(local, out)
+            reduce(local[0] if Wl == 1 else local, out)
             got = out.numpy()
             want = want_arena[starts[b]:starts[b + 1]]
             assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (rank, b)
@@ -124,10 +125,13 @@ def _rank(rank, world, port, dtype, cap):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world,dtype,cap", [(2, "f32", 16 * 1024), (3, "bf16", 8 * 1024), (3, "f32", 0)])
-def test_sharded_allreduce_gloo_equals_unsharded_oracle(built, world, dtype, cap):
+@pytest.mark.parametrize("world,dtype,cap,Wl", [(2, "f32", 16 * 1024, 1), (3, "bf16", 8 * 1024, 1), (3, "f32", 0, 1),
+                                               (2, "f32", 16 * 1024, 2), (3, "f32", 8 * 1024, 2),
+                                               (3, "bf16", 0, 2)])
+def test_sharded_allreduce_gloo_equals_unsharded_oracle(built, world, dtype, cap, Wl):
     import torch.multiprocessing as mp
-    mp.start_processes(_rank, args=(world, _free_port(), dtype, cap), nprocs=world, join=True, start_method="spawn")
+    mp.start_processes(_rank, args=(world, _free_port(), dtype, cap, Wl), nprocs=world, join=True,
+                       start_method="spawn")
 
 
 def _rank_mismatch(rank, world, port):
@@ -146,12 +150,17 @@ def _rank_mismatch(rank, world, port):
             numel[4], numel[5] = numel[5], numel[4]              # same sizes, other order: same count and arena
         with pytest.raises(RuntimeError, match="layout digest"):
             verify_layout(dist, Reducer(numel, "f32", 16 * 1024))
+        red = Reducer(RAGGED, "f32", 16 * 1024)
+        red.W = 1 + rank                  # as bound with one replica on rank 0 and two on rank 1
+        with pytest.raises(RuntimeError, match="replicas per rank"):
+            verify_layout(dist, red)
     finally:
         dist.destroy_process_group()
 
 
 def test_layouts_that_differ_across_ranks_are_refused(built):
     """The construction check: a MIN and a MAX all-reduce of each rank's
-    layout summary; every rank raises when one rank's buckets differ."""
+    layout summary; every rank raises when one rank's buckets, or the number
+    of replicas it holds, differ."""
     import torch.multiprocessing as mp
     mp.start_processes(_rank_mismatch, args=(2, _free_port()), nprocs=2, join=True, start_method="spawn")
