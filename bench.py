@@ -235,11 +235,19 @@ def time_steps(torch, stream, fn, steps, warmup, dist=None):
 
 
 def kernel_name(wl) -> str:
+    """The bucket kernel a workload's iteration launches: the context's
+    choice, except that with the automatic choice one mark_ready call per
+    event (calls not chained) launches the bulk-copy kernel."""
     from reduction_reducer_gb300 import _lib
     k = wl.red.get_option(_lib.OPT_QUERY_KERNEL)
     t = "float" if wl.dtype == "f32" else "uint16_t"
-    return (f"bucket_reduce_tma_kernel<{t}, {wl.W}>" if k == _lib.KERNEL_TMA
-            else f"bucket_reduce_kernel<{t}, {wl.W}>")
+    tma, ldg = f"bucket_reduce_tma_kernel<{t}, {wl.W}>", f"bucket_reduce_kernel<{t}, {wl.W}>"
+    if k == _lib.KERNEL_TMA:
+        return tma
+    if (wl.driver == "events" and wl.red.get_option(_lib.OPT_KERNEL) == _lib.KERNEL_AUTO
+            and not wl.red.get_option(_lib.OPT_CHAINED)):
+        return tma
+    return ldg
 
 
 def traffic_for(kernel_key, alg_bytes_per_launch):

@@ -392,7 +392,10 @@ enum ddp_option {
                                      the accumulate and hook copy kernels */
     DDP_OPT_KERNEL = 4,           /* 0: register-streaming kernel, 1: bulk-copy (TMA) pipeline,
                                      2 (default): per context, bulk copy when the median bucket has at
-                                     least DDP_OPT_AUTO_MIN_ELEMS elements, register streaming below */
+                                     least DDP_OPT_AUTO_MIN_ELEMS elements, register streaming below;
+                                     the launches of ddp_mark_ready and ddp_reduce_bucket calls, which
+                                     each wait for the preceding grid, take the bulk-copy kernel either
+                                     way unless DDP_OPT_CHAINED is set */
     DDP_OPT_STAGES = 5,           /* bulk-copy kernel: ring depth, 2..8 (default 3); fewer when the
                                      stages would not fit in shared memory */
     DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB);
@@ -412,8 +415,9 @@ enum ddp_option {
                                      the iteration's previous launch on the same stream starts at once and
                                      waits for it only before exiting; stream order still holds for any
                                      work after the iteration. */
-    DDP_OPT_QUERY_KERNEL = 10,    /* read only (ddp_get_option): kernel the bound context launches,
-                                     0 or 1; -1 before ddp_bind */
+    DDP_OPT_QUERY_KERNEL = 10,    /* read only (ddp_get_option): kernel the bound context chose at bind
+                                     (every launch of ddp_mark_ready_many and ddp_reduce_all), 0 or 1;
+                                     -1 before ddp_bind */
     DDP_OPT_FIND_UNUSED = 11,     /* 1: track unused parameters (find_unused_parameters; default 0):
                                      enables ddp_set_local_used and the local-use bits of
                                      ddp_accumulate_nosync_used; segments are never merged; W <= 64 */

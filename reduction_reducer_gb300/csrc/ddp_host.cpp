@@ -98,7 +98,8 @@ struct ddp_ctx {
     // three for register streaming): SMs that finish a slice early take
     // another, so a launch ends with a short tail and consecutive launches
     // interleave.  One kernel for all launches of a context, so consecutive
-    // launches can overlap.
+    // launches can overlap (one call per ready event, where every launch
+    // waits, takes the bulk-copy kernel: see launch_range).
     int opt_kernel = ddpk::KERNEL_AUTO;
     int opt_stages = 3;
     int opt_stage_bytes = 32 * 1024;
@@ -116,6 +117,7 @@ struct ddp_ctx {
     int64_t iter_launches = 0;      // launches issued in the current iteration
     void* iter_stream = nullptr;    // stream of the last of them
     int64_t call_launches = 0;      // launches issued by the current API call
+    bool event_call = false;        // the current call is ddp_mark_ready or ddp_reduce_bucket
     ddpk::LaunchCfg cfg{};
     int acc_ctas = 1;
     int aux_block = 256;            // threads per CTA of the accumulate and hook copy kernels
@@ -373,6 +375,17 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream, int tma_waves
     // opted in (DDP_OPT_CHAINED).
     const bool follows_own = c->iter_launches > 0 && stream == c->iter_stream;
     cfg.chain = c->pdl && follows_own && (c->call_launches > 0 || c->opt_chain) ? 1 : 0;
+    // One call per ready event (ddp_mark_ready, ddp_reduce_bucket), calls not
+    // chained: every launch of the iteration waits for the preceding grid,
+    // and with the automatic choice they all take the bulk-copy kernel, whose
+    // CTAs ask L2 for their first stages during the wait (the register-
+    // streaming kernel does not).  GB300, GPT-2-medium W=8 bf16, one
+    // mark_ready call per event: caps 0 / 1 / 5 MiB +10.8 / +5.3 / +3.6 %
+    // against register streaming; Linear(10,10) W=2 (one launch) equal.
+    // Batched calls keep the context's kernel for every launch: a bulk-copy
+    // first launch followed by chained register-streaming launches cost
+    // GPT-2-medium at cap 0 17 % (7.14 -> 5.94 TB/s).
+    if (c->opt_kernel == ddpk::KERNEL_AUTO && c->event_call && !c->opt_chain) cfg.kernel = ddpk::KERNEL_TMA;
     // A built-in hook's arithmetic is the fused pass's (the default hook) or
     // the fused pass with every replica value rounded to bf16 first (the
     // compression hook): it runs inside the one-pass kernel, with nothing
@@ -864,6 +877,7 @@ int ddp_abort_iteration(ddp_ctx* c) {
 int ddp_mark_ready(ddp_ctx* c, int32_t var, int32_t* launched, int32_t* n_launched, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
     c->call_launches = 0;
+    c->event_call = true;
     if (n_launched) *n_launched = 0;
     if (var < 0 || var >= c->P) return fail(c, DDP_ERR_INVALID_ARG, "variable index out of range");
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "mark_ready before bind");
@@ -884,6 +898,7 @@ int ddp_mark_ready_many(ddp_ctx* c, const int32_t* vars, int32_t n, int32_t* n_d
     if (n < 0 || (n > 0 && !vars)) return fail(c, DDP_ERR_INVALID_ARG, "bad event list");
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "mark_ready_many before bind");
     c->call_launches = 0;
+    c->event_call = false;
     // Released buckets [pend0, pend1) not launched yet: the runs released by
     // consecutive events of this call are adjacent (the cursor only moves
     // forward), so they merge into one launch (DDP_OPT_COALESCE_ELEMS).
@@ -929,6 +944,7 @@ int ddp_mark_ready_many(ddp_ctx* c, const int32_t* vars, int32_t n, int32_t* n_d
 int ddp_reduce_bucket(ddp_ctx* c, int32_t bucket, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
     c->call_launches = 0;
+    c->event_call = true;
     if (bucket < 0 || bucket >= c->B) return fail(c, DDP_ERR_INVALID_ARG, "bucket index out of range");
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "reduce_bucket before bind");
     ensure_started(c);
@@ -944,6 +960,7 @@ int ddp_reduce_bucket(ddp_ctx* c, int32_t bucket, void* stream) {
 int ddp_reduce_all(ddp_ctx* c, void* stream) {
     if (!c) return DDP_ERR_INVALID_ARG;
     c->call_launches = 0;
+    c->event_call = false;
     if (!c->dry && !c->bound) return fail(c, DDP_ERR_NOT_BOUND, "reduce_all before bind");
     ensure_started(c);
     const int32_t first = c->next;
