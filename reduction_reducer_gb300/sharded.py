@@ -100,6 +100,16 @@ class ShardedAllReduce:
         self.dtype = dtype
         self.mean = mean
         self._bufs = {}
+        self._plans = {}
+
+    def _plan(self, n):
+        """Every rank's (chunk, lo, hi) for a bucket of n elements, cached
+        per length (a layout has few distinct bucket lengths)."""
+        p = self._plans.get(n)
+        if p is None:
+            p = [shard_range(n, self.G, c) for c in range(self.G)]
+            self._plans[n] = p
+        return p
 
     def _buf(self, key, n, dtype, like):
         t = self._bufs.get(key)
@@ -123,7 +133,7 @@ class ShardedAllReduce:
         n = reps[0].numel()
         if any(t.numel() != n for t in reps) or out.numel() != n:
             raise ValueError("the replicas' buckets and the output differ in length")
-        plan = [shard_range(n, G, c) for c in range(G)]
+        plan = self._plan(n)
         chunk, lo, hi = plan[self.rank]
         mine_n = hi - lo
         splits = [h - l for _, l, h in plan]
@@ -147,10 +157,14 @@ class ShardedAllReduce:
                 shard_mean(parts, mine[:mine_n], self.dtype, int(torch.cuda.current_stream().cuda_stream))
         if chunk > mine_n:
             mine[mine_n:].zero_()            # padding of a short chunk: gathered, never used
-        # all-gather of equal (padded) chunks; they tile [0, n) in rank order
-        gathered = self._buf("gathered", G * chunk, torch.float32, reps[0])
-        self.dist.all_gather_into_tensor(gathered, mine, group=self.group)
-        out.copy_(gathered[:n])
+        # all-gather of equal (padded) chunks; they tile [0, n) in rank order,
+        # straight into the output when no chunk is padded
+        if G * chunk == n and out.is_contiguous():
+            self.dist.all_gather_into_tensor(out, mine, group=self.group)
+        else:
+            gathered = self._buf("gathered", G * chunk, torch.float32, reps[0])
+            self.dist.all_gather_into_tensor(gathered, mine, group=self.group)
+            out.copy_(gathered[:n])
 
 
 def sharded_hook(dist, replica_buffers, arena, group=None, dtype: str = "f32"):
@@ -169,6 +183,8 @@ def sharded_hook(dist, replica_buffers, arena, group=None, dtype: str = "f32"):
     reduce = ShardedAllReduce(dist, group, dtype)
     Wl = len(bufs)
 
+    streams = {}
+
     def hook(bucket, stream):
         if bucket.W != Wl:
             return 1                          # every rank holds Wl replicas; the others are the other ranks'
@@ -180,8 +196,11 @@ def sharded_hook(dist, replica_buffers, arena, group=None, dtype: str = "f32"):
             at = (int(bucket.replicas[r]) - t.data_ptr()) // t.element_size()
             local.append(t[at:at + n])
         res = (int(bucket.result) - arena.data_ptr()) // 4
-        st = torch.cuda.ExternalStream(int(stream), device=arena.device) if stream else \
-            torch.cuda.default_stream(arena.device)
+        key = int(stream or 0)
+        st = streams.get(key)
+        if st is None:
+            st = torch.cuda.ExternalStream(key, device=arena.device) if key else torch.cuda.default_stream(arena.device)
+            streams[key] = st
         with torch.cuda.stream(st):
             reduce(local, arena[res:res + n])
         return 0

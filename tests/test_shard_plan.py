@@ -113,6 +113,8 @@ def _rank(rank, world, port, dtype, cap, Wl):
         reduce = ShardedAllReduce(dist, None, dtype, mean=oracle_mean)
         lens = [sum(RAGGED[v] for v in m) for m in members]
         starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        if world == 2 and cap == 0:      # buckets gathered straight into the output and through padding
+            assert any(n and n % 16 == 0 for n in lens) and any(n % 16 for n in lens)
         for b in range(len(members)):            # bucket-index order on every rank
             local = [torch.from_numpy(m[b].view(np.int16)).view(torch.bfloat16) if dtype == "bf16"
                      else torch.from_numpy(m[b].copy()) for m in mine]
@@ -126,7 +128,7 @@ def _rank(rank, world, port, dtype, cap, Wl):
 
 
 @pytest.mark.parametrize("world,dtype,cap,Wl", [(2, "f32", 16 * 1024, 1), (3, "bf16", 8 * 1024, 1), (3, "f32", 0, 1),
-                                               (2, "f32", 16 * 1024, 2), (3, "f32", 8 * 1024, 2),
+                                               (2, "f32", 0, 1), (2, "f32", 16 * 1024, 2), (3, "f32", 8 * 1024, 2),
                                                (3, "bf16", 0, 2)])
 def test_sharded_allreduce_gloo_equals_unsharded_oracle(built, world, dtype, cap, Wl):
     import torch.multiprocessing as mp
