@@ -18,8 +18,10 @@ the 129 MB L2, so no flush is needed between steps.
 Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
 own independent replica of the workload (the W replicas of one emulation
 live on one GPU and need no collective: "replicas only"); value = total
-bytes over ranks / max time over ranks.  ``--sharded`` instead puts one
-replica on each rank and all-reduces every bucket across the ranks (NCCL).
+bytes over ranks / max time over ranks.  The same run then times the
+bucket all-reduce split across the N ranks (one replica per rank, NCCL) as
+``per_config["bert_large_sharded_allreduce"]``; ``--sharded`` times that
+alone as the main line (``--replicas-per-rank`` replicas on each rank).
 
 ``--impl reference`` times the CPU oracle (the plain NumPy restatement of the
 same path) on a bounded sample of the same workload on the host cores.
@@ -425,31 +427,16 @@ def run_gpt2_only(args):
     return 0
 
 
-def run_sharded(args):
-    """The bucket all-reduce across ranks that each hold Wl replicas
-    (--replicas-per-rank, default one; one rank per GPU under torchrun,
-    NCCL): every rank reduces its own BERT-large gradients (25 MiB buckets)
-    through the sharded hook -- per bucket, in bucket-index order, gather
-    into the bucket buffers, all-to-alls of the raw chunks, the owner's mean
-    in replica order, all-gather, copy-back.  Bytes per rank and step:
-    Wl*N*4 read + 2*N*4 written (the fused pass's algorithmic bytes at W =
-    Wl); value = those bytes over all ranks / the slowest rank's time (weak
-    scaling: per-rank work is fixed)."""
-    import torch
-    import torch.distributed as dist
-    from reduction_reducer_gb300.sharded import sharded_hook, verify_layout
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if world > 1 or "MASTER_ADDR" in os.environ:
-        dist.init_process_group("nccl", device_id=device)
-    else:
-        dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1, device_id=device)
-    stream = torch.cuda.Stream(device=device)
+def sharded_timing(torch, dist, device, rank, world, Wl, steps, warmup):
+    """Time the bucket all-reduce across the ranks of the default process
+    group, every rank holding Wl replicas of BERT-large (25 MiB buckets,
+    stored straggler order): per bucket, in bucket-index order, gather into
+    the bucket buffers, all-to-alls of the raw chunks, the owner's mean in
+    replica order, all-gather, copy-back.  Bytes per rank and step: Wl*N*4
+    read + 2*N*4 written (the fused pass's algorithmic bytes at W = Wl)."""
     from reduction_reducer_gb300 import Reducer
-    Wl = args.replicas_per_rank
+    from reduction_reducer_gb300.sharded import sharded_hook, verify_layout
+    stream = torch.cuda.Stream(device=device)
     numel = shapes.numels(shapes.bert_large())
     offs, total = gen.packed_offsets(numel, 64)
     flats = [gen.draw_flat_torch(total, rank * Wl + r, 0, "f32", device) for r in range(Wl)]
@@ -468,21 +455,49 @@ def run_sharded(args):
         red.mark_ready_many(order, stream)
 
     with torch.cuda.stream(stream):
-        ms, _, _ = time_steps(torch, stream, step, args.steps, args.warmup, dist if world > 1 else None)
+        ms, _, _ = time_steps(torch, stream, step, steps, warmup, dist if world > 1 else None)
     N = sum(numel)
     per_rank = Wl * N * 4 + 2 * N * 4
-    t = ms / args.steps
+    t = ms / steps
+    B = red.B
+    red.destroy()
+    del flats, grads, arena, out_flat, rbs
+    torch.cuda.empty_cache()
+    return {"gbs": round(per_rank * world / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4), "ranks": world,
+            "replicas_per_rank": Wl, "W": world * Wl, "P": len(numel), "N": N, "buckets": B,
+            "bytes_per_rank_step": per_rank,
+            "note": f"bucket all-reduce across {world} NCCL rank(s), {Wl} replica(s) each: all-to-all of raw "
+                    "chunks, owner mean, all-gather, in bucket order; gbs = bytes of all ranks / slowest rank"}
+
+
+def run_sharded(args):
+    """The bucket all-reduce across ranks that each hold Wl replicas
+    (--replicas-per-rank, default one; one rank per GPU under torchrun,
+    NCCL), timed by ``sharded_timing``; value = the bytes of all ranks / the
+    slowest rank's time (weak scaling: per-rank work is fixed)."""
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1 or "MASTER_ADDR" in os.environ:
+        dist.init_process_group("nccl", device_id=device)
+    else:
+        dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1, device_id=device)
+    r = sharded_timing(torch, dist, device, rank, world, args.replicas_per_rank, args.steps, args.warmup)
     if rank == 0:
         print(json.dumps({
-            "metric": METRIC, "value": round(per_rank * world / (t * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 4),
+            "metric": METRIC, "value": r["gbs"], "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": f"synthetic (seeded N(0,1e-3) gradients generated on the device, {Wl} replica(s) per rank)",
-            "config": {"workload": "bert_large", "W": world * Wl, "replicas_per_rank": Wl, "P": len(numel), "N": N,
-                       "cap_mib": 25, "buckets": red.B, "mode": "copy-back (n_out=1)",
+            "data": f"synthetic (seeded N(0,1e-3) gradients generated on the device, {r['replicas_per_rank']} "
+                    "replica(s) per rank)",
+            "config": {"workload": "bert_large", "W": r["W"], "replicas_per_rank": r["replicas_per_rank"],
+                       "P": r["P"], "N": r["N"], "cap_mib": 25, "buckets": r["buckets"], "mode": "copy-back (n_out=1)",
                        "parallelism": f"sharded all-reduce x{world} (all-to-all of raw chunks, owner mean, all-gather)",
-                       "bytes_per_rank_step": per_rank}}), flush=True)
-    red.destroy()
+                       "bytes_per_rank_step": r["bytes_per_rank_step"]}}), flush=True)
     dist.destroy_process_group()
     return 0
 
@@ -671,6 +686,11 @@ def run_ours(args):
     extra = {}
     if not args.no_extra:
         extra = extra_configs(torch, device, stream, args, dist, keep=wl)
+    if dist is not None and not args.no_extra:
+        # the same workload's bucket all-reduce split across the ranks (one
+        # replica per rank), beside the per-rank emulation timed above
+        extra["bert_large_sharded_allreduce"] = sharded_timing(
+            torch, dist, device, rank, world, 1, max(3, min(args.steps, 20)), max(3, args.warmup))
 
     e2e = None
     if not args.no_e2e:
