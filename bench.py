@@ -966,6 +966,13 @@ def extra_configs(torch, device, stream, args, dist, keep):
     # for the previous one (foreign work could sit between calls)
     keep.driver = "events"
     timed(keep, "bert_large_event_calls", "one mark_ready call per event (launches wait for their predecessor)")
+    # the same with calls chained (DDP_OPT_CHAINED: the caller guarantees that
+    # nothing else runs on the stream during the iteration)
+    from reduction_reducer_gb300 import _lib
+    keep.red.set_option(_lib.OPT_CHAINED, 1)
+    timed(keep, "bert_large_event_calls_chained",
+          "one mark_ready call per event, DDP_OPT_CHAINED = 1 (each launch follows its predecessor at once)")
+    keep.red.set_option(_lib.OPT_CHAINED, 0)
     keep.driver = "hooks"
     # BERT-large after a rebuild from the recorded (straggler) ready order,
     # first bucket capped at 1 MiB
@@ -997,7 +1004,6 @@ def extra_configs(torch, device, stream, args, dist, keep):
         timed(wl, f"gpt2_medium_w8_bf16_cap{cap}", f"GPT-2-medium bf16 W=8, cap {cap} MiB")
         if cap == 0:
             # the same per-gradient buckets with one launch per releasing event
-            from reduction_reducer_gb300 import _lib
             wl.red.set_option(_lib.OPT_COALESCE_ELEMS, 0)
             timed(wl, "gpt2_medium_w8_bf16_cap0_launch_per_event",
                   "GPT-2-medium bf16 W=8, cap 0, DDP_OPT_COALESCE_ELEMS = 0: one launch per releasing event")
@@ -1008,6 +1014,9 @@ def extra_configs(torch, device, stream, args, dist, keep):
             timed(wl, f"gpt2_medium_w8_bf16_cap{cap}_event_calls",
                   f"GPT-2-medium bf16 W=8, cap {cap} MiB, one mark_ready call per event (launches wait for their "
                   "predecessor)")
+            wl.red.set_option(_lib.OPT_CHAINED, 1)
+            timed(wl, f"gpt2_medium_w8_bf16_cap{cap}_event_calls_chained",
+                  f"GPT-2-medium bf16 W=8, cap {cap} MiB, one mark_ready call per event, DDP_OPT_CHAINED = 1")
         wl.free()
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
