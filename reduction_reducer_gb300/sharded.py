@@ -36,10 +36,12 @@ def verify_layout(dist, red, group=None, device=None):
     the sizes are compared across processes with a MIN and a MAX all-reduce
     before training starts): every rank of ``group`` must hold the same
     bucket layout -- parameter count, dtype, bucket count, arena size and the
-    bucket offsets and members -- since the buckets' collectives must pair
-    up in bucket order on every rank.  Raises RuntimeError naming what
-    differs.  ``device``: where the all-reduced tensor lives (default: cuda
-    for the NCCL backend, cpu otherwise)."""
+    bucket offsets and members -- and, once bound, the same number of
+    replicas, since the buckets' collectives must pair up in bucket order on
+    every rank and carry equal shares (so call it at the same point on every
+    rank: before ``bind`` everywhere or after it everywhere).  Raises
+    RuntimeError naming what differs.  ``device``: where the all-reduced
+    tensor lives (default: cuda for the NCCL backend, cpu otherwise)."""
     import hashlib
     import torch
     B, offs = red.get_bucket_info()
