@@ -64,7 +64,8 @@ def draw_sizes(rng, P):
 @pytest.mark.parametrize("seed", range(60))
 def test_fuzz_unused_parameters(seed):
     """Random local-use masks (some variables unused on every replica, whose
-    copy-backs must stay untouched) over random layouts, W up to 64."""
+    copy-backs must stay untouched) over random layouts, W up to 64, driven
+    in one mark_ready_many call or one mark_ready call per event."""
     import torch
     from oracle.buckets import assign_buckets
     from oracle.unused import globally_used, reduce_with_unused
@@ -77,7 +78,8 @@ def test_fuzz_unused_parameters(seed):
     W = int(rng.choice([1, 2, 3, 4, 8, 16, 33, 64]))
     dtype = "f32" if rng.random() < 0.5 else "bf16"
     cap = int(rng.choice(CAPS))
-    kernel = str(rng.choice(["ldg", "tma"]))
+    kernel = str(rng.choice(["ldg", "tma", "auto"]))
+    per_event = bool(seed % 3 == 2)
     n_out = int(rng.choice([1, W]))
     used = rng.random((W, P)) < float(rng.choice([0.3, 0.7, 0.95]))
     if not used.any():              # with no gradient anywhere no ready event occurs and nothing is reduced
@@ -96,7 +98,11 @@ def test_fuzz_unused_parameters(seed):
     red.begin_iteration()
     g = globally_used(used.tolist())
     order = [int(v) for v in rng.permutation(P) if g[v]]
-    assert red.mark_ready_many(order) == len(order)
+    if per_event:
+        for v in order:
+            red.mark_ready(v)
+    else:
+        assert red.mark_ready_many(order) == len(order)
     torch.cuda.synchronize()
     assert red.device_status() == 0
     got = arena.cpu().numpy()

@@ -40,7 +40,7 @@ def _built():
 
 def _reducer(numel, dtype, cap, kernel):
     red = Reducer(numel, dtype, cap)
-    red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_TMA if kernel == "tma" else _lib.KERNEL_LDG)
+    red.set_option(_lib.OPT_KERNEL, {"tma": _lib.KERNEL_TMA, "ldg": _lib.KERNEL_LDG, "auto": _lib.KERNEL_AUTO}[kernel])
     red.set_option(_lib.OPT_FIND_UNUSED, 1)
     return red
 
