@@ -365,7 +365,12 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream, int tma_waves
     if (st != DDP_OK) return st;
     const ddpk::InType in = c->dtype == DDP_F32 ? ddpk::IN_F32 : ddpk::IN_BF16;
     ddpk::LaunchCfg cfg = c->cfg;
+    // One replica reads a third of what it writes (bucket and copy-back), and
+    // its bulk-copy launches do best as one resident wave of long slices
+    // (GB300, BERT-large shapes, one mark_ready_many call: 6,779 against 6,475
+    // GB/s with two waves; one CTA per SM 6,574).
     if (tma_waves > 0) cfg.tma_waves = tma_waves;
+    else if (c->W == 1) cfg.tma_waves = 1;
     // the iteration's final launch has no successor to overlap its tail
     cfg.last = b1 == c->B ? 1 : 0;
     // Chained launches: a launch that directly follows this iteration's
