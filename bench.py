@@ -510,7 +510,6 @@ def run_mix_rates(args):
     The pass at W replicas reads W and writes 2 units per element: at W = 4
     it has the 2:1 mix of torch.add."""
     import torch
-    from reduction_reducer_gb300 import Reducer
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
 
@@ -541,12 +540,25 @@ def run_mix_rates(args):
         out[name] = {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 3)}
     del x, y, z
     torch.cuda.empty_cache()
+    stream = torch.cuda.Stream(device=dev)
+    for W, r in replica_sweep(torch, dev, stream, (1, 2, 4, 8, 16, 32), args.steps, args.warmup).items():
+        out[f"fused pass, BERT-large shapes, W={W} ({W} reads : 2 writes)"] = r
+    print(json.dumps({"mix_rates": out}), flush=True)
+    return 0
+
+
+def replica_sweep(torch, dev, stream, Ws, steps, warmup, dist=None):
+    """The fused pass on the BERT-large shapes (fp32, 25 MiB buckets, reverse
+    order, library defaults, one mark_ready_many call, one copy-back) for
+    each replica count in Ws: {W: {"gbs", "ms"}} of its algorithmic bytes
+    (W reads and 2 writes per element)."""
+    from reduction_reducer_gb300 import Reducer
     numel = shapes.numels(shapes.bert_large())
     offs, total = gen.packed_offsets(numel, 64)
     order = gen.reverse_order(len(numel))
-    stream = torch.cuda.Stream(device=dev)
     N = sum(numel)
-    for W in (1, 2, 4, 8, 16, 32):
+    out = {}
+    for W in Ws:
         flat = [gen.draw_flat_torch(total, r, 0, "f32", dev) for r in range(W)]
         grads = [[f[o:o + k] for o, k in zip(offs, numel)] for f in flat]
         red = Reducer(numel, "f32", 25 * MIB)
@@ -558,15 +570,13 @@ def run_mix_rates(args):
             red.begin_iteration()
             red.mark_ready_many(order, stream)
         with torch.cuda.stream(stream):
-            ms, _, _ = time_steps(torch, stream, step, args.steps, args.warmup)
-        t = ms / args.steps
-        out[f"fused pass, BERT-large shapes, W={W} ({W} reads : 2 writes)"] = {
-            "gbs": round(view_bytes(W, N, 4) / (t * 1e-3) / 1e9, 1), "ms": round(t, 4)}
+            ms, _, _ = time_steps(torch, stream, step, steps, warmup, dist)
+        t = ms / steps
+        out[W] = {"gbs": round(view_bytes(W, N, 4) / (t * 1e-3) / 1e9, 1), "ms": round(t, 4)}
         red.destroy()
         del flat, grads, arena, res
         torch.cuda.empty_cache()
-    print(json.dumps({"mix_rates": out}), flush=True)
-    return 0
+    return out
 
 
 def run_trace(args):
@@ -1020,6 +1030,15 @@ def extra_configs(torch, device, stream, args, dist, keep):
         wl.free()
         torch.cuda.empty_cache()
     out["nosync_resnet50_w16_k8"] = nosync_config(torch, device, stream, steps, warm, dist)
+    # the replica count on the BERT-large shapes (reverse order; the headline
+    # iteration is W = 4 with the stored straggler order)
+    sweep = replica_sweep(torch, device, stream, (1, 2, 4, 8, 16, 32), min(steps, 30), warm, dist)
+    for W, r in sweep.items():
+        out[f"bert_large_shapes_w{W}"] = {
+            "gbs": r["gbs"], "ms_per_step": r["ms"], "W": W,
+            "pct_of_w8": round(100 * r["gbs"] / sweep[8]["gbs"], 1),
+            "note": f"BERT-large shapes, W={W} fp32 ({W} reads : 2 writes per element), reverse order, one "
+                    "mark_ready_many call"}
     # whole iterations captured in a CUDA graph (launch-bound layouts)
     for name, cap in (("gpt2_medium", 0), ("bert_large", 25)):
         wl = Workload(name, torch, device, cap, n_out=1, driver="hooks")
