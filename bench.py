@@ -968,6 +968,25 @@ def extra_configs(torch, device, stream, args, dist, keep):
     wl = Workload("linear", torch, device, 25, n_out=1, driver="events")
     timed(wl, "linear_w2", "Linear(10,10), W=2, one mark_ready call per event; latency-bound (one launch)")
     out["linear_w2"]["us_per_step"] = round(out["linear_w2"]["ms_per_step"] * 1e3, 2)
+    # the same iteration's GPU latency without the host calls in between: 100
+    # iterations (begin_iteration + two mark_ready calls each) captured in one
+    # CUDA graph, replayed
+    with torch.cuda.stream(stream):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(100):
+                wl.step(stream)
+    reps = max(3, steps // 20)
+    with torch.cuda.stream(stream):
+        ms, _, _ = time_steps(torch, stream, g.replay, reps, warm, dist)
+    out["linear_w2_graph"] = {"us_per_step": round(ms * 1e3 / (reps * 100), 2), "W": wl.W, "buckets": wl.B,
+                              "kernel": kernel_name(wl),
+                              "note": "Linear(10,10), W=2: 100 iterations of one mark_ready call per event captured "
+                                      "in one CUDA graph and replayed (GPU latency of a one-launch iteration)"}
+    del g
     wl.free()
     # BERT-large, one launch over all buckets (kernel alone)
     keep.driver = "all"
