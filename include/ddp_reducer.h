@@ -101,7 +101,10 @@ int ddp_get_bucket_info(const ddp_ctx* ctx, int32_t* B, int64_t* bucket_offsets)
  *                copied back; n_out = 1 writes one shared copy; n_out = W
  *                writes every replica's copy.
  * Builds the device segment table (library-owned, freed by ddp_destroy or the
- * next bind).  Synchronous.  Pointers must stay valid while bound.
+ * next bind).  Synchronous.  Pointers must stay valid while bound.  Any W >= 1
+ * reduces; the bulk-copy kernel holds up to 7,260 streams (W, or 2W with a
+ * bound last step), so with more the automatic kernel choice streams through
+ * registers and an explicit bulk-copy choice fails its launches (CUDA).
  * Errors: INVALID_ARG (W < 1, NULL pointers, misaligned arena, n_out not in
  * {0, 1, W}), CUDA, NO_MEMORY. */
 int ddp_bind(ddp_ctx* ctx, int32_t W, const void* const* grads, float* bucket_arena,
@@ -339,7 +342,7 @@ int ddp_bind_last_step(ddp_ctx* ctx, const void* const* g_last);
  *     race on it.  Calls on one stream are ordered and safe.
  *   - Launch shape: always the bulk-copy kernel with 3 stages of 32 KiB and
  *     one CTA per SM; the context's launch options (ddp_set_option) are not
- *     used.
+ *     used.  W is at most 7,260 (the ring's streams); more fail with CUDA.
  *   - The status word of the kernel's bounded waits lives in the shared array
  *     and is not reported: ddp_get_device_status reads a bound context's own
  *     word, not this one.

@@ -391,6 +391,13 @@ int launch_range(ddp_ctx* c, int32_t b0, int32_t b1, void* stream, int tma_waves
     // first launch followed by chained register-streaming launches cost
     // GPT-2-medium at cap 0 17 % (7.14 -> 5.94 TB/s).
     if (c->opt_kernel == ddpk::KERNEL_AUTO && c->event_call && !c->opt_chain) cfg.kernel = ddpk::KERNEL_TMA;
+    // The bulk-copy ring holds two stages of at least 16 bytes per stream
+    // (one per replica, two with a bound last step) in the 227 KiB of shared
+    // memory a CTA can have; past that the automatic choice streams through
+    // registers (an explicit bulk-copy choice fails the launch).
+    constexpr int64_t kTmaMaxStreams = (227 * 1024 - 128) / (2 * 16);
+    if (c->opt_kernel == ddpk::KERNEL_AUTO && static_cast<int64_t>(c->W) * (c->tab.add ? 2 : 1) > kTmaMaxStreams)
+        cfg.kernel = ddpk::KERNEL_LDG;
     // A built-in hook's arithmetic is the fused pass's (the default hook) or
     // the fused pass with every replica value rounded to bf16 first (the
     // compression hook): it runs inside the one-pass kernel, with nothing

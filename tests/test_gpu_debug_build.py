@@ -77,7 +77,7 @@ def _reduce_case(numel, W, dtype, cap, kernel, mode, odd=False, n_out=1):
 @pytest.mark.parametrize("kernel", ["ldg", "tma"])
 @pytest.mark.parametrize("mode", ["mark_ready_many", "reduce_all"])
 @pytest.mark.parametrize("W,dtype,odd", [(3, "f32", False), (4, "f32", True), (8, "bf16", False), (5, "bf16", True),
-                                         (16, "f32", False)])
+                                         (16, "f32", False), (256, "f32", True), (256, "bf16", False)])
 def test_debug_build_reduce(W, dtype, odd, kernel, mode):
     _reduce_case(RAGGED, W, dtype, 16 * 1024, kernel, mode, odd=odd, n_out=W if W == 4 else 1)
 

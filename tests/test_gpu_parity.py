@@ -190,11 +190,35 @@ def test_ragged_every_W(W, dtype, kernel):
 
 @pytest.mark.parametrize("kernel", ["ldg", "tma"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("W", [32, 64])
+@pytest.mark.parametrize("W", [32, 64, 100, 256])
 def test_many_replicas(W, dtype, kernel):
-    """W beyond the compiled-in widths: the generic replica loop."""
+    """W beyond the compiled-in widths: the generic replica loop; from W = 100
+    on, the bulk-copy ring no longer fits 4 KiB per stream and its tiles
+    shrink (256 streams: 2 stages of 112-element tiles)."""
     numel = [3, 4097, 0, 70001, 16, 1000]
     full_compare(numel, W, dtype, cap=32 * 1024, order="random", n_out=1, kernel=kernel)
+
+
+@pytest.mark.parametrize("mode", ["mark_ready", "mark_ready_many"])
+def test_more_replicas_than_the_bulk_copy_ring_holds(mode):
+    """7,300 replicas: more streams than the bulk-copy ring has room for
+    (7,260).  The automatic kernel choice streams them through registers,
+    bit for bit; an explicit bulk-copy choice fails its launch with a CUDA
+    status before anything runs, and the device stays usable."""
+    from reduction_reducer_gb300 import CudaError
+    numel = [16, 5, 33]
+    full_compare(numel, 7300, "f32", cap=1 << 20, order="random", n_out=1, mode=mode, kernel="auto")
+    flats, views, offs = host_grads(numel, 7300, "f32")
+    _, grads_dev = host_to_device_views(flats, numel, offs, "f32", DEV)
+    red = Reducer(numel, "f32", 1 << 20)
+    red.set_option(_lib.OPT_KERNEL, _lib.KERNEL_TMA)
+    arena = torch.zeros(red.arena_numel(), device=DEV)
+    red.bind(grads_dev, arena, None)
+    red.begin_iteration()
+    with pytest.raises(CudaError):
+        red.mark_ready_many([2, 1, 0])
+    red.destroy()
+    full_compare(numel, 3, "f32", cap=1 << 20, order="random", n_out=1, kernel="tma")
 
 
 # Launch shapes other than the defaults: ring depth and stage bytes (a 112 KiB
