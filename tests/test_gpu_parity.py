@@ -352,6 +352,18 @@ def test_bind_rejects_misaligned_arena():
         red.bind(g, buf[1:], None)
 
 
+@pytest.mark.parametrize("mode", ["mark_ready", "mark_ready_many"])
+@pytest.mark.parametrize("cap", [0, 1 << 20])
+def test_many_small_parameters(cap, mode):
+    """20,000 parameters of 0-40 elements: a segment table of ~19,500
+    entries that every CTA searches; per-gradient buckets (cap 0: one bucket
+    per parameter, one launch per event, or coalesced runs in one call) and
+    1 MiB buckets."""
+    rng = np.random.default_rng(20_000)
+    numel = [int(x) for x in rng.integers(0, 41, size=20_000)]
+    full_compare(numel, 4, "f32", cap=cap, order="random", n_out=1, mode=mode, kernel="auto")
+
+
 def test_empty_and_zero_length_models():
     red = Reducer([], "f32", 25 * MIB)
     red.bind([[]], torch.zeros(4, device=DEV), None)

@@ -210,3 +210,45 @@ def test_unused_bert_large_full_size_every_element():
             assert bits_equal(got[offs[v]:offs[v] + n], want_outs[0][v]), (v, first_mismatch(got[offs[v]:offs[v] + n], want_outs[0][v]))
     assert not torch.isnan(arena).any()
     red.destroy()
+
+
+@pytest.mark.parametrize("kernel", ["ldg", "tma", "auto"])
+@pytest.mark.parametrize("per_event", [False, True])
+def test_unused_more_segments_than_one_launch_holds(kernel, per_event):
+    """9,000 small parameters in one bucket with unused tracking on: the
+    replicas' local-use masks travel in the launch's parameter block, at
+    most 3,840 segments per launch, so the bucket goes out as three chained
+    launches; every element and every untouched copy-back against the
+    oracle."""
+    rng = np.random.default_rng(9000)
+    P, W = 9000, 3
+    numel = [int(x) for x in rng.integers(0, 41, size=P)]
+    used = rng.random((W, P)) < 0.8
+    used[:, ::97] = False                 # some unused on every replica
+    flats, views, offs = host_grads(numel, W, "f32")
+    cap = 64 * MIB
+    members, locs = assign_buckets(numel, 4, cap)
+    assert len(members) == 1
+    want_arena, want_outs = reduce_with_unused(views, used.tolist(), members, locs, numel, n_out=1)
+    _, grads_dev = host_to_device_views(flats, numel, offs, "f32", DEV)
+    red = _reducer(numel, "f32", cap, kernel)
+    arena = torch.full((red.arena_numel(),), float("nan"), device=DEV)
+    bufs, out_views, out_offs = _guarded_outputs(numel, 1)
+    red.bind(grads_dev, arena, out_views[0])
+    red.set_local_used(used.tolist())
+    red.begin_iteration()
+    g = globally_used(used.tolist())
+    order = [int(v) for v in rng.permutation(P) if g[v]]
+    if per_event:
+        for v in order:
+            red.mark_ready(v)
+    else:
+        assert red.mark_ready_many(order) == len(order)
+    torch.cuda.synchronize()
+    assert red.device_status() == 0
+    assert red.launch_count() >= 3
+    got = arena.cpu().numpy()
+    assert bits_equal(got, want_arena), first_mismatch(got, want_arena)
+    _check_outputs(bufs, out_offs, numel, want_outs, used.tolist())
+    red.destroy()
+
