@@ -343,8 +343,15 @@ __device__ __forceinline__ void copy_run(const char* from, char* to, long long a
     const long long sc_end = vec && kb < ke ? kb * n : e;
     for (long long a = x + threadIdx.x; a < sc_end; a += blockDim.x)
         copy_elem(to + (a - a0) * elem, from + (a - a0) * elem, elem);
-    // four independent 16-byte vectors per thread in flight
-    constexpr int UC = 4;
+    // UC independent 16-byte vectors per thread in flight.  One: at 32
+    // registers eight 256-thread CTAs fit per SM and the warps keep the loads
+    // in flight (GB300, BERT-large W=4 through the gathered hook route:
+    // 2,499 -> 2,594 GB/s against four vectors at 80 registers and three
+    // CTAs per SM; two and three vectors in between).
+#ifndef DDP_COPY_UNROLL
+#define DDP_COPY_UNROLL 1
+#endif
+    constexpr int UC = DDP_COPY_UNROLL;
     const long long step = blockDim.x;
     for (long long k = kb + threadIdx.x; k < ke; k += UC * step) {
         float4 v[UC];
