@@ -7,13 +7,12 @@ gradients; the last micro-step's gradients are bound with
 leaves the accumulated fields as they were.
 """
 
-import numpy as np
 import pytest
 import torch
 
 from oracle.buckets import assign_buckets
 from oracle.nosync import accumulate, accumulate_steps, reduce_last_step
-from oracle.reduce import reduce_buckets, replica_mean
+from oracle.reduce import reduce_buckets
 from reduction_reducer_gb300 import InvalidArg, Reducer, _lib
 from workloads import gen, shapes
 

@@ -22,7 +22,7 @@ import torch
 
 from oracle.buckets import assign_buckets
 from oracle.nosync import accumulate_steps
-from oracle.reduce import reduce_buckets, replica_mean
+from oracle.reduce import reduce_buckets
 from reduction_reducer_gb300 import InvalidArg, Reducer, _lib
 from workloads import gen, shapes
 

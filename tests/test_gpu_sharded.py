@@ -23,7 +23,7 @@ from oracle.reduce import reduce_buckets, replica_mean
 from reduction_reducer_gb300 import Reducer, _lib
 from workloads import gen, shapes
 
-from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views, to_host
+from gpu_util import bits_equal, first_mismatch, host_grads, host_to_device_views
 
 pytestmark = pytest.mark.gpu
 

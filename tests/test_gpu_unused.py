@@ -13,7 +13,6 @@ import pytest
 import torch
 
 from oracle.buckets import assign_buckets
-from oracle.reduce import replica_mean
 from oracle.unused import accumulate_masked, globally_used, reduce_with_unused
 from reduction_reducer_gb300 import AlreadyReady, Reducer, _lib
 from workloads import gen, shapes

@@ -3,7 +3,6 @@
 import itertools
 
 import numpy as np
-import pytest
 
 from oracle.buckets import assign_buckets
 from oracle.readiness import launch_events
