@@ -982,8 +982,9 @@ int ddp_reduce_all(ddp_ctx* c, void* stream) {
     }
     c->next = c->B;
     finish_iteration(c);
-    // one launch over the whole remaining iteration: eight resident waves of
-    // the bulk-copy kernel shorten its tail (two suit the shorter launches of
+    // one launch over the whole remaining iteration: at least eight resident
+    // waves of the bulk-copy kernel, more while every CTA keeps ten stages
+    // (launch_reduce_tma), shorten its tail (two suit the shorter launches of
     // a readiness-driven iteration).  GB300, BERT-large W=4: 6,967 GB/s with
     // four waves, 7,012 with six, 7,041 with eight; ResNet-50 W=8 +0.2 %.
     return launch_range(c, first, c->B, stream, 8);

@@ -55,6 +55,8 @@ constexpr long long kPrefetchStages = DDP_PREFETCH_STAGES;   // stages prefetche
 constexpr int kPrefetchWaves = DDP_PREFETCH_WAVES;            // waves of CTAs that prefetch (0: every CTA)
 constexpr long long kLastMinStages = 8;   // stages per CTA that size an iteration's final launch
 constexpr long long kAccLastMinStages = 4;   // ... and the last accumulate launch of a call
+constexpr long long kWholeMinStages = 10;   // ... and the single launch of ddp_reduce_all
+constexpr long long kWholeMaxWaves = 64;    // its most resident waves
 
 // Launch trace (builds with -DDDP_TRACE only; ddp_read_launch_trace): per
 // launch of the bucket pass, per CTA, four %globaltimer stamps -- entry, past
@@ -664,7 +666,8 @@ int resident_ctas(K k, long long smem) {
 // against one CTA per SM: BERT-large W=4 7.05 -> 7.12 TB/s, GPT-2-medium at
 // cap 25 and 100 +1.6 / +1.3 %, ResNet-50 W=8 +0.7 %, no_sync ResNet-50 W=16
 // micro-steps +6 %.  A single launch over a whole iteration (reduce_all)
-// takes eight: BERT-large 6.78 (one wave) -> 6.97 (four) -> 7.07 TB/s.
+// takes at least eight (BERT-large 6.78 (one wave) -> 6.97 (four) -> 7.07
+// TB/s), more when its slices stay long (see launch_reduce_tma).
 template <typename K>
 int tma_ctas(const LaunchCfg& cfg, K k, long long smem) {
     const int waves = cfg.tma_waves > 0 ? cfg.tma_waves : 2;
@@ -804,10 +807,19 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     // +0.45 %, GPT-2-medium caps 25 / 100 +1.3 / +1.6 %; ResNet-50 W=8 (a
     // 4.3M-element last bucket: two waves either way) unchanged.  At least
     // four stages per CTA cost ResNet-50 1 %, sixteen gained less.
-    if (cfg.last && cfg.tma_ctas_per_sm == 0 && cfg.tma_waves <= 2) {
-        const long long per_cta = kLastMinStages * tile;
+    // ddp_reduce_all's single launch over the whole iteration (cfg.tma_waves
+    // above two) likewise takes eight to 64 waves, as many as leave every CTA
+    // kWholeMinStages stages: GB300, against eight waves, BERT-large W=4
+    // 7,043 -> 7,156 GB/s at 48 waves (11 stages per CTA), GPT-2-medium at
+    // cap 25 6,972 -> 7,171 at 64 (9 stages), ResNet-50 W=8 best at 8-12
+    // (7-10 stages) and 12 % slower at 32 waves (3 stages).
+    if (cfg.last && cfg.tma_ctas_per_sm == 0) {
+        const bool whole = cfg.tma_waves > 2;
+        const long long lo_w = whole ? cfg.tma_waves : 2;
+        const long long hi_w = whole ? kWholeMaxWaves : 8;
+        const long long per_cta = (whole ? kWholeMinStages : kLastMinStages) * tile;
         long long waves = (hi - lo) / (static_cast<long long>(p.first_wave) * per_cta);
-        waves = waves < 2 ? 2 : waves > 8 ? 8 : waves;
+        waves = waves < lo_w ? lo_w : waves > hi_w ? hi_w : waves;
         per_sm = static_cast<int>(waves) * resident;
     }
 
