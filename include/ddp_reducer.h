@@ -404,11 +404,11 @@ enum ddp_option {
     DDP_OPT_STAGE_BYTES = 6,      /* bulk-copy kernel: bytes of one stage, all W tiles (default 32 KiB);
                                      raised to 4 KiB per tile for many streams (W > 8, or W > 4 with
                                      a bound last step) */
-    DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernels: CTAs per SM, 1..8, or 0 (default): two resident
-                                     waves, one for a single replica (W = 1); an iteration's final
-                                     launch up to eight, as many as leave every CTA eight stages of
-                                     work; the single launch of ddp_reduce_all eight to 64, as many as
-                                     leave every CTA ten stages */
+    DDP_OPT_TMA_CTAS_PER_SM = 7,  /* bulk-copy kernels: CTAs per SM, 1..8, or 0 (default): resident
+                                     waves sized by the launch's slices -- two, or up to 64 while every
+                                     CTA keeps ten stages of work; one for a single replica (W = 1); an
+                                     iteration's final launch two to eight, as many as leave every CTA
+                                     eight stages; the single launch of ddp_reduce_all eight to 64 */
     DDP_OPT_AUTO_MIN_ELEMS = 8,   /* kernel 2: median bucket length (elements) from which the bulk-copy
                                      kernel is used (default 6 x 2^20) */
     DDP_OPT_CHAINED = 9,          /* 1: chained launches (default 0).  The caller guarantees that every

@@ -812,15 +812,26 @@ cudaError_t launch_reduce_tma(const SegTable& t, InType in, int W, int n_out, fl
     // kWholeMinStages stages: GB300, against eight waves, BERT-large W=4
     // 7,043 -> 7,156 GB/s at 48 waves (11 stages per CTA), GPT-2-medium at
     // cap 25 6,972 -> 7,171 at 64 (9 stages), ResNet-50 W=8 best at 8-12
-    // (7-10 stages) and 12 % slower at 32 waves (3 stages).
-    if (cfg.last && cfg.tma_ctas_per_sm == 0) {
-        const bool whole = cfg.tma_waves > 2;
-        const long long lo_w = whole ? cfg.tma_waves : 2;
-        const long long hi_w = whole ? kWholeMaxWaves : 8;
-        const long long per_cta = (whole ? kWholeMinStages : kLastMinStages) * tile;
-        long long waves = (hi - lo) / (static_cast<long long>(p.first_wave) * per_cta);
-        waves = waves < lo_w ? lo_w : waves > hi_w ? hi_w : waves;
-        per_sm = static_cast<int>(waves) * resident;
+    // (7-10 stages) and 12 % slower at 32 waves (3 stages).  Other launches
+    // keep two waves unless their slices would exceed kWholeMinStages stages
+    // (GPT-2-medium's 100 MiB buckets: 7,127 -> 7,166 GB/s; buckets of 25 MiB
+    // and less keep two waves).
+    if (cfg.tma_ctas_per_sm == 0) {
+        // Grids sized by their slices: as many resident waves, within
+        // [lo_w, hi_w], as leave every CTA min_st stages of work.
+        long long lo_w = 0, hi_w = 0, min_st = 0;
+        if (cfg.last && cfg.tma_waves > 2) {          // ddp_reduce_all: the whole iteration
+            lo_w = cfg.tma_waves, hi_w = kWholeMaxWaves, min_st = kWholeMinStages;
+        } else if (cfg.last) {                        // an iteration's final launch
+            lo_w = 2, hi_w = 8, min_st = kLastMinStages;
+        } else if (cfg.tma_waves == 2) {              // any other launch (not W = 1's single wave)
+            lo_w = 2, hi_w = kWholeMaxWaves, min_st = kWholeMinStages;
+        }
+        if (hi_w > 0) {
+            long long waves = (hi - lo) / (static_cast<long long>(p.first_wave) * min_st * tile);
+            waves = waves < lo_w ? lo_w : waves > hi_w ? hi_w : waves;
+            per_sm = static_cast<int>(waves) * resident;
+        }
     }
 
     const long long span = hi - p.base;
