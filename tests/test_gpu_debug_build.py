@@ -89,6 +89,16 @@ def test_debug_build_gpt2_reduced(kernel, cap_mib):
     _reduce_case(numel, 8, "bf16", cap_mib * MIB, kernel, "mark_ready_many")
 
 
+@pytest.mark.parametrize("mode", ["mark_ready_many", "reduce_all"])
+def test_debug_build_large_buckets(mode):
+    """GPT-2-medium with 8 layers in 100 MiB buckets (54.6M and 98.7M bf16
+    elements): the first bucket's bulk-copy launch gets eight resident
+    waves (sized by its slices), the final one eight, and the single
+    reduce_all launch 24."""
+    numel = shapes.numels(shapes.gpt2_medium(layers=8))
+    _reduce_case(numel, 8, "bf16", 100 * MIB, "tma", mode)
+
+
 @pytest.mark.parametrize("kernel", ["ldg", "tma"])
 def test_debug_build_nosync_and_last_step(kernel):
     numel = RAGGED
