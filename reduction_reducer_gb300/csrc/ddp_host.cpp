@@ -94,8 +94,8 @@ struct ddp_ctx {
     // Defaults from the GB300 sweeps: the kernel is chosen per context from
     // the median bucket length (bulk-copy pipeline with 3 stages of 32 KiB
     // from 6 x 2^20 elements up, register streaming below).  Both kernels
-    // launch more CTAs than fit at once (two resident waves for bulk copy,
-    // three for register streaming): SMs that finish a slice early take
+    // launch more CTAs than fit at once (two or more resident waves for bulk
+    // copy, three for register streaming): SMs that finish a slice early take
     // another, so a launch ends with a short tail and consecutive launches
     // interleave.  One kernel for all launches of a context, so consecutive
     // launches can overlap (one call per ready event, where every launch
@@ -103,7 +103,7 @@ struct ddp_ctx {
     int opt_kernel = ddpk::KERNEL_AUTO;
     int opt_stages = 3;
     int opt_stage_bytes = 32 * 1024;
-    int opt_tma_ctas = 0;           // 0: two resident waves
+    int opt_tma_ctas = 0;           // 0: resident waves sized by the launch (two by default)
     long long opt_auto_min = 6LL << 20;
     bool opt_chain = false;
     // Within one ddp_mark_ready_many call, consecutive released bucket runs
@@ -1143,7 +1143,7 @@ int ddp_set_option(ddp_ctx* c, int32_t option, int64_t value) {
             return refresh_launch_cfg(c);
         case DDP_OPT_TMA_CTAS_PER_SM:
             if (value < 0 || value > 8)
-                return fail(c, DDP_ERR_INVALID_ARG, "bulk-copy CTAs per SM must be 0 (two resident waves) .. 8");
+                return fail(c, DDP_ERR_INVALID_ARG, "bulk-copy CTAs per SM must be 0 (resident waves sized by the launch) .. 8");
             c->opt_tma_ctas = static_cast<int>(value);
             return refresh_launch_cfg(c);
         case DDP_OPT_BLOCK_THREADS:
